@@ -89,6 +89,8 @@ def test_tree_matches_brute_force_trie(seed):
             assert slots.tolist() == [brute.slot[tuple(toks[: i + 1])] for i in range(n)]
             if n:
                 match_ends.add(tuple(toks[:n]))
+                # a match that ends inside an edge splits it: its end is a node boundary
+                assert tuple(toks[:n]) in set(_present_paths(tree)[1].values())
             if rnd.random() < 0.3:
                 tree.lock(node)
                 locked.append((node, tuple(toks[:n])))
@@ -306,3 +308,23 @@ def test_duplicate_insert_in_one_batch_frees_the_later_copy():
     n, slots, _ = sim.tree.match(b)
     assert n == 5 and slots[:4].tolist() == r.rows[0][:4].tolist()
     assert sim.pool.available() == 50 - 6
+
+
+def test_lock_protects_exactly_the_matched_prefix():
+    """Reference counts protect what a running request uses (paper digest Sec. 3: only nodes
+    with count 0 are freed). A match that ends inside an edge locks exactly the matched tokens:
+    the rest of that edge is unreferenced and can go."""
+    pool = oracle.Pool(100)
+    tree = oracle.Tree(pool)
+    seq = [3, 1, 4, 1, 5, 9, 2, 6]
+    tree.insert(seq, pool.alloc(len(seq)))
+    n, slots, node = tree.match([3, 1, 4, 7])
+    assert n == 3
+    tree.lock(node)
+    ok, freed, _ = tree.evict(100)
+    assert not ok and freed == 5
+    held, _ = _present_paths(tree)
+    assert set(held) == {(3,), (3, 1), (3, 1, 4)}
+    tree.unlock(node)
+    ok, freed, _ = tree.evict(3)
+    assert ok and freed == 3 and pool.available() == 100
