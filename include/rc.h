@@ -1,0 +1,255 @@
+/*
+ * rc.h -- C ABI of the prefix-cached paged attention library (librc).
+ *
+ * The library implements the data path of RadixAttention (SGLang, "Efficient Execution of
+ * Structured Language Model Programs", arXiv 2312.07104): KV caches of all requests live in one
+ * pool of token-sized pages; a radix tree over token sequences finds each request's longest
+ * cached prefix, whose KV is reused, so only the unmatched suffix is computed; finished
+ * sequences are inserted back; unreferenced leaves are evicted in LRU order when the pool runs
+ * short.
+ *
+ * Conventions
+ *   - Every function returns an int status: RC_OK (0) or a negative RC_ERR_* code. The message
+ *     of the last failure on the calling thread is available from rc_last_error().
+ *   - The caller owns every buffer. Pointers documented as "device" point to GPU memory of the
+ *     current CUDA device; "host" pointers to CPU memory. The library allocates no device memory;
+ *     decode attention takes an explicit caller-provided workspace.
+ *   - Device entry points are asynchronous on the given stream (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream), never synchronise, and report launch failures as
+ *     RC_ERR_CUDA. Kernels that detect bad data (a slot index out of range, a length beyond the
+ *     slot-table row, an expired wait) set a device status word and skip the access instead of
+ *     trapping; rc_device_status() reads and clears it.
+ *   - Pool and tree objects are not thread-safe: one scheduler thread drives them.
+ *   - Layouts are row-major and contiguous. T = total new tokens of an extend batch, B = requests,
+ *     Hq / Hkv = query / KV heads (Hq % Hkv == 0; query head h reads KV head h / (Hq / Hkv)),
+ *     d = head_dim.
+ *   - KV pool of one layer: K and V each [num_slots, Hkv, d]; slot s holds the KV of one token
+ *     for all KV heads. The slot table req_to_token is [max_reqs, max_ctx] int32: row r lists
+ *     the slots of request r's tokens in order.
+ */
+#ifndef RC_H
+#define RC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RC_OK 0
+#define RC_ERR_INVALID -1     /* bad argument, stale node handle, double free */
+#define RC_ERR_OOM -2         /* fewer free slots than requested; nothing allocated */
+#define RC_ERR_INSUFFICIENT -3 /* eviction freed fewer tokens than requested */
+#define RC_ERR_CUDA -4        /* a CUDA runtime call failed */
+#define RC_ERR_DEVICE -5      /* a kernel reported bad data through the device status word */
+
+#define RC_DTYPE_BF16 0
+#define RC_DTYPE_F32 1
+
+typedef struct rc_pool rc_pool;
+typedef struct rc_radix rc_radix;
+/* Node handle. 0 is the root. A handle goes stale when its node is evicted; a stale handle is
+ * rejected with RC_ERR_INVALID. A split keeps the handle of the lower (deeper) part, so a handle
+ * always names the node that ends where it ended when it was returned. */
+typedef uint64_t rc_node;
+
+/* Thread-local message of the last failure (empty string if none). Never NULL. */
+const char* rc_last_error(void);
+/* Number of kernels this library has launched in this process (all device entry points). */
+uint64_t rc_launch_count(void);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Token pool (paper digest Sec. 3: KV stored in pages of one token; cached and running       */
+/* requests share one pool). Slots are the page indices 0 .. num_slots-1.                     */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Create a pool of num_slots free slots. initial_order (host, num_slots int32, a permutation of
+ * 0..num_slots-1, may be NULL for 0,1,2,...) is the initial free-list order. */
+int rc_pool_create(int64_t num_slots, const int32_t* initial_order, rc_pool** out);
+void rc_pool_destroy(rc_pool* pool);
+/* Take n slots from the head of the free list into out_slots (host, n int32). All or nothing:
+ * RC_ERR_OOM and no change when fewer than n are free. */
+int rc_kv_pool_alloc(rc_pool* pool, int64_t n, int32_t* out_slots);
+/* Return n slots (host) to the tail of the free list in the given order. RC_ERR_INVALID and no
+ * change if any slot is out of range, already free, or repeated. */
+int rc_kv_pool_free(rc_pool* pool, const int32_t* slots, int64_t n);
+int rc_kv_pool_available(const rc_pool* pool, int64_t* out);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Radix tree (paper digest Sec. 3 and Fig. 3; SGLang blog Sec. 2.3; RadixAttention explainer */
+/* "insert / match / split / evict"). Edges are token sequences; a node holds the slots of    */
+/* its edge's tokens. The tree frees evicted slots into the pool it was created with.         */
+/* ---------------------------------------------------------------------------------------- */
+
+int rc_radix_create(rc_pool* pool, rc_radix** out);
+/* Destroys the tree; slots it still holds are NOT returned to the pool. */
+void rc_radix_destroy(rc_radix* tree);
+
+/* Longest cached prefix of tokens[0:n] (host). Writes its length to *out_len, its slots to
+ * out_slots[0:*out_len] (host, capacity n) and the node where it ends to *out_node (0 if
+ * nothing matched). When the match ends inside an edge the edge is split there, so that
+ * locking *out_node protects exactly the matched tokens. Marks the path as most recently
+ * used (nodes stamped root to leaf with a logical clock). */
+int rc_radix_match_prefix(rc_radix* tree, const int32_t* tokens, int64_t n, int32_t* out_slots,
+                          int64_t* out_len, rc_node* out_node);
+/* Insert tokens[0:n] with their slots (host). Tokens already present keep the tree's slots;
+ * *out_existing = number of leading tokens that were present (the caller owns and should free
+ * its own slots[P:*out_existing] where P is what it matched). The sequence end becomes a node
+ * boundary (splitting an edge if needed); *out_node = that node. Marks the path as used. */
+int rc_radix_insert(rc_radix* tree, const int32_t* tokens, const int32_t* slots, int64_t n,
+                    int64_t* out_existing, rc_node* out_node);
+/* Reference counts: +1 / -1 on node and every ancestor (the root excluded). A node with a
+ * nonzero count is never evicted. Unlocking a node whose count is zero is RC_ERR_INVALID. */
+int rc_radix_lock(rc_radix* tree, rc_node node);
+int rc_radix_unlock(rc_radix* tree, rc_node node);
+/* Evict least-recently-used leaves with reference count 0, whole nodes at a time, smallest
+ * (stamp, node id) first, until at least n_tokens are freed; a parent that becomes such a leaf
+ * joins the candidates. Freed slots go to the pool tail, node by node, in token order.
+ * *out_freed = tokens freed (may exceed n_tokens). RC_ERR_INSUFFICIENT if fewer than n_tokens
+ * could be freed (what could be freed is freed). */
+int rc_radix_evict_lru(rc_radix* tree, int64_t n_tokens, int64_t* out_freed);
+
+typedef struct rc_stats {
+  int64_t nodes;             /* excluding the root */
+  int64_t cached_tokens;     /* tokens held by the tree */
+  int64_t evictable_tokens;  /* tokens in nodes with reference count 0 */
+  int64_t protected_tokens;  /* tokens in nodes with reference count > 0 */
+  int64_t splits;
+  int64_t evicted_nodes;
+  int64_t evicted_tokens;
+  int64_t matched_tokens;    /* sum of match lengths (prefill tokens skipped) */
+  int64_t match_queries;     /* sum of query lengths given to match */
+} rc_stats;
+int rc_radix_stats(const rc_radix* tree, rc_stats* out);
+
+/* Canonical dump for tests: depth first, children in ascending order of their first token; per
+ * node (root excluded): id, parent id, reference count, stamp, edge length L, L tokens, L slots
+ * (int64 each). Node ids count creations from 1 (root 0); a split's new upper node takes the
+ * next id. Returns the number of int64 written, or minus the number needed if cap is short. */
+int64_t rc_radix_dump(const rc_radix* tree, int64_t* buf, int64_t cap);
+
+/* Batched host steps for a scheduler step (host pointers). Sequence b is
+ * tokens[indptr[b] : indptr[b+1]]; rows is a [B, row_stride] int32 host array of slot rows.
+ *
+ * rc_radix_match_batch: for b in order, match the first match_len[b] tokens of sequence b
+ * (match_len may be NULL = whole sequence), lock the node where the match ends, write the
+ * matched slots to rows[b, 0:prefix_len[b]] and the node to nodes[b]. */
+int rc_radix_match_batch(rc_radix* tree, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                         const int32_t* match_len, int32_t* rows, int64_t row_stride,
+                         int32_t* prefix_len, rc_node* nodes);
+/* rc_radix_insert_batch: for b in order, insert sequence b with slots rows[b, 0:len_b]; free the
+ * caller's duplicate slots rows[b, prefix_len[b] : existing_b] to the pool; if keep_locked,
+ * lock the inserted sequence's end node (written to end_nodes[b] if end_nodes is not NULL);
+ * then unlock unlock_nodes[b] (skipped when unlock_nodes is NULL). *out_freed = duplicates
+ * freed (may be NULL). */
+int rc_radix_insert_batch(rc_radix* tree, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                          const int32_t* rows, int64_t row_stride, const int32_t* prefix_len,
+                          const rc_node* unlock_nodes, int32_t keep_locked, rc_node* end_nodes,
+                          int64_t* out_freed);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Device entry points                                                                       */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Slot-table write: req_to_token[seg_row[i], seg_col[i] + j] = values[seg_indptr[i] + j] for
+ * j < seg_indptr[i+1] - seg_indptr[i]. All arrays device int32. A segment outside the table
+ * sets the device status word and is skipped. */
+typedef struct rc_slot_write_args {
+  int32_t num_segments;
+  int32_t max_reqs;          /* rows of req_to_token */
+  int32_t max_ctx;           /* columns of req_to_token */
+  int64_t total_values;      /* seg_indptr[num_segments] (host-known) */
+  const int32_t* seg_row;
+  const int32_t* seg_col;
+  const int32_t* seg_indptr; /* [num_segments + 1] */
+  const int32_t* values;
+  int32_t* req_to_token;
+} rc_slot_write_args;
+int rc_slot_table_write(const rc_slot_write_args* args, void* stream);
+
+/* Extend attention (SGLang blog Sec. 2.3 "compute only the unmatched tokens"; paper digest
+ * App. A.1). For request b with matched prefix P = prefix_len[b] and S = qo_indptr[b+1] -
+ * qo_indptr[b] new tokens at positions P .. P+S-1, each new token's query attends to the P
+ * cached keys, gathered through req_to_token[req_idx[b], 0:P], and causally to the new keys of
+ * positions <= its own, which are read from k_new / v_new:
+ *   O[t,h] = sum_{j <= P+i} softmax_j(sm_scale * <q_t,h , k_j,h/g>) v_j,h/g,  t = qo_indptr[b]+i
+ * and the new K/V rows are scattered: k_pool[out_loc[t]] = k_new[t], v_pool likewise.
+ *   q [T, Hq, d], k_new / v_new [T, Hkv, d], o [T, Hq, d] in dtype; lse [T, Hq] fp32 natural log
+ *   of the softmax denominator of the scaled scores (optional, NULL to skip); out_loc [T],
+ *   qo_indptr [B+1], prefix_len [B], req_idx [B] device int32. bf16 requires head_dim 128
+ *   (tensor-core path); f32 takes head_dim 64 or 128. Requests may have S = 0. */
+typedef struct rc_extend_args {
+  int32_t dtype;
+  int32_t num_reqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t max_ctx;           /* columns of req_to_token, multiple of 4 */
+  int32_t max_q_len;         /* >= every S (host-known; sizes the grid) */
+  int32_t max_prefix_len;    /* >= every P (host-known) */
+  int64_t num_tokens;        /* T */
+  int64_t num_slots;
+  float sm_scale;
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* out_loc;
+  const int32_t* qo_indptr;
+  const int32_t* prefix_len;
+  const int32_t* req_idx;
+  const int32_t* req_to_token;
+  void* k_pool;              /* this layer's K plane [num_slots, Hkv, d] */
+  void* v_pool;
+  void* o;
+  float* lse;
+} rc_extend_args;
+int rc_extend_attention(const rc_extend_args* args, void* stream);
+
+/* Decode attention (paper digest App. A.1; RadixAttention explainer: each generated token
+ * attends to the KV of all previous tokens). Request b has seq_len[b] tokens including its new
+ * one, whose slot is out_loc[b] == req_to_token[req_idx[b], seq_len[b]-1]. Its query q[b]
+ * attends to all seq_len[b] keys: the first seq_len[b]-1 gathered from the pool, the last read
+ * from k_new[b] / v_new[b], which are also scattered to the pool at out_loc[b]. The context is
+ * cut into chunks of kv_chunk tokens processed in parallel (split-K); each chunk's partial
+ * state goes to the workspace and a merge kernel combines them with log-sum-exp weights.
+ *   q [B, Hq, d], k_new / v_new [B, Hkv, d], o [B, Hq, d] in dtype; lse [B, Hq] fp32 optional;
+ *   out_loc, seq_len, req_idx [B] device int32. head_dim 64 or 128. */
+typedef struct rc_decode_args {
+  int32_t dtype;
+  int32_t num_reqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t max_ctx;
+  int32_t kv_chunk;          /* tokens per split, multiple of 64; 0 = library default */
+  int64_t max_total_tokens;  /* >= sum of seq_len (host-known; sizes workspace and grid) */
+  int64_t num_slots;
+  float sm_scale;
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* out_loc;
+  const int32_t* seq_len;
+  const int32_t* req_idx;
+  const int32_t* req_to_token;
+  void* k_pool;
+  void* v_pool;
+  void* o;
+  float* lse;
+} rc_decode_args;
+/* Workspace bytes rc_decode_attention needs for these arguments (device memory, 256-B aligned,
+ * no initialisation needed). */
+int rc_decode_workspace_bytes(const rc_decode_args* args, size_t* out_bytes);
+int rc_decode_attention(const rc_decode_args* args, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Read and clear the device status word of the current device (synchronises `stream`).
+ * *out_code = 0 if no kernel reported bad data since the last call, else the first code seen:
+ * 1 slot out of range, 2 position beyond the slot-table row, 3 a wait expired. */
+int rc_device_status(int32_t* out_code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RC_H */

@@ -1,0 +1,260 @@
+"""prefix_cached_paged_gb300 -- RadixAttention's data path on one GB300 (sm_103a).
+
+A thin binding of librc (include/rc.h): a token-granular KV pool, a radix tree that finds each
+request's longest cached prefix and evicts unreferenced leaves in LRU order (host C++), and the
+extend / decode attention kernels that run on a paged KV pool through a slot table (CUDA).
+The binding only marshals arguments: every step runs in librc, and there is no fallback path --
+without the compiled library every call raises.
+
+Names follow the C ABI without the `rc_` prefix. Device functions take torch CUDA tensors (used
+for device memory and streams only) and launch on the current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from ._lib import (RC_DTYPE_BF16, RC_DTYPE_F32, RC_ERR_CUDA, RC_ERR_DEVICE, RC_ERR_INSUFFICIENT,
+                   RC_ERR_INVALID, RC_ERR_OOM, RC_OK, RcDecodeArgs, RcError, RcExtendArgs,
+                   RcSlotWriteArgs, RcStats, check, lib)
+
+__all__ = [
+    "Pool", "RadixTree", "RcError", "slot_table_write", "extend_attention", "decode_attention",
+    "decode_workspace_bytes", "device_status", "launch_count", "RC_OK", "RC_ERR_INVALID",
+    "RC_ERR_OOM", "RC_ERR_INSUFFICIENT", "RC_ERR_CUDA", "RC_ERR_DEVICE",
+]
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def launch_count() -> int:
+    return int(lib().rc_launch_count())
+
+
+class Pool:
+    """The token pool (free list of KV slots). rc_pool_* / rc_kv_pool_*."""
+
+    def __init__(self, num_slots: int, initial_order=None):
+        self._order = None if initial_order is None else _i32(initial_order)
+        h = ctypes.c_void_p()
+        check(lib().rc_pool_create(int(num_slots), None if self._order is None else
+                                   _p(self._order), ctypes.byref(h)), "rc_pool_create")
+        self.h = h
+        self.num_slots = int(num_slots)
+
+    def __del__(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            lib().rc_pool_destroy(self.h)
+            self.h = None
+
+    def alloc(self, n: int, out: np.ndarray | None = None) -> np.ndarray:
+        out = np.empty(int(n), dtype=np.int32) if out is None else out
+        check(lib().rc_kv_pool_alloc(self.h, int(n), _p(out)), "rc_kv_pool_alloc")
+        return out
+
+    def free(self, slots) -> None:
+        s = _i32(slots)
+        check(lib().rc_kv_pool_free(self.h, _p(s), len(s)), "rc_kv_pool_free")
+
+    def available(self) -> int:
+        v = ctypes.c_int64()
+        check(lib().rc_kv_pool_available(self.h, ctypes.byref(v)), "rc_kv_pool_available")
+        return int(v.value)
+
+
+class RadixTree:
+    """The radix tree over token sequences. rc_radix_*."""
+
+    def __init__(self, pool: Pool):
+        self.pool = pool
+        h = ctypes.c_void_p()
+        check(lib().rc_radix_create(pool.h, ctypes.byref(h)), "rc_radix_create")
+        self.h = h
+
+    def __del__(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            lib().rc_radix_destroy(self.h)
+            self.h = None
+
+    def match_prefix(self, tokens):
+        t = _i32(tokens)
+        out = np.empty(len(t), dtype=np.int32)
+        n = ctypes.c_int64()
+        node = ctypes.c_uint64()
+        check(lib().rc_radix_match_prefix(self.h, _p(t), len(t), _p(out), ctypes.byref(n),
+                                          ctypes.byref(node)), "rc_radix_match_prefix")
+        return int(n.value), out[: n.value].copy(), int(node.value)
+
+    def insert(self, tokens, slots):
+        t, s = _i32(tokens), _i32(slots)
+        ex = ctypes.c_int64()
+        node = ctypes.c_uint64()
+        check(lib().rc_radix_insert(self.h, _p(t), _p(s), len(t), ctypes.byref(ex),
+                                    ctypes.byref(node)), "rc_radix_insert")
+        return int(ex.value), int(node.value)
+
+    def lock(self, node: int) -> None:
+        check(lib().rc_radix_lock(self.h, int(node)), "rc_radix_lock")
+
+    def unlock(self, node: int) -> None:
+        check(lib().rc_radix_unlock(self.h, int(node)), "rc_radix_unlock")
+
+    def evict_lru(self, n_tokens: int):
+        """Returns (status, freed): status RC_OK or RC_ERR_INSUFFICIENT."""
+        f = ctypes.c_int64()
+        rc = lib().rc_radix_evict_lru(self.h, int(n_tokens), ctypes.byref(f))
+        if rc not in (RC_OK, RC_ERR_INSUFFICIENT):
+            check(rc, "rc_radix_evict_lru")
+        return rc, int(f.value)
+
+    def stats(self) -> dict:
+        s = RcStats()
+        check(lib().rc_radix_stats(self.h, ctypes.byref(s)), "rc_radix_stats")
+        return {k: int(getattr(s, k)) for k, _ in RcStats._fields_}
+
+    def dump(self) -> np.ndarray:
+        n = lib().rc_radix_dump(self.h, None, 0)
+        need = -n if n < 0 else n
+        buf = np.empty(max(need, 1), dtype=np.int64)
+        w = lib().rc_radix_dump(self.h, _p(buf), need)
+        assert w >= 0
+        return buf[:w].copy()
+
+    def match_batch(self, tokens: np.ndarray, indptr: np.ndarray, match_len, rows: np.ndarray):
+        """Match + lock B sequences in order. rows: [B, row_stride] int32 (written in place).
+        Returns (prefix_len int32[B], nodes uint64[B])."""
+        B = len(indptr) - 1
+        pl = np.empty(B, dtype=np.int32)
+        nodes = np.empty(B, dtype=np.uint64)
+        ml = None if match_len is None else _i32(match_len)
+        check(lib().rc_radix_match_batch(self.h, _p(tokens), _p(indptr), B,
+                                         None if ml is None else _p(ml), _p(rows),
+                                         rows.shape[1], _p(pl), _p(nodes)),
+              "rc_radix_match_batch")
+        return pl, nodes
+
+    def insert_batch(self, tokens, indptr, rows, prefix_len, unlock_nodes, keep_locked=False):
+        """Insert B sequences with their slot rows, free duplicates, optionally lock the ends,
+        unlock the matched nodes. Returns (end_nodes uint64[B], duplicates freed)."""
+        B = len(indptr) - 1
+        ends = np.empty(B, dtype=np.uint64)
+        freed = ctypes.c_int64()
+        un = None if unlock_nodes is None else np.ascontiguousarray(unlock_nodes, np.uint64)
+        check(lib().rc_radix_insert_batch(self.h, _p(tokens), _p(indptr), B, _p(rows),
+                                          rows.shape[1], _p(_i32(prefix_len)),
+                                          None if un is None else _p(un), int(keep_locked),
+                                          _p(ends), ctypes.byref(freed)),
+              "rc_radix_insert_batch")
+        return ends, int(freed.value)
+
+
+# ------------------------------------------------------------------ device entry points
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return RC_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return RC_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def slot_table_write(req_to_token, seg_row, seg_col, seg_indptr, values, stream=None):
+    """req_to_token[seg_row[i], seg_col[i] + j] = values[seg_indptr[i] + j] (device int32)."""
+    a = RcSlotWriteArgs(num_segments=seg_row.numel(), max_reqs=req_to_token.shape[0],
+                        max_ctx=req_to_token.shape[1], total_values=values.numel(),
+                        seg_row=seg_row.data_ptr(), seg_col=seg_col.data_ptr(),
+                        seg_indptr=seg_indptr.data_ptr(), values=values.data_ptr(),
+                        req_to_token=req_to_token.data_ptr())
+    check(lib().rc_slot_table_write(ctypes.byref(a), _stream(stream)), "rc_slot_table_write")
+
+
+def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
+                 k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len):
+    T, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    return RcExtendArgs(
+        dtype=_dtype_code(q), num_reqs=prefix_len.numel(), num_q_heads=Hq, num_kv_heads=Hkv,
+        head_dim=d, max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
+        max_prefix_len=int(max_prefix_len), num_tokens=T, num_slots=k_pool.shape[0],
+        sm_scale=float(sm_scale), q=q.data_ptr(), k_new=k_new.data_ptr(),
+        v_new=v_new.data_ptr(), out_loc=out_loc.data_ptr(), qo_indptr=qo_indptr.data_ptr(),
+        prefix_len=prefix_len.data_ptr(), req_idx=req_idx.data_ptr(),
+        req_to_token=req_to_token.data_ptr(), k_pool=k_pool.data_ptr(),
+        v_pool=v_pool.data_ptr(), o=o.data_ptr(), lse=0 if lse is None else lse.data_ptr())
+
+
+def extend_attention(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
+                     k_pool, v_pool, o, *, sm_scale, max_q_len, max_prefix_len, lse=None,
+                     stream=None):
+    """Extend attention of one layer (see rc_extend_attention). k_pool / v_pool are this layer's
+    planes [num_slots, Hkv, d]."""
+    a = _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
+                     k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len)
+    check(lib().rc_extend_attention(ctypes.byref(a), _stream(stream)), "rc_extend_attention")
+
+
+def _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool, o,
+                 lse, sm_scale, max_total_tokens, kv_chunk):
+    B, Hq, d = q.shape
+    return RcDecodeArgs(
+        dtype=_dtype_code(q), num_reqs=B, num_q_heads=Hq, num_kv_heads=k_new.shape[1],
+        head_dim=d, max_ctx=req_to_token.shape[1], kv_chunk=int(kv_chunk),
+        max_total_tokens=int(max_total_tokens), num_slots=k_pool.shape[0],
+        sm_scale=float(sm_scale), q=q.data_ptr(), k_new=k_new.data_ptr(),
+        v_new=v_new.data_ptr(), out_loc=out_loc.data_ptr(), seq_len=seq_len.data_ptr(),
+        req_idx=req_idx.data_ptr(), req_to_token=req_to_token.data_ptr(),
+        k_pool=k_pool.data_ptr(), v_pool=v_pool.data_ptr(), o=o.data_ptr(),
+        lse=0 if lse is None else lse.data_ptr())
+
+
+def decode_workspace_bytes(q, k_new, req_to_token, k_pool, *, max_total_tokens, kv_chunk=0) -> int:
+    B, Hq, d = q.shape
+    a = RcDecodeArgs(dtype=_dtype_code(q), num_reqs=B, num_q_heads=Hq,
+                     num_kv_heads=k_new.shape[1], head_dim=d, max_ctx=req_to_token.shape[1],
+                     kv_chunk=int(kv_chunk), max_total_tokens=int(max_total_tokens),
+                     num_slots=k_pool.shape[0])
+    n = ctypes.c_size_t()
+    check(lib().rc_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)),
+          "rc_decode_workspace_bytes")
+    return int(n.value)
+
+
+def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
+                     o, workspace, *, sm_scale, max_total_tokens, kv_chunk=0, lse=None,
+                     stream=None):
+    """Split-K decode attention of one layer (see rc_decode_attention). workspace: a uint8 CUDA
+    tensor of at least decode_workspace_bytes(...) bytes."""
+    a = _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
+                     o, lse, sm_scale, max_total_tokens, kv_chunk)
+    check(lib().rc_decode_attention(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "rc_decode_attention")
+
+
+def device_status(stream=None) -> int:
+    """Read and clear the device status word (0 = no kernel reported bad data)."""
+    v = ctypes.c_int32()
+    check(lib().rc_device_status(ctypes.byref(v), _stream(stream)), "rc_device_status")
+    return int(v.value)

@@ -1,0 +1,553 @@
+// Decode attention over the paged KV pool with split-K (RadixAttention explainer: every new
+// token attends to the KV of all previous tokens; paper digest App. A.1 decoding).
+//
+// Design (HBM-bound: every context token's K and V row is read once per KV head):
+//   * plan kernel (1 CTA): cuts each request's context into chunks of kv_chunk tokens and writes
+//     the job list (request, chunk) with per-request offsets into the workspace;
+//   * main kernel (persistent, #SMs x occupancy CTAs of 4 warps): every warp is an independent
+//     worker that takes (job, KV head) items from an atomic counter. For an item it streams the
+//     chunk's K and V rows (one contiguous row of head_dim elements per token) from the pool into
+//     a private 3-stage shared-memory ring with cp.async.bulk on mbarriers, the slot indices
+//     prefetched one stage ahead. All G = Hq/Hkv query heads of the KV head are computed from
+//     each row, so the KV is read once. Scores: lanes (token, half of head_dim) with a one-step
+//     shuffle; online softmax in base 2 (scale * log2 e folded into q); P.V: each lane owns
+//     head_dim/32 output columns of every query head. The new token's K/V come from k_new/v_new
+//     (and are scattered to the pool by the last chunk's item), so no read races the scatter;
+//   * a request with one chunk writes its output directly; otherwise each chunk writes
+//     (O normalised, log2-sum-exp) to the workspace and the merge kernel combines them.
+#include <algorithm>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "host_common.h"
+
+namespace rc {
+namespace {
+
+constexpr int kTok = 16;     // tokens per stage
+constexpr int kStages = 3;   // ring depth per warp
+constexpr int kWarps = 4;    // warps per CTA
+constexpr int kDefaultChunk = 512;
+
+struct Workspace {
+  int* njobs;     // [0]: jobs written, [1]: item counter
+  int* jbase;     // [B+1]
+  int2* jobs;     // [max_jobs] (request, chunk)
+  float* plse;    // [max_items * G]
+  float* po;      // [max_items * G * D]
+  int64_t max_jobs;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Workspace carve(void* base, int B, int G, int D, int64_t max_jobs, int Hkv, size_t* total) {
+  Workspace w{};
+  char* p = (char*)base;
+  size_t off = 0;
+  w.njobs = (int*)(p + off);
+  off += align256(2 * sizeof(int));
+  w.jbase = (int*)(p + off);
+  off += align256((size_t)(B + 1) * sizeof(int));
+  w.jobs = (int2*)(p + off);
+  off += align256((size_t)max_jobs * sizeof(int2));
+  const int64_t max_items = max_jobs * Hkv;
+  w.plse = (float*)(p + off);
+  off += align256((size_t)max_items * G * sizeof(float));
+  w.po = (float*)(p + off);
+  off += align256((size_t)max_items * G * D * sizeof(float));
+  w.max_jobs = max_jobs;
+  if (total) *total = off;
+  return w;
+}
+
+struct Params {
+  rc_decode_args a;
+  Workspace w;
+  int chunk;
+  int* status;
+};
+
+// ---------------------------------------------------------------- plan
+__global__ void decode_plan_kernel(Params p) {
+  __shared__ int warp_sums[32];
+  __shared__ int running_s;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int B = p.a.num_reqs;
+  if (tid == 0) running_s = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + tid;
+    int n = 0;
+    if (b < B) {
+      const int L = p.a.seq_len[b];
+      if (L < 1 || L > p.a.max_ctx) {
+        set_status(p.status, kStatusPosRange);
+      } else {
+        n = (L + p.chunk - 1) / p.chunk;
+      }
+    }
+    // block exclusive scan of n
+    int x = n;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sums[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    const int excl = running_s + (wid ? warp_sums[wid - 1] : 0) + x - n;
+    if (b < B) {
+      p.w.jbase[b] = excl;
+      for (int c = 0; c < n; ++c) {
+        if (excl + c < p.w.max_jobs)
+          p.w.jobs[excl + c] = make_int2(b, c);
+        else
+          set_status(p.status, kStatusPosRange);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) running_s += warp_sums[(blockDim.x >> 5) - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.w.jbase[B] = running_s;
+    p.w.njobs[0] = (int)min((int64_t)running_s, p.w.max_jobs);
+    p.w.njobs[1] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- main
+template <typename T, int D, int G>
+struct Cfg {
+  static constexpr int RB = D * (int)sizeof(T);  // bytes of one K or V row
+  static constexpr int RK = RB + 16;             // padded K row stride in shared memory
+  static constexpr int STAGE = kTok * (RK + RB);
+  static constexpr int RING = kStages * STAGE;
+  static constexpr int QS = G * D * 4;           // fp32 q of the warp's item
+  static constexpr int PS = kTok * G * 4;        // probabilities of one stage
+  static constexpr int BAR = kStages * 8;
+  static constexpr int WARP_BYTES = (RING + QS + PS + BAR + 127) / 128 * 128;
+  static constexpr int SMEM = kWarps * WARP_BYTES;
+  static constexpr int DPL = D / 32;             // output columns per lane
+  static_assert(RB % 16 == 0, "rows must be multiples of 16 bytes");
+  static_assert(STAGE % 16 == 0 && QS % 16 == 0 && PS % 16 == 0, "alignment");
+};
+
+template <typename T>
+__device__ __forceinline__ void load_cols(const char* p, float* v, int n);
+template <>
+__device__ __forceinline__ void load_cols<__nv_bfloat16>(const char* p, float* v, int n) {
+  if (n == 4) {
+    const uint2 w = *(const uint2*)p;
+    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+  } else {  // n == 2
+    const uint32_t w = *(const uint32_t*)p;
+    v[0] = bf16lo(w); v[1] = bf16hi(w);
+  }
+}
+template <>
+__device__ __forceinline__ void load_cols<float>(const char* p, float* v, int n) {
+  if (n == 4) {
+    const float4 w = *(const float4*)p;
+    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+  } else {
+    const float2 w = *(const float2*)p;
+    v[0] = w.x; v[1] = w.y;
+  }
+}
+
+// 16 bytes of a row -> fp32 values (8 for bf16, 4 for fp32)
+template <typename T>
+struct Chunk16;
+template <>
+struct Chunk16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void get(const char* p, float* k) {
+    const uint4 w = *(const uint4*)p;
+    k[0] = bf16lo(w.x); k[1] = bf16hi(w.x); k[2] = bf16lo(w.y); k[3] = bf16hi(w.y);
+    k[4] = bf16lo(w.z); k[5] = bf16hi(w.z); k[6] = bf16lo(w.w); k[7] = bf16hi(w.w);
+  }
+};
+template <>
+struct Chunk16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void get(const char* p, float* k) {
+    const float4 w = *(const float4*)p;
+    k[0] = w.x; k[1] = w.y; k[2] = w.z; k[3] = w.w;
+  }
+};
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kWarps * 32) decode_main_kernel(Params p) {
+  using C = Cfg<T, D, G>;
+  extern __shared__ __align__(128) char smem[];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  char* wbase = smem + wid * C::WARP_BYTES;
+  char* ring = wbase;
+  float* q_s = (float*)(wbase + C::RING);
+  float* p_s = (float*)(wbase + C::RING + C::QS);
+  uint64_t* bars = (uint64_t*)(wbase + C::RING + C::QS + C::PS);
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const rc_decode_args& a = p.a;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  const int n_items = p.w.njobs[0] * Hkv;
+  const float qscale = a.sm_scale * kLog2e;
+  const T* kpool = (const T*)a.k_pool;
+  const T* vpool = (const T*)a.v_pool;
+  uint32_t phases = 0;  // bit s = parity to wait for on stage buffer s
+  const int t = lane & 15, half = lane >> 4;
+
+  while (true) {
+    int item = 0;
+    if (lane == 0) item = atomicAdd(&p.w.njobs[1], 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (item >= n_items) break;
+    const int job = item / Hkv, h = item - job * Hkv;
+    const int2 bc = p.w.jobs[job];
+    const int b = bc.x, c = bc.y;
+    const int L = a.seq_len[b];
+    const int row = a.req_idx[b];
+    const int t0 = c * p.chunk;
+    const int t1 = min(L, t0 + p.chunk);
+    const int nchunks = (L + p.chunk - 1) / p.chunk;
+    const int nst = (t1 - t0 + kTok - 1) / kTok;
+    const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
+    const T* knew = (const T*)a.k_new + ((int64_t)b * Hkv + h) * D;
+    const T* vnew = (const T*)a.v_new + ((int64_t)b * Hkv + h) * D;
+
+    // q of the G query heads of this KV head, pre-scaled to base-2 logits
+    {
+      const T* qg = (const T*)a.q + ((int64_t)b * Hq + (int64_t)h * G) * D;
+      for (int e = lane; e < G * D; e += 32) q_s[e] = Elem<T>::to_f(qg[e]) * qscale;
+    }
+
+    // slot of the token this lane loads in stage s (-1: past the chunk; -2: the new token)
+    auto slot_of = [&](int s) -> int {
+      const int pos = t0 + s * kTok + lane;
+      if (lane >= kTok || pos >= t1) return -1;
+      if (pos == L - 1) return -2;
+      const int sl = rt[pos];
+      if (sl < 0 || (int64_t)sl >= a.num_slots) {
+        set_status(p.status, kStatusSlotRange);
+        return -3;
+      }
+      return sl;
+    };
+    // issue stage s (slot already resolved); returns the mask of real tokens
+    auto issue = [&](int s, int sl) {
+      const int buf = s % kStages;
+      char* kd = ring + buf * C::STAGE + lane * C::RK;
+      char* vd = ring + buf * C::STAGE + kTok * C::RK + lane * C::RB;
+      const bool live = sl != -1;
+      const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[buf], nlive * 2u * C::RB);
+      if (live) {
+        const T* ks;
+        const T* vs;
+        if (sl == -2) {
+          ks = knew;
+          vs = vnew;
+        } else {
+          const int64_t r = ((int64_t)(sl < 0 ? 0 : sl) * Hkv + h) * D;  // bad slot: read row 0
+          ks = kpool + r;
+          vs = vpool + r;
+        }
+        bulk_g2s(kd, ks, C::RB, &bars[buf]);
+        bulk_g2s(vd, vs, C::RB, &bars[buf]);
+      }
+    };
+
+    int next_slot = slot_of(0);
+    const int pro = min(nst, kStages - 1);
+    for (int s = 0; s < pro; ++s) {
+      issue(s, next_slot);
+      next_slot = slot_of(s + 1);
+    }
+    __syncwarp();  // q_s visible to all lanes
+
+    float m[G], lsum[G], acc[G][C::DPL];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      lsum[g] = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::DPL; ++k) acc[g][k] = 0.f;
+    }
+
+    bool ok = true;
+    for (int s = 0; s < nst; ++s) {
+      if (s + kStages - 1 < nst) {
+        issue(s + kStages - 1, next_slot);
+        next_slot = slot_of(s + kStages);
+      }
+      const int buf = s % kStages;
+      if (!mbar_wait(&bars[buf], (phases >> buf) & 1u, p.status)) {
+        ok = false;
+        break;
+      }
+      phases ^= 1u << buf;
+      const int base_pos = t0 + s * kTok;
+      const int ntok = min(kTok, t1 - base_pos);
+      const int my_slot_ok = (base_pos + t < t1);
+      // ---- scores: lane (t, half) covers head_dim/2 columns of token t
+      float sc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) sc[g] = 0.f;
+      {
+        const char* krow = ring + buf * C::STAGE + t * C::RK + half * (C::RB / 2);
+        const int d0 = half * (D / 2);
+#pragma unroll
+        for (int cc = 0; cc < C::RB / 2 / 16; ++cc) {
+          float k[Chunk16<T>::N];
+          Chunk16<T>::get(krow + cc * 16, k);
+          const int dd = d0 + cc * Chunk16<T>::N;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int e = 0; e < Chunk16<T>::N; e += 4) {
+              const float4 qv = *(const float4*)&q_s[g * D + dd + e];
+              sc[g] = fmaf(qv.x, k[e], sc[g]);
+              sc[g] = fmaf(qv.y, k[e + 1], sc[g]);
+              sc[g] = fmaf(qv.z, k[e + 2], sc[g]);
+              sc[g] = fmaf(qv.w, k[e + 3], sc[g]);
+            }
+          }
+        }
+      }
+      float alpha[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], 16);
+        if (!my_slot_ok) sc[g] = -INFINITY;
+        float mx = sc[g];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        const float mn = fmaxf(m[g], mx);
+        alpha[g] = (mn == -INFINITY) ? 1.f : exp2f(m[g] - mn);
+        const float pr = (sc[g] == -INFINITY) ? 0.f : exp2f(sc[g] - mn);
+        lsum[g] = lsum[g] * alpha[g] + (half == 0 ? pr : 0.f);
+        m[g] = mn;
+        if (half == 0) p_s[t * G + g] = pr;
+      }
+      __syncwarp();
+      // ---- P.V: lane owns columns [lane*DPL, lane*DPL + DPL)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int k = 0; k < C::DPL; ++k) acc[g][k] *= alpha[g];
+      const char* vb = ring + buf * C::STAGE + kTok * C::RK + lane * C::DPL * (int)sizeof(T);
+      for (int tt = 0; tt < ntok; ++tt) {
+        float v[C::DPL];
+        load_cols<T>(vb + tt * C::RB, v, C::DPL);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pr = p_s[tt * G + g];
+#pragma unroll
+          for (int k = 0; k < C::DPL; ++k) acc[g][k] = fmaf(pr, v[k], acc[g][k]);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      // a copy never landed: wait (bounded) for this warp's other copies, then stop
+      for (int s = 0; s < kStages; ++s) mbar_wait(&bars[s], (phases >> s) & 1u, p.status, 100000000ull);
+      return;
+    }
+
+    // ---- epilogue
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float l = lsum[g];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse2 = l > 0.f ? m[g] + log2f(l) : -INFINITY;
+      const int hq = h * G + g;
+      if (nchunks == 1) {
+        T* o = (T*)a.o + ((int64_t)b * Hq + hq) * D + lane * C::DPL;
+#pragma unroll
+        for (int k = 0; k < C::DPL; ++k) o[k] = Elem<T>::from_f(acc[g][k] * inv);
+        if (a.lse && lane == 0) a.lse[(int64_t)b * Hq + hq] = lse2 * kLn2;
+      } else {
+        const int64_t pi = (int64_t)item * G + g;
+        float* po = p.w.po + pi * D + lane * C::DPL;
+#pragma unroll
+        for (int k = 0; k < C::DPL; ++k) po[k] = acc[g][k] * inv;
+        if (lane == 0) p.w.plse[pi] = lse2;
+      }
+    }
+    // ---- the last chunk scatters the new token's K and V rows into the pool
+    if (c == nchunks - 1) {
+      const int sl = a.out_loc[b];
+      if (sl < 0 || (int64_t)sl >= a.num_slots) {
+        if (lane == 0) set_status(p.status, kStatusSlotRange);
+      } else {
+        const int64_t r = ((int64_t)sl * Hkv + h) * D;
+        for (int e = lane; e < C::RB / 16; e += 32) {
+          ((uint4*)((T*)a.k_pool + r))[e] = ((const uint4*)knew)[e];
+          ((uint4*)((T*)a.v_pool + r))[e] = ((const uint4*)vnew)[e];
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- merge
+template <typename T, int D, int G>
+__global__ void decode_merge_kernel(Params p) {
+  const rc_decode_args& a = p.a;
+  const int b = blockIdx.x;
+  const int hq = blockIdx.y;
+  const int L = a.seq_len[b];
+  if (L < 1 || L > a.max_ctx) return;
+  const int nchunks = (L + p.chunk - 1) / p.chunk;
+  if (nchunks == 1) return;
+  const int Hkv = a.num_kv_heads;
+  const int h = hq / G, g = hq - h * G;
+  const int j0 = p.w.jbase[b];
+  if ((int64_t)j0 + nchunks > p.w.max_jobs) return;
+  float M = -INFINITY;
+  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, p.w.plse[((int64_t)(j0 + c) * Hkv + h) * G + g]);
+  const int d = threadIdx.x;
+  float num = 0.f, den = 0.f;
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t pi = ((int64_t)(j0 + c) * Hkv + h) * G + g;
+    const float lc = p.w.plse[pi];
+    const float w = (lc == -INFINITY) ? 0.f : exp2f(lc - M);
+    den += w;
+    num = fmaf(w, p.w.po[pi * D + d], num);
+  }
+  T* o = (T*)a.o + ((int64_t)b * a.num_q_heads + hq) * D;
+  o[d] = Elem<T>::from_f(den > 0.f ? num / den : 0.f);
+  if (a.lse && d == 0) a.lse[(int64_t)b * a.num_q_heads + hq] = (M + log2f(den)) * kLn2;
+}
+
+// ---------------------------------------------------------------- host side
+int64_t max_jobs_for(const rc_decode_args* a, int chunk) {
+  return (a->max_total_tokens + chunk - 1) / chunk + a->num_reqs;
+}
+
+int chunk_of(const rc_decode_args* a) { return a->kv_chunk > 0 ? a->kv_chunk : kDefaultChunk; }
+
+int validate(const rc_decode_args* a) {
+  RC_CHECK_ARG(a != nullptr, "rc_decode_attention: args is NULL");
+  RC_CHECK_ARG(a->dtype == RC_DTYPE_BF16 || a->dtype == RC_DTYPE_F32,
+               "rc_decode_attention: dtype %d", a->dtype);
+  RC_CHECK_ARG(a->num_reqs >= 0 && a->num_q_heads > 0 && a->num_kv_heads > 0 &&
+                   a->num_q_heads % a->num_kv_heads == 0,
+               "rc_decode_attention: bad head counts");
+  const int G = a->num_q_heads / a->num_kv_heads;
+  RC_CHECK_ARG(G == 1 || G == 2 || G == 4 || G == 8, "rc_decode_attention: group size %d", G);
+  RC_CHECK_ARG(a->head_dim == 64 || a->head_dim == 128, "rc_decode_attention: head_dim %d",
+               a->head_dim);
+  RC_CHECK_ARG(a->max_ctx > 0 && a->num_slots > 0 && a->max_total_tokens >= 0,
+               "rc_decode_attention: bad sizes");
+  RC_CHECK_ARG(a->kv_chunk == 0 || (a->kv_chunk > 0 && a->kv_chunk % 64 == 0),
+               "rc_decode_attention: kv_chunk %d", a->kv_chunk);
+  return RC_OK;
+}
+
+template <typename T, int D, int G>
+int launch_t(const Params& p, cudaStream_t s) {
+  using C = Cfg<T, D, G>;
+  auto kern = decode_main_kernel<T, D, G>;
+  static int blocks_per_sm = -1;
+  static int num_sms = 0;
+  static std::once_flag once;
+  static cudaError_t init_err = cudaSuccess;
+  std::call_once(once, [&]() {
+    init_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    int dev = 0;
+    if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
+    if (init_err == cudaSuccess)
+      init_err = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (init_err == cudaSuccess)
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern,
+                                                               kWarps * 32, C::SMEM);
+  });
+  if (init_err != cudaSuccess)
+    return fail(RC_ERR_CUDA, "rc_decode_attention: setup: %s", cudaGetErrorString(init_err));
+  decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+  const int grid = std::max(1, num_sms * std::max(1, blocks_per_sm));
+  kern<<<grid, kWarps * 32, C::SMEM, s>>>(p);
+  dim3 mg(p.a.num_reqs, p.a.num_q_heads);
+  decode_merge_kernel<T, D, G><<<mg, D, 0, s>>>(p);
+  count_launches(3);
+  return check_launch("rc_decode_attention");
+}
+
+template <typename T, int D>
+int launch_g(const Params& p, int G, cudaStream_t s) {
+  switch (G) {
+    case 1: return launch_t<T, D, 1>(p, s);
+    case 2: return launch_t<T, D, 2>(p, s);
+    case 4: return launch_t<T, D, 4>(p, s);
+    default: return launch_t<T, D, 8>(p, s);
+  }
+}
+
+}  // namespace
+}  // namespace rc
+
+extern "C" int rc_decode_workspace_bytes(const rc_decode_args* a, size_t* out_bytes) {
+  const int v = rc::validate(a);
+  if (v != RC_OK) return v;
+  RC_CHECK_ARG(out_bytes != nullptr, "rc_decode_workspace_bytes: out_bytes is NULL");
+  const int chunk = rc::chunk_of(a);
+  const int G = a->num_q_heads / a->num_kv_heads;
+  size_t total = 0;
+  rc::carve(nullptr, a->num_reqs, G, a->head_dim, rc::max_jobs_for(a, chunk), a->num_kv_heads,
+            &total);
+  *out_bytes = total;
+  return RC_OK;
+}
+
+extern "C" int rc_decode_attention(const rc_decode_args* a, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  const int v = rc::validate(a);
+  if (v != RC_OK) return v;
+  if (a->num_reqs == 0) return RC_OK;
+  RC_CHECK_ARG(a->q && a->k_new && a->v_new && a->out_loc && a->seq_len && a->req_idx &&
+                   a->req_to_token && a->k_pool && a->v_pool && a->o && workspace,
+               "rc_decode_attention: NULL pointer");
+  const uintptr_t al = (uintptr_t)a->k_new | (uintptr_t)a->v_new | (uintptr_t)a->k_pool |
+                       (uintptr_t)a->v_pool | (uintptr_t)workspace;
+  RC_CHECK_ARG((al & 15) == 0, "rc_decode_attention: K/V pointers and workspace must be 16-byte aligned");
+  const int chunk = rc::chunk_of(a);
+  const int G = a->num_q_heads / a->num_kv_heads;
+  size_t need = 0;
+  rc::Params p{};
+  p.a = *a;
+  p.chunk = chunk;
+  p.w = rc::carve(workspace, a->num_reqs, G, a->head_dim, rc::max_jobs_for(a, chunk),
+                  a->num_kv_heads, &need);
+  RC_CHECK_ARG(workspace_bytes >= need, "rc_decode_attention: workspace %zu bytes < %zu needed",
+               workspace_bytes, need);
+  p.status = rc::device_status_ptr();
+  if (!p.status) return rc::fail(RC_ERR_CUDA, "rc_decode_attention: no device status word");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (a->dtype == RC_DTYPE_BF16)
+    return a->head_dim == 128 ? rc::launch_g<__nv_bfloat16, 128>(p, G, s)
+                              : rc::launch_g<__nv_bfloat16, 64>(p, G, s);
+  return a->head_dim == 128 ? rc::launch_g<float, 128>(p, G, s) : rc::launch_g<float, 64>(p, G, s);
+}

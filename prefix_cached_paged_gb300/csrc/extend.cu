@@ -1,0 +1,35 @@
+// rc_extend_attention: argument checks and the dtype -> kernel mapping.
+//   bf16, head_dim 128 -> the tcgen05 tensor-core kernel (extend_tc.cu)
+//   fp32               -> the CUDA-core kernel (extend_simt.cu)
+#include "device_common.cuh"
+#include "extend_common.h"
+#include "host_common.h"
+
+extern "C" int rc_extend_attention(const rc_extend_args* a, void* stream) {
+  RC_CHECK_ARG(a != nullptr, "rc_extend_attention: args is NULL");
+  RC_CHECK_ARG(a->dtype == RC_DTYPE_BF16 || a->dtype == RC_DTYPE_F32,
+               "rc_extend_attention: dtype %d", a->dtype);
+  RC_CHECK_ARG(a->num_reqs >= 0 && a->num_q_heads > 0 && a->num_kv_heads > 0 &&
+                   a->num_q_heads % a->num_kv_heads == 0,
+               "rc_extend_attention: bad head counts");
+  RC_CHECK_ARG(a->head_dim == 128 || (a->dtype == RC_DTYPE_F32 && a->head_dim == 64),
+               "rc_extend_attention: head_dim %d unsupported for this dtype", a->head_dim);
+  RC_CHECK_ARG(a->max_ctx > 0 && a->max_ctx % 4 == 0, "rc_extend_attention: max_ctx %d",
+               a->max_ctx);
+  RC_CHECK_ARG(a->max_q_len >= 0 && a->max_prefix_len >= 0 && a->num_tokens >= 0 &&
+                   a->num_slots > 0,
+               "rc_extend_attention: bad sizes");
+  if (a->num_reqs == 0 || a->num_tokens == 0 || a->max_q_len == 0) return RC_OK;
+  RC_CHECK_ARG(a->q && a->k_new && a->v_new && a->out_loc && a->qo_indptr && a->prefix_len &&
+                   a->req_idx && a->req_to_token && a->k_pool && a->v_pool && a->o,
+               "rc_extend_attention: NULL pointer");
+  const uintptr_t al = (uintptr_t)a->q | (uintptr_t)a->k_new | (uintptr_t)a->v_new |
+                       (uintptr_t)a->k_pool | (uintptr_t)a->v_pool | (uintptr_t)a->o |
+                       (uintptr_t)a->req_to_token;
+  RC_CHECK_ARG((al & 15) == 0, "rc_extend_attention: tensors must be 16-byte aligned");
+  int* st = rc::device_status_ptr();
+  if (!st) return rc::fail(RC_ERR_CUDA, "rc_extend_attention: no device status word");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (a->dtype == RC_DTYPE_BF16) return rc::launch_extend_tc(a, st, s);
+  return rc::launch_extend_simt(a, st, s);
+}

@@ -1,0 +1,152 @@
+"""Scheduler-step composition of librc's host calls, plus device-side state for a model.
+
+`HostCache` runs one batch through the pages' loop with librc's batched calls (SGLang blog
+Sec. 2.3: traverse, reuse, compute, insert; LRU eviction when the pool runs short; paper digest
+App. A.2 batch formation):
+
+  plan:   match every sequence (all but its last token; all of it for a cache fill) and lock the
+          matched node (rc_radix_match_batch); if fewer slots are free than the batch needs,
+          evict LRU leaves for the shortfall (rc_radix_evict_lru); allocate the unmatched
+          suffixes in request order, then any extra slots (rc_kv_pool_alloc);
+  finish: insert every sequence with its slot row, free duplicate slots, unlock
+          (rc_radix_insert_batch).
+
+`DeviceKV` holds a model's KV planes and slot table on the GPU and uploads a plan's metadata.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import RC_OK, Pool, RadixTree, RcError
+
+
+@dataclass
+class Plan:
+    tokens: np.ndarray        # concatenated sequences, int32
+    indptr: np.ndarray        # int64 [B+1]
+    lengths: np.ndarray       # int64 [B]
+    prefix_len: np.ndarray    # int32 [B], matched (reused) tokens
+    nodes: np.ndarray         # uint64 [B], locked by the match
+    rows: np.ndarray          # int32 [B, row_stride], full slot rows
+    qo_indptr: np.ndarray     # int32 [B+1], offsets of the computed tokens
+    out_loc: np.ndarray       # int32 [T], slots of the computed tokens
+    extra: np.ndarray         # int32 [extra], slots allocated after the batch's own
+    evict_request: int = 0
+    evicted: int = 0
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.qo_indptr[-1])
+
+
+class HostCache:
+    def __init__(self, num_slots: int, row_stride: int, initial_order=None):
+        self.pool = Pool(num_slots, initial_order)
+        self.tree = RadixTree(self.pool)
+        self.row_stride = int(row_stride)
+
+    def _make_room(self, need: int, plan: Plan, nodes) -> None:
+        avail = self.pool.available()
+        if avail < need:
+            plan.evict_request = need - avail
+            rc, freed = self.tree.evict_lru(need - avail)
+            plan.evicted = freed
+            if rc != RC_OK:
+                for n in nodes:
+                    self.tree.unlock(int(n))
+                raise RcError(rc, f"make room for {need} slots ({avail} free, {freed} evicted)")
+
+    def plan(self, seqs, extra: int = 0, match_all: bool = False) -> Plan:
+        seqs = [np.asarray(s, dtype=np.int32) for s in seqs]
+        B = len(seqs)
+        lengths = np.array([len(s) for s in seqs], dtype=np.int64)
+        indptr = np.zeros(B + 1, dtype=np.int64)
+        np.cumsum(lengths, out=indptr[1:])
+        tokens = np.concatenate(seqs) if B else np.zeros(0, np.int32)
+        match_len = lengths if match_all else np.maximum(lengths - 1, 0)
+        rows = np.zeros((B, self.row_stride), dtype=np.int32)
+        prefix_len, nodes = self.tree.match_batch(tokens, indptr, match_len.astype(np.int32),
+                                                  rows)
+        S = lengths - prefix_len
+        qo = np.zeros(B + 1, dtype=np.int32)
+        np.cumsum(S, out=qo[1:])
+        plan = Plan(tokens, indptr, lengths, prefix_len, nodes, rows, qo,
+                    np.zeros(0, np.int32), np.zeros(0, np.int32))
+        need = int(qo[-1]) + int(extra)
+        self._make_room(need, plan, nodes)
+        new = self.pool.alloc(need)
+        for b in range(B):
+            rows[b, prefix_len[b]:lengths[b]] = new[qo[b]:qo[b + 1]]
+        plan.out_loc = new[: qo[-1]]
+        plan.extra = new[qo[-1]:]
+        return plan
+
+    def finish(self, plan: Plan, keep_locked: bool = False):
+        """Insert, free duplicates, unlock. Returns (end nodes, duplicates freed)."""
+        return self.tree.insert_batch(plan.tokens, plan.indptr, plan.rows, plan.prefix_len,
+                                      plan.nodes, keep_locked)
+
+    def alloc(self, n: int) -> np.ndarray:
+        """n slots for decode tokens, evicting LRU leaves if the pool is short."""
+        p = Plan(*(np.zeros(0),) * 9)
+        self._make_room(n, p, [])
+        out = self.pool.alloc(n)
+        self.last_alloc_evicted = p.evicted
+        return out
+
+
+class DeviceKV:
+    """KV planes [layers, num_slots, Hkv, d] for K and V and the slot table on one GPU."""
+
+    def __init__(self, layers, num_slots, n_kv_heads, head_dim, dtype, max_reqs, max_ctx,
+                 device="cuda"):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device)
+        self.k = torch.empty((layers, num_slots, n_kv_heads, head_dim), dtype=dtype,
+                             device=self.device)
+        self.v = torch.empty_like(self.k)
+        self.req_to_token = torch.zeros((max_reqs, max_ctx), dtype=torch.int32,
+                                        device=self.device)
+        self._stage = None
+        self._stage_event = None
+
+    def upload_i32(self, arrays):
+        """Copy int32 host arrays to the device in one transfer through a pinned staging buffer;
+        returns device views in order."""
+        torch = self.torch
+        arrays = [np.ascontiguousarray(a, dtype=np.int32).ravel() for a in arrays]
+        sizes = [len(a) for a in arrays]
+        total = max(sum(sizes), 1)
+        if self._stage_event is not None:
+            self._stage_event.synchronize()
+        if self._stage is None or self._stage.numel() < total:
+            self._stage = torch.empty(max(total, 1 << 16), dtype=torch.int32, pin_memory=True)
+        host = self._stage.numpy()
+        off = 0
+        for a in arrays:
+            host[off:off + len(a)] = a
+            off += len(a)
+        dev = self._stage[:total].to(self.device, non_blocking=True)
+        self._stage_event = torch.cuda.Event()
+        self._stage_event.record()
+        out, off = [], 0
+        for n in sizes:
+            out.append(dev[off:off + n])
+            off += n
+        return out
+
+    def write_rows(self, row_ids, rows, lengths, cols=None):
+        """req_to_token[row_ids[b], cols[b] : cols[b] + lengths[b]] = rows[b, cols[b]:...]."""
+        from . import slot_table_write
+        B = len(row_ids)
+        cols = np.zeros(B, np.int64) if cols is None else np.asarray(cols)
+        seg_len = np.asarray(lengths, dtype=np.int64) - 0
+        vals = [rows[b, cols[b]:cols[b] + seg_len[b]] for b in range(B)]
+        indptr = np.zeros(B + 1, dtype=np.int64)
+        np.cumsum(seg_len, out=indptr[1:])
+        values = np.concatenate(vals) if B else np.zeros(0, np.int32)
+        r, c, ip, v = self.upload_i32([row_ids, cols, indptr, values])
+        slot_table_write(self.req_to_token, r, c, ip, v)

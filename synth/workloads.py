@@ -37,7 +37,8 @@ class Model:
 @dataclass
 class Phase:
     """kind: 'extend' (compute the unmatched suffix of each sequence), 'cache' (insert sequences
-    as already computed; their KV is written straight into the pool), 'decode' (one new token per
+    one at a time as already computed; their KV is written straight into the pool), 'decode'
+    (one new token per
     request over its cached context: seqs are full sequences, context = all but the last token)."""
     kind: str
     seqs: list

@@ -1,0 +1,176 @@
+"""librc's host side against the oracle (CPU only): bit-exact slots, match lengths, evictions and
+whole-tree dumps, plus the C-ABI exports."""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import prefix_cached_paged_gb300 as rc
+from prefix_cached_paged_gb300 import runtime
+from prefix_cached_paged_gb300._lib import SIGNATURES, lib
+from synth import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "rc.h")).read()
+    declared = set(re.findall(r"^\s*(?:[\w\*]+\s+)+\**(rc_\w+)\s*\(", header, re.M))
+    assert declared, "no declarations parsed"
+    L = lib()
+    for name in sorted(declared):
+        assert hasattr(L, name), name
+    assert declared == set(SIGNATURES), declared ^ set(SIGNATURES)
+
+
+def test_pool_semantics():
+    p = rc.Pool(5, [4, 2, 0, 1, 3])
+    assert p.alloc(2).tolist() == [4, 2]
+    with pytest.raises(rc.RcError) as e:
+        p.alloc(4)
+    assert e.value.code == rc.RC_ERR_OOM and p.available() == 3
+    with pytest.raises(rc.RcError):
+        p.free([4, 4])          # repeated
+    with pytest.raises(rc.RcError):
+        p.free([0])             # already free
+    with pytest.raises(rc.RcError):
+        p.free([7])             # out of range
+    assert p.available() == 3
+    p.free([2, 4])
+    assert p.alloc(5).tolist() == [0, 1, 3, 2, 4]
+    with pytest.raises(rc.RcError):
+        rc.Pool(3, [0, 0, 1])
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_ops_match_oracle_bit_exact(seed):
+    rnd = random.Random(1000 + seed)
+    alpha = rnd.choice([2, 3, 5])
+    N = 300
+    order = np.array(rnd.sample(range(N), N), dtype=np.int32)
+    op_, ot = oracle.Pool(N, order), None
+    ot = oracle.Tree(op_)
+    pp = rc.Pool(N, order)
+    pt = rc.RadixTree(pp)
+    locked = []  # (oracle id, product handle)
+    for step in range(150):
+        r = rnd.random()
+        toks = [rnd.randrange(alpha) for _ in range(rnd.randint(0, 14))]
+        if r < 0.35:
+            n1, s1, id1 = ot.match(toks)
+            n2, s2, h2 = pt.match_prefix(toks)
+            assert (n1, s1.tolist()) == (n2, s2.tolist())
+            if rnd.random() < 0.4:
+                ot.lock(id1)
+                pt.lock(h2)
+                locked.append((id1, h2))
+        elif r < 0.7:
+            a1 = op_.alloc(len(toks))
+            if a1 is None:
+                with pytest.raises(rc.RcError):
+                    pp.alloc(len(toks))
+                continue
+            a2 = pp.alloc(len(toks))
+            assert a1.tolist() == a2.tolist()
+            e1, _ = ot.insert(toks, a1)
+            e2, _ = pt.insert(toks, a2)
+            assert e1 == e2
+            op_.free(a1[:e1])
+            pp.free(a2[:e2])
+        elif r < 0.8 and locked:
+            i1, h2 = locked.pop(rnd.randrange(len(locked)))
+            ot.unlock(i1)
+            pt.unlock(h2)
+        else:
+            want = rnd.randint(0, 30)
+            ok1, f1, _ = ot.evict(want)
+            st, f2 = pt.evict_lru(want)
+            assert f1 == f2 and ok1 == (st == rc.RC_OK)
+        assert op_.available() == pp.available()
+        np.testing.assert_array_equal(ot.dump(), pt.dump())
+    s1, s2 = ot.stats(), pt.stats()
+    for k in ("splits", "evicted_nodes", "evicted_tokens", "nodes", "cached_tokens",
+              "protected_tokens"):
+        assert s1[k] == s2[k], k
+    # the free lists agree in order
+    n = op_.available()
+    assert op_.alloc(n).tolist() == pp.alloc(n).tolist()
+
+
+def test_stale_handles_and_unlock_underflow():
+    pool = rc.Pool(20)
+    t = rc.RadixTree(pool)
+    t.insert([1, 2, 3], pool.alloc(3))
+    n, _, h = t.match_prefix([1, 2, 3])
+    st, freed = t.evict_lru(3)
+    assert st == rc.RC_OK and freed == 3
+    with pytest.raises(rc.RcError) as e:
+        t.lock(h)
+    assert e.value.code == rc.RC_ERR_INVALID
+    t.insert([4, 5], pool.alloc(2))
+    _, _, h2 = t.match_prefix([4, 5])
+    with pytest.raises(rc.RcError):
+        t.unlock(h2)
+
+
+def _run_phases_both(w, steps=None):
+    """Run a workload's host steps through the product runtime and the oracle's loop; compare."""
+    pc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order)
+    oc = oracle.CacheSim(w.pool_slots, w.pool_order)
+    for ph in w.phases:
+        if ph.kind == "decode":
+            ctx = [s[:-1] for s in ph.seqs]
+            pp = pc.plan(ctx, extra=len(ctx), match_all=True)
+            op = oc.decode_prepare(ctx)
+            assert pp.prefix_len.tolist() == op.prefix_len
+            assert pp.extra.tolist() == op.extra_slots.tolist()
+            continue
+        match_all = ph.kind == "cache"
+        # a cache phase inserts its sequences one at a time (requests that finished earlier)
+        batches = [[s] for s in ph.seqs] if match_all else [ph.seqs]
+        for seqs in batches:
+            pp = pc.plan(seqs, match_all=match_all)
+            op = oc.extend_prepare(seqs, match_all=match_all)
+            assert pp.prefix_len.tolist() == op.prefix_len
+            for b, s in enumerate(seqs):
+                assert pp.rows[b, :len(s)].tolist() == op.rows[b].tolist()
+            assert (pp.evict_request, pp.evicted) == (op.evict_request, op.evicted)
+            _, dups = pc.finish(pp, keep_locked=ph.keep_locked)
+            oc.extend_finish(seqs, op, keep_locked=ph.keep_locked)
+            assert dups == op.freed_dups
+        np.testing.assert_array_equal(oc.tree.dump(), pc.tree.dump())
+    return pc, oc
+
+
+@pytest.mark.parametrize("name", ["tiny_extend", "few_shot_extend", "two_level_extend"])
+def test_extend_workloads_match_oracle(name):
+    w = W.CONFIGS[name]()
+    pc, oc = _run_phases_both(w)
+    assert pc.pool.available() == oc.pool.available()
+
+
+@pytest.mark.slow
+def test_multi_turn_decode_host_matches_oracle():
+    w = W.multi_turn_decode()
+    _run_phases_both(w)
+
+
+@pytest.mark.slow
+def test_fork_mixed_steps_host_match_oracle():
+    fm = W.fork_mixed_step()
+    w = fm.workload
+    pc, oc = _run_phases_both(w)
+    assert pc.pool.available() == 4096
+    for step in range(3):
+        ext = fm.extend_seqs(step)
+        pp = pc.plan(ext, extra=len(fm.decode_seqs))
+        op = oc.extend_prepare(ext, extra=len(fm.decode_seqs))
+        assert pp.prefix_len.tolist() == op.prefix_len == [1500] * 80
+        assert pp.evicted == op.evicted and pp.evicted >= 12032
+        assert pp.extra.tolist() == op.extra_slots.tolist()
+        pc.finish(pp)
+        oc.extend_finish(ext, op)
+        np.testing.assert_array_equal(oc.tree.dump(), pc.tree.dump())
