@@ -1,0 +1,471 @@
+"""Benchmark: prefix-cached paged attention on one GB300 (replicas across GPUs under torchrun).
+
+Default workload: the fork / self-consistency mixed step -- 32 layers of Llama-2-7B attention
+(32 x 128 MHA, bf16), a 300k-slot pool kept full so that LRU eviction runs every step, 16
+programs x 5 forks extending 200 new tokens over a cached 1500-token prefix, and 128 requests
+decoding over contexts of 512..8192 tokens. One step is the whole hot path: radix match + lock,
+LRU eviction, slot allocation, slot-table write, and per layer extend attention (with the K/V
+scatter) and split-K decode attention (with its merge), then insert + unlock.
+
+Prints one JSON line. `value` is extend-attention throughput in algorithmic TFLOP/s
+(4 * d * Hq * (S*P + S(S+1)/2) per request and layer) over the time the extend launches take
+inside the step; `decode` gives decode KV GB/s (L * (2 * Hkv * d * 2 B + 4 B) per request and
+layer) over the decode launches; `prefill_tokens_skipped` the matched-token count.
+
+--impl reference times the oracle (plain CPU C++, fp64) on the same workload and metric, a
+bounded sample of units per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "extend attn TFLOP/s & decode KV GB/s vs GB300 peak; prefill tokens skipped"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload: fork mixed step
+def extend_flops(P, S, Hq, d):
+    P = np.asarray(P, dtype=np.float64)
+    S = np.asarray(S, dtype=np.float64)
+    return float(np.sum(4.0 * d * Hq * (S * P + S * (S + 1) / 2)))
+
+
+def decode_bytes(seq_len, Hkv, d, elem=2):
+    return float(np.sum(np.asarray(seq_len, dtype=np.float64) * (2 * Hkv * d * elem + 4)))
+
+
+def setup_fork_mixed(args):
+    import torch
+    from synth import workloads as W
+    from tests import harness as H
+    import synth
+    from synth import device as sdev
+
+    fm = W.fork_mixed_step(layers=args.layers)
+    w = fm.workload
+    m = w.model
+    eng = H.make_engine(w, max_reqs=len(fm.decode_seqs) + 80 + 8, kv_chunk=args.kv_chunk)
+    t0 = time.time()
+    for ph in w.phases:
+        H.run_cache_phase(eng, m, ph.seqs, keep_locked=False)
+    db = eng.decode_begin([s[:-1] for s in fm.decode_seqs])
+    setup_s = time.time() - t0
+    assert eng.host.pool.available() == 4096, eng.host.pool.available()
+    # step inputs (identical values reused by every step: values do not change the work)
+    ext0 = fm.extend_seqs(0)
+    P0 = 1500
+    h_ext = np.concatenate([synth.prefix_hashes(m.seed, s)[P0:] for s in ext0])
+    hd_ext = sdev.hashes_to_device(h_ext)
+    T = len(h_ext)
+    h_dec = np.array([synth.prefix_hashes(m.seed, s)[-1] for s in fm.decode_seqs], np.uint64)
+    hd_dec = sdev.hashes_to_device(h_dec)
+    Bd = len(fm.decode_seqs)
+    dt = torch.bfloat16
+    xq = torch.empty((m.layers, T, m.n_q_heads, m.head_dim), dtype=dt, device="cuda")
+    xk = torch.empty((m.layers, T, m.n_kv_heads, m.head_dim), dtype=dt, device="cuda")
+    xv = torch.empty_like(xk)
+    dq = torch.empty((m.layers, Bd, m.n_q_heads, m.head_dim), dtype=dt, device="cuda")
+    dk = torch.empty((m.layers, Bd, m.n_kv_heads, m.head_dim), dtype=dt, device="cuda")
+    dv = torch.empty_like(dk)
+    for layer in range(m.layers):
+        sdev.fill_rows(hd_ext, synth.TENSOR_Q, layer, xq[layer])
+        sdev.fill_rows(hd_ext, synth.TENSOR_K, layer, xk[layer])
+        sdev.fill_rows(hd_ext, synth.TENSOR_V, layer, xv[layer])
+        sdev.fill_rows(hd_dec, synth.TENSOR_Q, layer, dq[layer])
+        sdev.fill_rows(hd_dec, synth.TENSOR_K, layer, dk[layer])
+        sdev.fill_rows(hd_dec, synth.TENSOR_V, layer, dv[layer])
+    xo = torch.empty((T, m.n_q_heads, m.head_dim), dtype=dt, device="cuda")
+    do = torch.empty((Bd, m.n_q_heads, m.head_dim), dtype=dt, device="cuda")
+    torch.cuda.synchronize()
+    n_steps = args.warmup + args.steps + 3   # + the end-to-end steps
+    seqs = [fm.extend_seqs(s) for s in range(n_steps)]
+    return dict(fm=fm, w=w, m=m, eng=eng, db=db, xq=xq, xk=xk, xv=xv, dq=dq, dk=dk, dv=dv,
+                xo=xo, do=do, T=T, Bd=Bd, seqs=seqs, setup_s=setup_s, ext0=ext0,
+                max_total=int(db.seq_len.sum()) + Bd * (n_steps + 1))
+
+
+def run_step(ctx, s, ev=None, host_t=None, e2e=None):
+    """One mixed step over batch s. ev: list of (start, after-extend, after-decode) CUDA events
+    per layer. e2e: host buffers (copies in and out inside the step)."""
+    eng, m, db = ctx["eng"], ctx["m"], ctx["db"]
+    t0 = time.perf_counter()
+    eb = eng.extend_begin(ctx["seqs"][s], extra=ctx["Bd"])
+    eng.decode_step(db, new_slots=eb.plan.extra)
+    t1 = time.perf_counter()
+    mt = ctx["max_total"]   # fixed bound: the workspace is sized once
+    for layer in range(m.layers):
+        if ev is not None:
+            ev[layer][0].record()
+        if e2e is not None:
+            for src, dst in ((e2e["xq"], ctx["xq"][0]), (e2e["xk"], ctx["xk"][0]),
+                             (e2e["xv"], ctx["xv"][0])):
+                dst.copy_(src, non_blocking=True)
+            xq, xk, xv = ctx["xq"][0], ctx["xk"][0], ctx["xv"][0]
+        else:
+            xq, xk, xv = ctx["xq"][layer], ctx["xk"][layer], ctx["xv"][layer]
+        eng.extend_layer(eb, layer, xq, xk, xv, ctx["xo"])
+        if e2e is not None:
+            e2e["xo"].copy_(ctx["xo"], non_blocking=True)
+        if ev is not None:
+            ev[layer][1].record()
+        if e2e is not None:
+            for src, dst in ((e2e["dq"], ctx["dq"][0]), (e2e["dk"], ctx["dk"][0]),
+                             (e2e["dv"], ctx["dv"][0])):
+                dst.copy_(src, non_blocking=True)
+            dq, dk, dv = ctx["dq"][0], ctx["dk"][0], ctx["dv"][0]
+        else:
+            dq, dk, dv = ctx["dq"][layer], ctx["dk"][layer], ctx["dv"][layer]
+        eng.decode_layer(db, layer, dq, dk, dv, ctx["do"], max_total_tokens=mt)
+        if e2e is not None:
+            e2e["do"].copy_(ctx["do"], non_blocking=True)
+        if ev is not None:
+            ev[layer][2].record()
+    t2 = time.perf_counter()
+    _, dups = eng.extend_end(eb)
+    t3 = time.perf_counter()
+    if host_t is not None:
+        host_t.append((t1 - t0) + (t3 - t2))
+    return eb
+
+
+def bench_ours(args, rank, world, local):
+    import torch
+    import prefix_cached_paged_gb300 as rc
+
+    ctx = setup_fork_mixed(args)
+    m, eng, db = ctx["m"], ctx["eng"], ctx["db"]
+    for s in range(args.warmup):
+        run_step(ctx, s)
+    torch.cuda.synchronize()
+
+    # ---------------- timed region (device-resident inputs)
+    S = [np.asarray(ctx["seqs"][args.warmup + k]) for k in range(args.steps)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(m.layers)]
+           for _ in range(args.steps)]
+    host_t = []
+    plans = []
+    seq_lens = []
+    launches0 = rc.launch_count()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for k in range(args.steps):
+        seq_lens.append(db.seq_len.copy() + 1)
+        plans.append(run_step(ctx, args.warmup + k, ev=evs[k], host_t=host_t))
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    launches = rc.launch_count() - launches0
+    total_ms = start.elapsed_time(end)
+    ext_ms = sum(e[l][0].elapsed_time(e[l][1]) for e in evs for l in range(m.layers))
+    dec_ms = sum(e[l][1].elapsed_time(e[l][2]) for e in evs for l in range(m.layers))
+    assert rc.device_status() == 0
+
+    # algorithmic work of the timed steps
+    ext_flops = 0.0
+    skipped = prompt = 0
+    for p in plans:
+        Pl = p.plan.prefix_len.astype(np.int64)
+        Sl = p.plan.lengths - Pl
+        ext_flops += extend_flops(Pl, Sl, m.n_q_heads, m.head_dim) * m.layers
+        skipped += int(Pl.sum())
+        prompt += int(p.plan.lengths.sum())
+    dec_bytes = sum(decode_bytes(sl, m.n_kv_heads, m.head_dim) * m.layers for sl in seq_lens)
+    total_ms = max_over_ranks(total_ms, world)
+    ext_ms_m = max_over_ranks(ext_ms, world)
+    dec_ms_m = max_over_ranks(dec_ms, world)
+    ext_tflops = world * ext_flops / (ext_ms_m * 1e-3) / 1e12
+    dec_gbs = world * dec_bytes / (dec_ms_m * 1e-3) / 1e9
+
+    # ---------------- end to end: inputs from pinned host memory, outputs back, every layer
+    e2e = None
+    if args.e2e:
+        T, Bd = ctx["T"], ctx["Bd"]
+        hb = {}
+        for name in ("xq", "xk", "xv", "dq", "dk", "dv"):
+            hb[name] = ctx[name][0].cpu().pin_memory()
+        hb["xo"] = torch.empty(ctx["xo"].shape, dtype=ctx["xo"].dtype).pin_memory()
+        hb["do"] = torch.empty(ctx["do"].shape, dtype=ctx["do"].dtype).pin_memory()
+        h2d = sum(hb[n].numel() * hb[n].element_size() for n in ("xq", "xk", "xv", "dq", "dk",
+                                                                    "dv")) * m.layers
+        d2h = (hb["xo"].numel() * 2 + hb["do"].numel() * 2) * m.layers
+        ne = max(1, min(args.steps, 3))
+        base = args.warmup + args.steps
+        eevs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                 for _ in range(m.layers)] for _ in range(ne)]
+        ef = 0.0
+        dbb = 0.0
+        torch.cuda.synchronize()
+        barrier(world)
+        for k in range(ne):
+            sl = db.seq_len.copy() + 1
+            p = run_step(ctx, base + k, ev=eevs[k], e2e=hb)
+            Pl = p.plan.prefix_len.astype(np.int64)
+            ef += extend_flops(Pl, p.plan.lengths - Pl, m.n_q_heads, m.head_dim) * m.layers
+            dbb += decode_bytes(sl, m.n_kv_heads, m.head_dim) * m.layers
+        torch.cuda.synchronize()
+        e_ext = max_over_ranks(sum(e[l][0].elapsed_time(e[l][1]) for e in eevs
+                                   for l in range(m.layers)), world)
+        e_dec = max_over_ranks(sum(e[l][1].elapsed_time(e[l][2]) for e in eevs
+                                   for l in range(m.layers)), world)
+        e2e = {"value": round(world * ef / (e_ext * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "decode_gbs": round(world * dbb / (e_dec * 1e-3) / 1e9, 1),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": ne,
+               "note": "per layer: H2D of that layer's q/k_new/v_new from pinned host memory, "
+                       "extend, D2H of its output; same for decode"}
+
+    pk = peaks()
+    dec_frac = dec_gbs / world / pk["hbm_gbs"]
+    ext_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # dominant kernel by time: decode (3 launches per call: plan, split-K main, merge)
+    dom_is_decode = dec_ms >= ext_ms
+    per_launch_dec_bytes = dec_bytes / (args.steps * m.layers)
+    dec_call_ms = dec_ms / (args.steps * m.layers)
+    ext_call_ms = ext_ms / (args.steps * m.layers)
+    roof_dec = {"kernel": "decode_attention (plan + split-K main + merge)", "bound": "hbm",
+                "achieved": round(per_launch_dec_bytes / (dec_call_ms * 1e-3) / 1e9, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(per_launch_dec_bytes / (dec_call_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                "traffic": args.traffic_decode, "peak_source": pk["source"] + " hbm_gbs"}
+    per_launch_ext = ext_flops / (args.steps * m.layers)
+    roof_ext = {"kernel": "extend_attention", "bound": "tensor",
+                "achieved": round(per_launch_ext / (ext_call_ms * 1e-3) / 1e12, 2),
+                "peak": ext_peak, "unit": "TFLOP/s",
+                "frac": round(per_launch_ext / (ext_call_ms * 1e-3) / 1e12 / ext_peak, 4),
+                "traffic": args.traffic_extend,
+                "peak_source": pk["source"] + " bf16_tflops_sustained"}
+    cpu = cpu_baseline(ctx, args) if (rank == 0 and world == 1 and args.cpu_baseline) else None
+    out = {
+        "metric": METRIC, "value": round(ext_tflops, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fork_mixed_step", "layers": m.layers, "heads": "32x128 MHA",
+                   "pool_slots": ctx["w"].pool_slots, "extend": "16 programs x 5 forks, P=1500, "
+                   "S=200", "decode": "128 requests, ctx 512..8192 uniform",
+                   "l2": "inputs larger than L2 (decode reads ~9 GB of KV per layer)",
+                   "parallelism": f"replicas x{world}", "kv_chunk": args.kv_chunk or 512},
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "frac_of_hbm": round(dec_frac, 4)},
+        "prefill_tokens_skipped": {"skipped": skipped, "prompt_tokens": prompt,
+                                   "hit_rate": round(skipped / max(prompt, 1), 4)},
+        "evicted_tokens_per_step": int(np.mean([p.plan.evicted for p in plans])),
+        "host_ms_per_step": round(1e3 * float(np.mean(host_t)), 3),
+        "extend_ms_per_step": round(ext_ms / args.steps, 3),
+        "decode_ms_per_step": round(dec_ms / args.steps, 3),
+        "roofline": roof_dec if dom_is_decode else roof_ext,
+        "roofline_extend": roof_ext, "roofline_decode": roof_dec,
+        "clocks": clk, "gpu_launches": int(launches), "e2e": e2e,
+        "cpu_baseline": cpu, "setup_s": round(ctx["setup_s"], 1),
+    }
+    return out
+
+
+def cpu_baseline(ctx, args, budget_s=None):
+    """The oracle, as it stands, on a bounded sample of the step's extend units (fp64 attention
+    of (request, layer, head) units on all host cores). Returns the metric in TFLOP/s."""
+    import oracle
+    import synth
+    m = ctx["m"]
+    seqs = ctx["ext0"]
+    budget_s = args.cpu_budget if budget_s is None else budget_s
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(7)
+    units, flops = [], 0.0
+    # one unit: a request's 200 queries of one head over 1700 keys
+    n_units = threads * 2
+    for _ in range(n_units):
+        b, layer, h = (int(rng.integers(len(seqs))), int(rng.integers(m.layers)),
+                       int(rng.integers(m.n_kv_heads)))
+        s = seqs[b]
+        hs = synth.prefix_hashes(m.seed, s)
+        P = 1500
+        q = synth.values(hs[P:], synth.TENSOR_Q, layer, [h], m.head_dim, m.dtype)
+        k = synth.values(hs, synth.TENSOR_K, layer, [h], m.head_dim, m.dtype)
+        v = synth.values(hs, synth.TENSOR_V, layer, [h], m.head_dim, m.dtype)
+        units.append((q, k, v, P))
+        flops += extend_flops([P], [len(s) - P], 1, m.head_dim)
+    t0 = time.perf_counter()
+    oracle.attention_units(units, m.sm_scale, 1, 1, threads)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while dt * (reps + 1) / reps < budget_s and reps < 8:
+        t1 = time.perf_counter()
+        oracle.attention_units(units, m.sm_scale, 1, 1, threads)
+        dt += time.perf_counter() - t1
+        reps += 1
+    return {"value": round(flops * reps / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n_units} extend units (request x layer x head: 200 queries over 1700 "
+                      f"keys, fp64) of the fork mixed step, x{reps} passes, {dt:.1f} s"}
+
+
+def bench_reference(args, rank, world):
+    """The oracle timed on the host cores, same workload and metric, bounded sample per step."""
+    if rank != 0:
+        return None
+    from synth import workloads as W
+    fm = W.fork_mixed_step(layers=args.layers)
+    ctx = {"m": fm.workload.model, "ext0": fm.extend_seqs(0)}
+    vals = []
+    per = max(2.0, args.ref_budget / max(args.steps + args.warmup, 1))
+    t0 = time.perf_counter()
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline(ctx, args, budget_s=per)
+        if k >= args.warmup:
+            vals.append(r)
+    total = time.perf_counter() - t0
+    v = float(np.mean([r["value"] for r in vals]))
+    return {"metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "impl": "reference",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / (args.warmup + args.steps), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "fork_mixed_step", "layers": args.layers},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": vals[0]["cores"], "sample": vals[0]["sample"]},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--kv-chunk", type=int, default=0)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--traffic-decode", type=float, default=None)
+    ap.add_argument("--traffic-extend", type=float, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        out = bench_reference(args, rank, world)
+    else:
+        import __graft_entry__
+        __graft_entry__.build()
+        out = bench_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

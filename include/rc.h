@@ -185,6 +185,7 @@ typedef struct rc_extend_args {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   int32_t head_dim;
+  int32_t max_reqs;          /* rows of req_to_token; every req_idx must be below it */
   int32_t max_ctx;           /* columns of req_to_token, multiple of 4 */
   int32_t max_q_len;         /* >= every S (host-known; sizes the grid) */
   int32_t max_prefix_len;    /* >= every P (host-known) */
@@ -221,7 +222,8 @@ typedef struct rc_decode_args {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   int32_t head_dim;
-  int32_t max_ctx;
+  int32_t max_reqs;          /* rows of req_to_token; every req_idx must be below it */
+  int32_t max_ctx;           /* columns of req_to_token */
   int32_t kv_chunk;          /* tokens per split, multiple of 64; 0 = library default */
   int64_t max_total_tokens;  /* >= sum of seq_len (host-known; sizes workspace and grid) */
   int64_t num_slots;

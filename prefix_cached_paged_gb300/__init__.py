@@ -196,7 +196,7 @@ def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_t
     Hkv = k_new.shape[1]
     return RcExtendArgs(
         dtype=_dtype_code(q), num_reqs=prefix_len.numel(), num_q_heads=Hq, num_kv_heads=Hkv,
-        head_dim=d, max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
+        head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
         max_prefix_len=int(max_prefix_len), num_tokens=T, num_slots=k_pool.shape[0],
         sm_scale=float(sm_scale), q=q.data_ptr(), k_new=k_new.data_ptr(),
         v_new=v_new.data_ptr(), out_loc=out_loc.data_ptr(), qo_indptr=qo_indptr.data_ptr(),
@@ -220,7 +220,7 @@ def _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_poo
     B, Hq, d = q.shape
     return RcDecodeArgs(
         dtype=_dtype_code(q), num_reqs=B, num_q_heads=Hq, num_kv_heads=k_new.shape[1],
-        head_dim=d, max_ctx=req_to_token.shape[1], kv_chunk=int(kv_chunk),
+        head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], kv_chunk=int(kv_chunk),
         max_total_tokens=int(max_total_tokens), num_slots=k_pool.shape[0],
         sm_scale=float(sm_scale), q=q.data_ptr(), k_new=k_new.data_ptr(),
         v_new=v_new.data_ptr(), out_loc=out_loc.data_ptr(), seq_len=seq_len.data_ptr(),
@@ -232,7 +232,8 @@ def _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_poo
 def decode_workspace_bytes(q, k_new, req_to_token, k_pool, *, max_total_tokens, kv_chunk=0) -> int:
     B, Hq, d = q.shape
     a = RcDecodeArgs(dtype=_dtype_code(q), num_reqs=B, num_q_heads=Hq,
-                     num_kv_heads=k_new.shape[1], head_dim=d, max_ctx=req_to_token.shape[1],
+                     num_kv_heads=k_new.shape[1], head_dim=d, max_reqs=req_to_token.shape[0],
+                     max_ctx=req_to_token.shape[1],
                      kv_chunk=int(kv_chunk), max_total_tokens=int(max_total_tokens),
                      num_slots=k_pool.shape[0])
     n = ctypes.c_size_t()

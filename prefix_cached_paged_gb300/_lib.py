@@ -64,8 +64,8 @@ class RcSlotWriteArgs(ctypes.Structure):
 
 class RcExtendArgs(ctypes.Structure):
     _fields_ = [("dtype", _I32), ("num_reqs", _I32), ("num_q_heads", _I32),
-                ("num_kv_heads", _I32), ("head_dim", _I32), ("max_ctx", _I32),
-                ("max_q_len", _I32), ("max_prefix_len", _I32), ("num_tokens", _I64),
+                ("num_kv_heads", _I32), ("head_dim", _I32), ("max_reqs", _I32),
+                ("max_ctx", _I32), ("max_q_len", _I32), ("max_prefix_len", _I32), ("num_tokens", _I64),
                 ("num_slots", _I64), ("sm_scale", ctypes.c_float), ("q", _P), ("k_new", _P),
                 ("v_new", _P), ("out_loc", _P), ("qo_indptr", _P), ("prefix_len", _P),
                 ("req_idx", _P), ("req_to_token", _P), ("k_pool", _P), ("v_pool", _P),
@@ -74,8 +74,8 @@ class RcExtendArgs(ctypes.Structure):
 
 class RcDecodeArgs(ctypes.Structure):
     _fields_ = [("dtype", _I32), ("num_reqs", _I32), ("num_q_heads", _I32),
-                ("num_kv_heads", _I32), ("head_dim", _I32), ("max_ctx", _I32),
-                ("kv_chunk", _I32), ("max_total_tokens", _I64), ("num_slots", _I64),
+                ("num_kv_heads", _I32), ("head_dim", _I32), ("max_reqs", _I32),
+                ("max_ctx", _I32), ("kv_chunk", _I32), ("max_total_tokens", _I64), ("num_slots", _I64),
                 ("sm_scale", ctypes.c_float), ("q", _P), ("k_new", _P), ("v_new", _P),
                 ("out_loc", _P), ("seq_len", _P), ("req_idx", _P), ("req_to_token", _P),
                 ("k_pool", _P), ("v_pool", _P), ("o", _P), ("lse", _P)]

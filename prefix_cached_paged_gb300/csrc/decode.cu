@@ -80,7 +80,8 @@ __global__ void decode_plan_kernel(Params p) {
     int n = 0;
     if (b < B) {
       const int L = p.a.seq_len[b];
-      if (L < 1 || L > p.a.max_ctx) {
+      const int row = p.a.req_idx[b];
+      if (L < 1 || L > p.a.max_ctx || row < 0 || row >= p.a.max_reqs) {
         set_status(p.status, kStatusPosRange);
       } else {
         n = (L + p.chunk - 1) / p.chunk;
@@ -419,7 +420,8 @@ __global__ void decode_merge_kernel(Params p) {
   const int b = blockIdx.x;
   const int hq = blockIdx.y;
   const int L = a.seq_len[b];
-  if (L < 1 || L > a.max_ctx) return;
+  const int row = a.req_idx[b];
+  if (L < 1 || L > a.max_ctx || row < 0 || row >= a.max_reqs) return;
   const int nchunks = (L + p.chunk - 1) / p.chunk;
   if (nchunks == 1) return;
   const int Hkv = a.num_kv_heads;
@@ -460,7 +462,7 @@ int validate(const rc_decode_args* a) {
   RC_CHECK_ARG(G == 1 || G == 2 || G == 4 || G == 8, "rc_decode_attention: group size %d", G);
   RC_CHECK_ARG(a->head_dim == 64 || a->head_dim == 128, "rc_decode_attention: head_dim %d",
                a->head_dim);
-  RC_CHECK_ARG(a->max_ctx > 0 && a->num_slots > 0 && a->max_total_tokens >= 0,
+  RC_CHECK_ARG(a->max_ctx > 0 && a->max_reqs > 0 && a->num_slots > 0 && a->max_total_tokens >= 0,
                "rc_decode_attention: bad sizes");
   RC_CHECK_ARG(a->kv_chunk == 0 || (a->kv_chunk > 0 && a->kv_chunk % 64 == 0),
                "rc_decode_attention: kv_chunk %d", a->kv_chunk);

@@ -14,8 +14,8 @@ extern "C" int rc_extend_attention(const rc_extend_args* a, void* stream) {
                "rc_extend_attention: bad head counts");
   RC_CHECK_ARG(a->head_dim == 128 || (a->dtype == RC_DTYPE_F32 && a->head_dim == 64),
                "rc_extend_attention: head_dim %d unsupported for this dtype", a->head_dim);
-  RC_CHECK_ARG(a->max_ctx > 0 && a->max_ctx % 4 == 0, "rc_extend_attention: max_ctx %d",
-               a->max_ctx);
+  RC_CHECK_ARG(a->max_ctx > 0 && a->max_ctx % 4 == 0 && a->max_reqs > 0,
+               "rc_extend_attention: max_ctx %d / max_reqs %d", a->max_ctx, a->max_reqs);
   RC_CHECK_ARG(a->max_q_len >= 0 && a->max_prefix_len >= 0 && a->num_tokens >= 0 &&
                    a->num_slots > 0,
                "rc_extend_attention: bad sizes");

@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(128) extend_simt_kernel(rc_extend_args a, int*
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads, G = Hq / Hkv;
   const int hk = hq / G;
   const int row = a.req_idx[b];
-  if (P < 0 || (int64_t)P + S > a.max_ctx) {
+  if (P < 0 || (int64_t)P + S > a.max_ctx || row < 0 || row >= a.max_reqs || qo < 0 ||
+      (int64_t)qo + S > a.num_tokens) {
     if (threadIdx.x == 0) set_status(status, kStatusPosRange);
     return;
   }

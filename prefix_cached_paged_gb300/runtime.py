@@ -138,12 +138,13 @@ class DeviceKV:
             off += n
         return out
 
-    def write_rows(self, row_ids, rows, lengths, cols=None):
-        """req_to_token[row_ids[b], cols[b] : cols[b] + lengths[b]] = rows[b, cols[b]:...]."""
+    def write_rows(self, row_ids, rows, ends, cols=None):
+        """req_to_token[row_ids[b], cols[b]:ends[b]] = rows[b, cols[b]:ends[b]] (cols default 0),
+        one upload and one slot-table kernel for the whole batch."""
         from . import slot_table_write
         B = len(row_ids)
-        cols = np.zeros(B, np.int64) if cols is None else np.asarray(cols)
-        seg_len = np.asarray(lengths, dtype=np.int64) - 0
+        cols = np.zeros(B, np.int64) if cols is None else np.asarray(cols, dtype=np.int64)
+        seg_len = np.asarray(ends, dtype=np.int64) - cols
         vals = [rows[b, cols[b]:cols[b] + seg_len[b]] for b in range(B)]
         indptr = np.zeros(B + 1, dtype=np.int64)
         np.cumsum(seg_len, out=indptr[1:])

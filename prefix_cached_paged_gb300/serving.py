@@ -1,0 +1,153 @@
+"""One model's prefix-cached paged attention state and its per-step calls.
+
+`Engine` ties the host pool and radix tree (HostCache) to the device KV planes and slot table
+(DeviceKV) and exposes the steps a scheduler runs, each a composition of librc calls:
+
+  extend_begin   plan a batch (match + lock, evict if short, allocate), write each request's slot
+                 row into the device slot table and upload the kernel metadata;
+  extend_layer   extend attention of one layer (scatters the new K/V into the pool);
+  extend_end     insert the sequences, free duplicate slots, unlock, release slot-table rows;
+  decode_begin   requests enter decoding: match their cached context, lock it, take a row;
+  decode_step    allocate one slot per request for its new token and write it to the row;
+  decode_layer   split-K decode attention of one layer;
+  decode_end     unlock and release rows.
+
+The model's projections (q, k_new, v_new per layer) are the caller's: this module never
+computes them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import decode_attention, decode_workspace_bytes, extend_attention
+from .runtime import DeviceKV, HostCache, Plan
+
+
+@dataclass
+class ExtendBatch:
+    plan: Plan
+    row_ids: np.ndarray
+    qo_indptr: object      # device int32 [B+1]
+    prefix_len: object     # device int32 [B]
+    req_idx: object        # device int32 [B]
+    out_loc: object        # device int32 [T]
+    max_q_len: int
+    max_prefix_len: int
+
+    @property
+    def num_tokens(self) -> int:
+        return self.plan.num_tokens
+
+
+@dataclass
+class DecodeBatch:
+    row_ids: np.ndarray
+    nodes: np.ndarray      # locked context nodes
+    seq_len: np.ndarray    # host int32 [B], including the current new token
+    new_slots: np.ndarray  # host int32 [B], slots of the current new tokens
+    dev_seq_len: object = None
+    dev_req_idx: object = None
+    dev_out_loc: object = None
+
+
+class Engine:
+    def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
+                 max_ctx, initial_order=None, device="cuda", kv_chunk=0):
+        self.layers = layers
+        self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
+        self.sm_scale = 1.0 / float(np.sqrt(head_dim))
+        self.host = HostCache(num_slots, max_ctx, initial_order)
+        self.dev = DeviceKV(layers, num_slots, n_kv_heads, head_dim, dtype, max_reqs, max_ctx,
+                            device)
+        self.max_ctx = max_ctx
+        self.kv_chunk = kv_chunk
+        self._free_rows = list(range(max_reqs - 1, -1, -1))
+        self._ws = None
+
+    # ---------------------------------------------------------------- rows
+    def _take_rows(self, n):
+        if n > len(self._free_rows):
+            raise RuntimeError(f"slot table has {len(self._free_rows)} free rows, {n} needed")
+        return np.array([self._free_rows.pop() for _ in range(n)], dtype=np.int32)
+
+    def _release_rows(self, rows):
+        self._free_rows.extend(int(r) for r in rows[::-1])
+
+    # ---------------------------------------------------------------- extend
+    def extend_begin(self, seqs, extra: int = 0, match_all: bool = False) -> ExtendBatch:
+        plan = self.host.plan(seqs, extra=extra, match_all=match_all)
+        B = len(seqs)
+        row_ids = self._take_rows(B)
+        self.dev.write_rows(row_ids, plan.rows, plan.lengths)
+        qo, pl, ri, ol = self.dev.upload_i32([plan.qo_indptr, plan.prefix_len, row_ids,
+                                              plan.out_loc])
+        S = plan.lengths - plan.prefix_len
+        return ExtendBatch(plan, row_ids, qo, pl, ri, ol, int(S.max()) if B else 0,
+                           int(plan.prefix_len.max()) if B else 0)
+
+    def extend_layer(self, batch: ExtendBatch, layer: int, q, k_new, v_new, o, lse=None):
+        extend_attention(q, k_new, v_new, batch.out_loc, batch.qo_indptr, batch.prefix_len,
+                         batch.req_idx, self.dev.req_to_token, self.dev.k[layer],
+                         self.dev.v[layer], o, sm_scale=self.sm_scale,
+                         max_q_len=batch.max_q_len, max_prefix_len=batch.max_prefix_len, lse=lse)
+
+    def extend_end(self, batch: ExtendBatch, keep_locked: bool = False):
+        ends, dups = self.host.finish(batch.plan, keep_locked=keep_locked)
+        self._release_rows(batch.row_ids)
+        return ends, dups
+
+    # ---------------------------------------------------------------- decode
+    def decode_begin(self, contexts) -> DecodeBatch:
+        """Requests enter decoding: each context must be cached; it is matched and locked, its
+        slots written to a fresh slot-table row. The first decode_step allocates the new tokens."""
+        plan = self.host.plan(contexts, match_all=True)
+        if plan.num_tokens:
+            self.host.pool.free(plan.out_loc)
+            for n in plan.nodes:
+                self.host.tree.unlock(int(n))
+            raise ValueError("decode_begin: every context must already be cached")
+        row_ids = self._take_rows(len(contexts))
+        self.dev.write_rows(row_ids, plan.rows, plan.lengths)
+        self._decode_plan = plan
+        return DecodeBatch(row_ids, plan.nodes, plan.lengths.astype(np.int32),
+                           np.zeros(len(contexts), np.int32))
+
+    def decode_step(self, batch: DecodeBatch, new_slots=None) -> DecodeBatch:
+        """Append one token per request: allocate its slot (evicting if needed) unless given,
+        write it to the request's row at position seq_len, and upload the step's metadata."""
+        B = len(batch.row_ids)
+        if new_slots is None:
+            new_slots = self.host.alloc(B)
+        cols = batch.seq_len.astype(np.int64)
+        rows = np.zeros((B, self.max_ctx), dtype=np.int32)
+        rows[np.arange(B), cols] = new_slots
+        self.dev.write_rows(batch.row_ids, rows, cols + 1, cols=cols)
+        batch.seq_len = batch.seq_len + 1
+        batch.new_slots = np.asarray(new_slots, dtype=np.int32)
+        batch.dev_seq_len, batch.dev_req_idx, batch.dev_out_loc = self.dev.upload_i32(
+            [batch.seq_len, batch.row_ids, batch.new_slots])
+        return batch
+
+    def workspace(self, q, k_new, max_total_tokens):
+        need = decode_workspace_bytes(q, k_new, self.dev.req_to_token, self.dev.k[0],
+                                      max_total_tokens=max_total_tokens, kv_chunk=self.kv_chunk)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = self.dev.torch.empty(need, dtype=self.dev.torch.uint8,
+                                            device=self.dev.device)
+        return self._ws
+
+    def decode_layer(self, batch: DecodeBatch, layer: int, q, k_new, v_new, o, lse=None,
+                     max_total_tokens=None):
+        mt = int(batch.seq_len.sum()) if max_total_tokens is None else max_total_tokens
+        ws = self.workspace(q, k_new, mt)
+        decode_attention(q, k_new, v_new, batch.dev_out_loc, batch.dev_seq_len,
+                         batch.dev_req_idx, self.dev.req_to_token, self.dev.k[layer],
+                         self.dev.v[layer], o, ws, sm_scale=self.sm_scale, max_total_tokens=mt,
+                         kv_chunk=self.kv_chunk, lse=lse)
+
+    def decode_end(self, batch: DecodeBatch):
+        for n in batch.nodes:
+            self.host.tree.unlock(int(n))
+        self._release_rows(batch.row_ids)

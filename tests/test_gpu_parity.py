@@ -1,0 +1,259 @@
+"""GPU path (librc through its C ABI) against the oracle, on seeded synthetic workloads.
+
+Bit-exact: match lengths / prefill tokens skipped, slot rows in the device slot table, and the
+pool rows the kernels scatter (compared with the generator's values). Within tolerance (bf16:
+max-abs 1e-2 and rel-L2 5e-3 against fp64; fp32: 1e-4 and 1e-5): attention outputs and LSE.
+Small cases compare every (request, layer, KV head) unit; the full-size workloads compare a
+seeded sample of units in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+
+import synth
+from synth import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _libs():
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    from synth import device as sdev
+    rc.lib()
+    sdev.build()
+    rc.device_status()  # clear
+    yield
+    torch.cuda.synchronize()
+
+
+def _status_clear():
+    import prefix_cached_paged_gb300 as rc
+    assert rc.device_status() == 0
+
+
+def _check_extend(w, batch, outs, seqs, units, lse_check=True):
+    m = w.model
+    qo = batch.plan.qo_indptr
+    P = batch.plan.prefix_len
+    worst = (0.0, 0.0)
+    for (b, layer, kvh) in units:
+        o_ref, lse_ref = H.oracle_unit(m, seqs[b], int(P[b]), layer, kvh)
+        o, l = outs[layer]
+        got = o[qo[b]:qo[b + 1], kvh * m.group:(kvh + 1) * m.group].float().cpu().numpy()
+        ok, ma, rl = H.compare(got, o_ref, m.dtype)
+        worst = (max(worst[0], ma), max(worst[1], rl))
+        assert ok, f"unit {(b, layer, kvh)} P={P[b]} S={qo[b+1]-qo[b]}: max-abs {ma} rel {rl}"
+        if lse_check and l is not None:
+            gl = l[qo[b]:qo[b + 1], kvh * m.group:(kvh + 1) * m.group].cpu().numpy()
+            assert np.max(np.abs(gl - lse_ref)) < (2e-3 if m.dtype == "bf16" else 1e-5)
+    return worst
+
+
+def _check_slot_rows(engine, batch):
+    rows = engine.dev.req_to_token.cpu().numpy()
+    for i, r in enumerate(batch.row_ids):
+        L = int(batch.plan.lengths[i])
+        np.testing.assert_array_equal(rows[r, :L], batch.plan.rows[i, :L])
+
+
+def _check_scatter(engine, w, seqs, batch, sample=None):
+    """Pool rows at the computed tokens' slots equal the generator's K/V values, bit for bit."""
+    m = w.model
+    hs = H.new_token_hashes(m, seqs, batch.plan.prefix_len)
+    slots = batch.plan.out_loc
+    idx = np.arange(len(slots)) if sample is None else sample
+    for layer in range(m.layers):
+        kk = engine.dev.k[layer][slots[idx]].cpu()
+        vv = engine.dev.v[layer][slots[idx]].cpu()
+        ek = synth.values_bits(hs[idx], synth.TENSOR_K, layer, range(m.n_kv_heads), m.head_dim,
+                               m.dtype)
+        ev = synth.values_bits(hs[idx], synth.TENSOR_V, layer, range(m.n_kv_heads), m.head_dim,
+                               m.dtype)
+        if m.dtype == "bf16":
+            kk = kk.view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+            vv = vv.view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+        else:
+            kk, vv = kk.numpy(), vv.numpy()
+        np.testing.assert_array_equal(kk, ek)
+        np.testing.assert_array_equal(vv, ev)
+
+
+def test_device_fill_matches_generator():
+    import torch
+    from synth import device as sdev
+    h = synth.prefix_hashes(3, synth.tokens(3, 9, 300))
+    hd = sdev.hashes_to_device(h)
+    for dt, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
+        out = torch.empty((300, 4, 128), dtype=tdt, device="cuda")
+        sdev.fill_rows(hd, synth.TENSOR_V, 5, out, head0=2)
+        exp = synth.values(h, synth.TENSOR_V, 5, range(2, 6), 128, dt)
+        np.testing.assert_array_equal(out.float().cpu().numpy(), exp)
+
+
+def test_tiny_extend_fp32_all_units():
+    w = W.tiny_extend()
+    eng = H.make_engine(w)
+    skipped = 0
+    for ph in w.phases:
+        b, outs = H.run_extend_phase(eng, w.model, ph.seqs, lse=True)
+        skipped += int(b.plan.prefix_len.sum())
+        units = [(i, 0, h) for i in range(len(ph.seqs)) for h in range(w.model.n_kv_heads)]
+        _check_extend(w, b, outs, ph.seqs, units)
+        _check_slot_rows(eng, b)
+        _check_scatter(eng, w, ph.seqs, b)
+    assert skipped == 192
+    _status_clear()
+
+
+def _custom_extend(Hq, Hkv, pairs, seed=11, dtype="bf16"):
+    """Requests with given (cached prefix P, new tokens S): phase 1 caches the prefixes, phase 2
+    extends all requests in one batch."""
+    m = W.Model(1, Hq, Hkv, 128, dtype, seed)
+    pre, seqs = [], []
+    for i, (P, S) in enumerate(pairs):
+        p = synth.tokens(seed, 500 + i, P)
+        s = synth.tokens(seed, 900 + i, S)
+        if P:
+            pre.append(p)
+        seqs.append(np.concatenate([p, s]).astype(np.int32))
+    L = max(len(s) for s in seqs)
+    w = W.Workload("custom", m, 40_000, synth.permutation(seed, 40_000), max_ctx=(L + 15) // 16 * 16)
+    w.phases = [W.Phase("cache", pre), W.Phase("extend", seqs)]
+    return w
+
+
+PAIRS = [(0, 1), (0, 130), (1, 1), (37, 64), (130, 129), (300, 7), (513, 200), (2, 257),
+         (128, 128), (255, 1)]
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 2), (16, 4)])
+def test_extend_bf16_ragged_all_units(Hq, Hkv):
+    w = _custom_extend(Hq, Hkv, PAIRS)
+    eng = H.make_engine(w)
+    H.run_cache_phase(eng, w.model, w.phases[0].seqs)
+    seqs = w.phases[1].seqs
+    b, outs = H.run_extend_phase(eng, w.model, seqs, lse=True)
+    assert b.plan.prefix_len.tolist() == [min(p, p + s - 1) for p, s in PAIRS]
+    units = [(i, 0, h) for i in range(len(seqs)) for h in range(Hkv)]
+    _check_extend(w, b, outs, seqs, units)
+    _check_slot_rows(eng, b)
+    _check_scatter(eng, w, seqs, b)
+    _status_clear()
+
+
+def _sample_units(rng, n_req, layers, n_kv, k):
+    return sorted({(int(rng.integers(n_req)), int(rng.integers(layers)), int(rng.integers(n_kv)))
+                   for _ in range(k)})
+
+
+def test_few_shot_extend_full_size_sampled():
+    w = W.few_shot_extend()
+    eng = H.make_engine(w)
+    H.run_extend_phase(eng, w.model, w.phases[0].seqs)   # warm: the prefix alone
+    seqs = w.phases[1].seqs
+    b, outs = H.run_extend_phase(eng, w.model, seqs, lse=True)
+    assert int(b.plan.prefix_len.sum()) == 128_000 and b.num_tokens == 3200
+    rng = np.random.default_rng(0)
+    _check_extend(w, b, outs, seqs, _sample_units(rng, 64, 1, 32, 40))
+    _check_slot_rows(eng, b)
+    _check_scatter(eng, w, seqs, b, sample=rng.choice(3200, 256, replace=False))
+    _status_clear()
+
+
+def test_two_level_extend_full_size_sampled():
+    w = W.two_level_extend()
+    eng = H.make_engine(w)
+    H.run_extend_phase(eng, w.model, w.phases[0].seqs)
+    H.run_extend_phase(eng, w.model, w.phases[1].seqs)
+    seqs = w.phases[2].seqs
+    b, outs = H.run_extend_phase(eng, w.model, seqs, lse=True)
+    v = w.notes["v"]
+    assert b.plan.prefix_len.tolist() == [1000 + v[i // 4] for i in range(64)]
+    rng = np.random.default_rng(1)
+    _check_extend(w, b, outs, seqs, _sample_units(rng, 64, 1, 8, 32))
+    _check_slot_rows(eng, b)
+    _check_scatter(eng, w, seqs, b, sample=rng.choice(b.num_tokens, 256, replace=False))
+    _status_clear()
+
+
+def _check_decode(w, db, outs, seqs, units):
+    m = w.model
+    for (b, layer, kvh) in units:
+        s = seqs[b]
+        o_ref, lse_ref = H.oracle_unit(m, s, len(s) - 1, layer, kvh)
+        o, l = outs[layer]
+        got = o[b, kvh * m.group:(kvh + 1) * m.group].float().cpu().numpy()[None]
+        ok, ma, rl = H.compare(got, o_ref, m.dtype)
+        assert ok, f"decode unit {(b, layer, kvh)} L={len(s)}: max-abs {ma} rel {rl}"
+        if l is not None:
+            gl = l[b, kvh * m.group:(kvh + 1) * m.group].cpu().numpy()
+            assert np.max(np.abs(gl - lse_ref[0])) < (2e-3 if m.dtype == "bf16" else 1e-5)
+
+
+def _decode_scatter(eng, w, seqs, db):
+    m = w.model
+    h = np.array([synth.prefix_hashes(m.seed, s)[-1] for s in seqs], dtype=np.uint64)
+    for layer in range(m.layers):
+        kk = eng.dev.k[layer][db.new_slots].float().cpu().numpy()
+        np.testing.assert_array_equal(
+            kk, synth.values(h, synth.TENSOR_K, layer, range(m.n_kv_heads), m.head_dim, m.dtype))
+
+
+@pytest.mark.parametrize("chunk", [0, 64, 192, 4096])
+def test_decode_small_all_units(chunk):
+    L = [1, 2, 63, 64, 65, 191, 192, 193, 700, 1500, 3000, 129]
+    m = W.Model(1, 32, 8, 128, "bf16", 5)
+    seqs = [synth.tokens(5, 40 + i, n) for i, n in enumerate(L)]
+    w = W.Workload("dec_small", m, 20_000, synth.permutation(5, 20_000), max_ctx=3008)
+    eng = H.make_engine(w, max_reqs=32, kv_chunk=chunk)
+    H.run_cache_phase(eng, m, [s[:-1] for s in seqs if len(s) > 1])
+    db, outs = H.run_decode(eng, m, seqs, lse=True)
+    _check_decode(w, db, outs, seqs, [(i, 0, h) for i in range(len(L)) for h in range(8)])
+    _decode_scatter(eng, w, seqs, db)
+    _status_clear()
+
+
+@pytest.mark.parametrize("Hq,Hkv,dtype,d", [(8, 8, "bf16", 128), (16, 2, "bf16", 128),
+                                            (8, 1, "bf16", 64), (4, 4, "f32", 128),
+                                            (4, 2, "f32", 64)])
+def test_decode_group_and_dtype_variants(Hq, Hkv, dtype, d):
+    L = [5, 300, 1030]
+    m = W.Model(2, Hq, Hkv, d, dtype, 6)
+    seqs = [synth.tokens(6, 60 + i, n) for i, n in enumerate(L)]
+    w = W.Workload("dec_var", m, 4000, None, max_ctx=1040)
+    eng = H.make_engine(w, max_reqs=8, kv_chunk=256)
+    H.run_cache_phase(eng, m, [s[:-1] for s in seqs])
+    db, outs = H.run_decode(eng, m, seqs, lse=True)
+    _check_decode(w, db, outs, seqs, [(i, l, h) for i in range(3) for l in range(2)
+                                      for h in range(Hkv)])
+    _status_clear()
+
+
+def test_multi_turn_decode_full_size_sampled():
+    w = W.multi_turn_decode()
+    eng = H.make_engine(w, max_reqs=264)
+    H.run_cache_phase(eng, w.model, w.phases[0].seqs)
+    seqs = w.phases[1].seqs
+    db, outs = H.run_decode(eng, w.model, seqs, lse=True)
+    rng = np.random.default_rng(2)
+    units = _sample_units(rng, 256, 1, 8, 48)
+    # always include the longest and the shortest request
+    Ls = np.array([len(s) for s in seqs])
+    units += [(int(Ls.argmax()), 0, 3), (int(Ls.argmin()), 0, 5)]
+    _check_decode(w, db, outs, seqs, units)
+    _decode_scatter(eng, w, seqs, db)
+    _status_clear()
+
+
+def test_multi_turn_decode_unshared_twin_sampled():
+    w0 = W.multi_turn_decode()
+    w = W.multi_turn_decode(shared=False, lengths=w0.notes["lengths"])
+    eng = H.make_engine(w, max_reqs=264)
+    H.run_cache_phase(eng, w.model, w.phases[0].seqs)
+    seqs = w.phases[1].seqs
+    db, outs = H.run_decode(eng, w.model, seqs)
+    rng = np.random.default_rng(3)
+    _check_decode(w, db, outs, seqs, _sample_units(rng, 256, 1, 8, 24))
+    _status_clear()
