@@ -15,6 +15,7 @@ App. A.2 batch formation):
 """
 from __future__ import annotations
 
+import time
 from dataclasses import dataclass
 
 import numpy as np
@@ -58,7 +59,16 @@ class HostCache:
                     self.tree.unlock(int(n))
                 raise RcError(rc, f"make room for {need} slots ({avail} free, {freed} evicted)")
 
+    host_seconds = 0.0   # accumulated time spent in the tree / pool calls of plan and finish
+
     def plan(self, seqs, extra: int = 0, match_all: bool = False) -> Plan:
+        t0 = time.perf_counter()
+        try:
+            return self._plan(seqs, extra, match_all)
+        finally:
+            self.host_seconds += time.perf_counter() - t0
+
+    def _plan(self, seqs, extra: int = 0, match_all: bool = False) -> Plan:
         seqs = [np.asarray(s, dtype=np.int32) for s in seqs]
         B = len(seqs)
         lengths = np.array([len(s) for s in seqs], dtype=np.int64)
@@ -85,8 +95,12 @@ class HostCache:
 
     def finish(self, plan: Plan, keep_locked: bool = False):
         """Insert, free duplicates, unlock. Returns (end nodes, duplicates freed)."""
-        return self.tree.insert_batch(plan.tokens, plan.indptr, plan.rows, plan.prefix_len,
-                                      plan.nodes, keep_locked)
+        t0 = time.perf_counter()
+        try:
+            return self.tree.insert_batch(plan.tokens, plan.indptr, plan.rows, plan.prefix_len,
+                                          plan.nodes, keep_locked)
+        finally:
+            self.host_seconds += time.perf_counter() - t0
 
     def alloc(self, n: int) -> np.ndarray:
         """n slots for decode tokens, evicting LRU leaves if the pool is short."""
@@ -110,8 +124,9 @@ class DeviceKV:
         self.v = torch.empty_like(self.k)
         self.req_to_token = torch.zeros((max_reqs, max_ctx), dtype=torch.int32,
                                         device=self.device)
-        self._stage = None
-        self._stage_event = None
+        self._ring = [None] * 8      # pinned staging buffers, reused round-robin
+        self._ring_ev = [None] * 8
+        self._ring_i = 0
 
     def upload_i32(self, arrays):
         """Copy int32 host arrays to the device in one transfer through a pinned staging buffer;
@@ -120,18 +135,22 @@ class DeviceKV:
         arrays = [np.ascontiguousarray(a, dtype=np.int32).ravel() for a in arrays]
         sizes = [len(a) for a in arrays]
         total = max(sum(sizes), 1)
-        if self._stage_event is not None:
-            self._stage_event.synchronize()
-        if self._stage is None or self._stage.numel() < total:
-            self._stage = torch.empty(max(total, 1 << 16), dtype=torch.int32, pin_memory=True)
-        host = self._stage.numpy()
+        i = self._ring_i
+        self._ring_i = (i + 1) % len(self._ring)
+        if self._ring_ev[i] is not None:
+            self._ring_ev[i].synchronize()   # the copy that last used this buffer is done
+        if self._ring[i] is None or self._ring[i].numel() < total:
+            self._ring[i] = torch.empty(max(total, 1 << 16), dtype=torch.int32, pin_memory=True)
+        stage = self._ring[i]
+        host = stage.numpy()
         off = 0
         for a in arrays:
             host[off:off + len(a)] = a
             off += len(a)
-        dev = self._stage[:total].to(self.device, non_blocking=True)
-        self._stage_event = torch.cuda.Event()
-        self._stage_event.record()
+        dev = stage[:total].to(self.device, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record()
+        self._ring_ev[i] = ev
         out, off = [], 0
         for n in sizes:
             out.append(dev[off:off + n])
