@@ -246,6 +246,24 @@ int rc_decode_workspace_bytes(const rc_decode_args* args, size_t* out_bytes);
 int rc_decode_attention(const rc_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/* Decode attention for callers that cannot allocate device memory. Some callers have no way
+ * to provide a workspace: a plugin interface that hands an operator only its input and output
+ * buffers, or a serving loop that forbids device allocation once it is running (an allocation
+ * can stall the whole device). This entry point takes the same arguments as
+ * rc_decode_attention but no workspace: its scratch lives in one fixed area of
+ * RC_DECODE_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * keeps until the process exits. It calls no allocator of any kind. The paper has no
+ * counterpart; this is a deployment convenience.
+ *   - Arguments whose scratch need (rc_decode_workspace_bytes) exceeds the area are rejected
+ *     with RC_ERR_INVALID; a larger kv_chunk needs less scratch.
+ *   - The first call on a device looks up the area's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the area and it keeps the last call's contents (everything
+ *     that must start at zero is reset by the call itself). Calls whose kernels overlap on the
+ *     GPU -- on different streams without ordering between them -- race on the area. */
+#define RC_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+int rc_decode_attention_noalloc(const rc_decode_args* args, void* stream);
+
 /* Read and clear the device status word of the current device (synchronises `stream`).
  * *out_code = 0 if no kernel reported bad data since the last call, else the first code seen:
  * 1 slot out of range, 2 position beyond the slot-table row, 3 a wait expired. */

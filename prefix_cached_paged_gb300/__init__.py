@@ -21,7 +21,7 @@ from ._lib import (RC_DTYPE_BF16, RC_DTYPE_F32, RC_ERR_CUDA, RC_ERR_DEVICE, RC_E
 
 __all__ = [
     "Pool", "RadixTree", "RcError", "slot_table_write", "extend_attention", "decode_attention",
-    "decode_workspace_bytes", "device_status", "launch_count", "RC_OK", "RC_ERR_INVALID",
+    "decode_workspace_bytes", "decode_attention_noalloc", "device_status", "launch_count", "RC_OK", "RC_ERR_INVALID",
     "RC_ERR_OOM", "RC_ERR_INSUFFICIENT", "RC_ERR_CUDA", "RC_ERR_DEVICE",
 ]
 
@@ -252,6 +252,21 @@ def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k
     check(lib().rc_decode_attention(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "rc_decode_attention")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def decode_attention_noalloc(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool,
+                             v_pool, o, *, sm_scale, max_total_tokens, kv_chunk=0, lse=None,
+                             stream=None):
+    """decode_attention without a workspace, for callers that cannot allocate device memory
+    (see rc_decode_attention_noalloc): its scratch is a fixed STATIC_SCRATCH_BYTES area inside
+    librc shared by every call on the device, so calls that overlap on the GPU race."""
+    a = _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
+                     o, lse, sm_scale, max_total_tokens, kv_chunk)
+    check(lib().rc_decode_attention_noalloc(ctypes.byref(a), _stream(stream)),
+          "rc_decode_attention_noalloc")
 
 
 def device_status(stream=None) -> int:

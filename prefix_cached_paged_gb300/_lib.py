@@ -46,6 +46,7 @@ SIGNATURES = {
     "rc_extend_attention": (ctypes.c_int, [_P, _P]),
     "rc_decode_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "rc_decode_attention": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
+    "rc_decode_attention_noalloc": (ctypes.c_int, [_P, _P]),
     "rc_device_status": (ctypes.c_int, [ctypes.POINTER(_I32), _P]),
 }
 

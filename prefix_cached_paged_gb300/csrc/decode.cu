@@ -553,3 +553,44 @@ extern "C" int rc_decode_attention(const rc_decode_args* a, void* workspace,
                               : rc::launch_g<__nv_bfloat16, 64>(p, G, s);
   return a->head_dim == 128 ? rc::launch_g<float, 128>(p, G, s) : rc::launch_g<float, 64>(p, G, s);
 }
+
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch for rc_decode_attention_noalloc: a fixed device array of this translation unit, so a
+// caller that cannot allocate still gets split-K decode. Its device address is looked up once
+// per device (host code may not use the symbol itself as a device pointer).
+namespace {
+__device__ __align__(256) unsigned char g_decode_scratch[RC_DECODE_STATIC_SCRATCH_BYTES];
+constexpr int kMaxScratchDevices = 64;
+void* g_decode_scratch_ptr[kMaxScratchDevices] = {};
+std::mutex g_decode_scratch_mu;
+}  // namespace
+
+extern "C" int rc_decode_attention_noalloc(const rc_decode_args* a, void* stream) {
+  const int v = rc::validate(a);
+  if (v != RC_OK) return v;
+  size_t need = 0;
+  const int rc0 = rc_decode_workspace_bytes(a, &need);
+  if (rc0 != RC_OK) return rc0;
+  if (need > RC_DECODE_STATIC_SCRATCH_BYTES)
+    return rc::fail(RC_ERR_INVALID,
+                    "rc_decode_attention_noalloc: these arguments need %zu bytes of scratch but the "
+                    "built-in area holds %zu; use a larger kv_chunk or rc_decode_attention",
+                    need, (size_t)RC_DECODE_STATIC_SCRATCH_BYTES);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices)
+    return rc::fail(RC_ERR_CUDA, "rc_decode_attention_noalloc: no usable current device");
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_decode_scratch_mu);
+    if (!g_decode_scratch_ptr[dev]) {
+      e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+      if (e != cudaSuccess)
+        return rc::fail(RC_ERR_CUDA, "rc_decode_attention_noalloc: scratch address lookup: %s",
+                        cudaGetErrorString(e));
+      g_decode_scratch_ptr[dev] = ptr;
+    }
+    ptr = g_decode_scratch_ptr[dev];
+  }
+  return rc_decode_attention(a, ptr, RC_DECODE_STATIC_SCRATCH_BYTES, stream);
+}
