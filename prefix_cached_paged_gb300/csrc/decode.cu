@@ -413,6 +413,296 @@ __global__ void __launch_bounds__(kWarps * 32) decode_main_kernel(Params p) {
   }
 }
 
+// ---------------------------------------------------------------- main, bf16 (warp-level MMA)
+// Same work split and ring as the CUDA-core kernel, but the two contractions of a stage run on
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate), which cuts the instruction count per KV row by
+// an order of magnitude so that the kernel stays bound by HBM, not by issue:
+//   S^T [16 tokens x 8] = K [16 tokens x d] . Q^T [d x 8]       (the G <= 8 query heads as N)
+//   O^T [d x 8]        += V^T [d x 16 tokens] . P^T [16 x 8]
+// K fragments by ldmatrix, V^T by ldmatrix.trans (both from 272-byte padded rows: conflict-free),
+// Q^T fragments held in registers for the whole item, P^T from the S^T accumulator by
+// movmatrix.trans. P is split into a bf16 high part and a bf16 remainder (two MMAs), so P.V
+// keeps ~16 bits of the fp32 probabilities.
+template <int D>
+struct MmaCfg {
+  static constexpr int RB = D * 2;               // bytes of one bf16 K or V row
+  static constexpr int RS = RB + 16;             // padded row stride in shared memory
+  static constexpr int STAGE = kTok * 2 * RS;    // K rows then V rows
+  static constexpr int RING = kStages * STAGE;
+  static constexpr int WARP_BYTES = (RING + kStages * 8 + 127) / 128 * 128;
+  static constexpr int SMEM = kWarps * WARP_BYTES;
+  static constexpr int KSTEPS = D / 16;
+  static_assert(kTok == 16, "one m16 tile of tokens per stage");
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *(const uint32_t*)&v;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
+  using C = MmaCfg<D>;
+  extern __shared__ __align__(128) char smem[];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  char* ring = smem + wid * C::WARP_BYTES;
+  uint64_t* bars = (uint64_t*)(ring + C::RING);
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint32_t ring_s = smem_u32(ring);
+
+  const rc_decode_args& a = p.a;
+  const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  const int n_items = p.w.njobs[0] * Hkv;
+  const float qscale = a.sm_scale * kLog2e;
+  const __nv_bfloat16* kpool = (const __nv_bfloat16*)a.k_pool;
+  const __nv_bfloat16* vpool = (const __nv_bfloat16*)a.v_pool;
+  uint32_t phases = 0;
+  // ldmatrix row addresses (per lane, relative to a stage): K as the A operand (token rows),
+  // V^T through the transposing load (token rows, d halves)
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8, k_col = (lane >> 4) * 8;
+  const int v_row = (lane & 7) + (lane >> 4) * 8, v_col = ((lane >> 3) & 1) * 8;
+
+  while (true) {
+    int item = 0;
+    if (lane == 0) item = atomicAdd(&p.w.njobs[1], 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (item >= n_items) break;
+    const int job = item / Hkv, h = item - job * Hkv;
+    const int2 bc = p.w.jobs[job];
+    const int b = bc.x, c = bc.y;
+    const int L = a.seq_len[b];
+    const int row = a.req_idx[b];
+    const int t0 = c * p.chunk;
+    const int t1 = min(L, t0 + p.chunk);
+    const int nchunks = (L + p.chunk - 1) / p.chunk;
+    const int nst = (t1 - t0 + kTok - 1) / kTok;
+    const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
+    const __nv_bfloat16* knew = (const __nv_bfloat16*)a.k_new + ((int64_t)b * Hkv + h) * D;
+    const __nv_bfloat16* vnew = (const __nv_bfloat16*)a.v_new + ((int64_t)b * Hkv + h) * D;
+
+    // slot of the token lane `lane` (< 16) copies in stage s: -2 = the new token (also used to
+    // fill the rows past the chunk end, so every shared row holds finite values)
+    auto slot_of = [&](int s) -> int {
+      const int pos = t0 + s * kTok + lane;
+      if (lane >= kTok) return -1;
+      if (pos >= t1 || pos == L - 1) return -2;
+      const int sl = rt[pos];
+      if (sl < 0 || (int64_t)sl >= a.num_slots) {
+        set_status(p.status, kStatusSlotRange);
+        return 0;
+      }
+      return sl;
+    };
+    auto issue = [&](int s, int sl) {
+      const int buf = s % kStages;
+      char* kd = ring + buf * C::STAGE + lane * C::RS;
+      char* vd = ring + buf * C::STAGE + kTok * C::RS + lane * C::RS;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[buf], kTok * 2u * C::RB);
+      __syncwarp();
+      if (lane < kTok) {
+        const __nv_bfloat16* ks = knew;
+        const __nv_bfloat16* vs = vnew;
+        if (sl >= 0) {
+          const int64_t r = ((int64_t)sl * Hkv + h) * D;
+          ks = kpool + r;
+          vs = vpool + r;
+        }
+        bulk_g2s(kd, ks, C::RB, &bars[buf]);
+        bulk_g2s(vd, vs, C::RB, &bars[buf]);
+      }
+    };
+
+    int next_slot = slot_of(0);
+    const int pro = min(nst, kStages - 1);
+    for (int s = 0; s < pro; ++s) {
+      issue(s, next_slot);
+      next_slot = slot_of(s + 1);
+    }
+    // Q^T fragments: column n = gid is query head h*G + gid (zero for gid >= G)
+    uint32_t qb[C::KSTEPS][2];
+    {
+      const __nv_bfloat16* qg = (const __nv_bfloat16*)a.q + ((int64_t)b * Hq + h * G + gid) * D;
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        qb[kk][0] = gid < G ? *(const uint32_t*)(qg + kk * 16 + tig * 2) : 0u;
+        qb[kk][1] = gid < G ? *(const uint32_t*)(qg + kk * 16 + tig * 2 + 8) : 0u;
+      }
+    }
+    float acc[C::KSTEPS][4];
+#pragma unroll
+    for (int i = 0; i < C::KSTEPS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*tig, 2*tig + 1
+
+    bool ok = true;
+    for (int s = 0; s < nst; ++s) {
+      if (s + kStages - 1 < nst) {
+        issue(s + kStages - 1, next_slot);
+        next_slot = slot_of(s + kStages);
+      }
+      const int buf = s % kStages;
+      if (!mbar_wait(&bars[buf], (phases >> buf) & 1u, p.status)) {
+        ok = false;
+        break;
+      }
+      phases ^= 1u << buf;
+      const uint32_t kb = ring_s + buf * C::STAGE;
+      const uint32_t vb = kb + kTok * C::RS;
+      // ---- S^T = K Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < C::KSTEPS; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kb + k_row * C::RS + (kk * 16 + k_col) * 2, a0, a1, a2, a3);
+        mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+      const int base_pos = t0 + s * kTok;
+      const bool v_lo = base_pos + gid < t1, v_hi = base_pos + gid + 8 < t1;
+      sc[0] = v_lo ? sc[0] * qscale : -INFINITY;
+      sc[1] = v_lo ? sc[1] * qscale : -INFINITY;
+      sc[2] = v_hi ? sc[2] * qscale : -INFINITY;
+      sc[3] = v_hi ? sc[3] * qscale : -INFINITY;
+      float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, o));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, o));
+      }
+      // lazy rescale: move the running max only when it grows by more than 2^8
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const bool r0 = n0 > m0 + 8.f, r1 = n1 > m1 + 8.f;
+      const float u0 = r0 ? n0 : m0, u1 = r1 ? n1 : m1;
+      const float al0 = (r0 && m0 != -INFINITY) ? exp2f(m0 - n0) : 1.f;
+      const float al1 = (r1 && m1 != -INFINITY) ? exp2f(m1 - n1) : 1.f;
+      m0 = u0;
+      m1 = u1;
+      const float p0 = exp2f(sc[0] - u0), p1 = exp2f(sc[1] - u1);
+      const float p2 = exp2f(sc[2] - u0), p3 = exp2f(sc[3] - u1);
+      l0 = l0 * al0 + p0 + p2;
+      l1 = l1 * al1 + p1 + p3;
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < C::KSTEPS; ++i) {
+          acc[i][0] *= al0;
+          acc[i][1] *= al1;
+          acc[i][2] *= al0;
+          acc[i][3] *= al1;
+        }
+      }
+      // ---- P^T fragments (high and remainder parts)
+      const uint32_t hx = bf2(p0, p1), hy = bf2(p2, p3);
+      const uint32_t lx = bf2(p0 - bf16lo(hx), p1 - bf16hi(hx));
+      const uint32_t ly = bf2(p2 - bf16lo(hy), p3 - bf16hi(hy));
+      const uint32_t bh0 = movm_t(hx), bh1 = movm_t(hy), bl0 = movm_t(lx), bl1 = movm_t(ly);
+      // ---- O^T += V^T P^T
+#pragma unroll
+      for (int i = 0; i < C::KSTEPS; ++i) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vb + v_row * C::RS + (i * 16 + v_col) * 2, a0, a1, a2, a3);
+        mma16816(acc[i], a0, a1, a2, a3, bh0, bh1);
+        mma16816(acc[i], a0, a1, a2, a3, bl0, bl1);
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      for (int s = 0; s < kStages; ++s)
+        mbar_wait(&bars[s], (phases >> s) & 1u, p.status, 100000000ull);
+      return;
+    }
+    // ---- epilogue: full denominators per head, then O^T columns -> output rows
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    const int hA = 2 * tig, hB = 2 * tig + 1;
+    const float iA = l0 > 0.f ? 1.f / l0 : 0.f, iB = l1 > 0.f ? 1.f / l1 : 0.f;
+    const float lseA = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
+    const float lseB = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+    if (nchunks == 1) {
+      __nv_bfloat16* o = (__nv_bfloat16*)a.o + ((int64_t)b * Hq + h * G) * D;
+#pragma unroll
+      for (int i = 0; i < C::KSTEPS; ++i) {
+        const int d0 = i * 16 + gid;
+        if (hA < G) {
+          o[hA * D + d0] = __float2bfloat16_rn(acc[i][0] * iA);
+          o[hA * D + d0 + 8] = __float2bfloat16_rn(acc[i][2] * iA);
+        }
+        if (hB < G) {
+          o[hB * D + d0] = __float2bfloat16_rn(acc[i][1] * iB);
+          o[hB * D + d0 + 8] = __float2bfloat16_rn(acc[i][3] * iB);
+        }
+      }
+      if (a.lse && gid == 0) {
+        if (hA < G) a.lse[(int64_t)b * Hq + h * G + hA] = lseA * kLn2;
+        if (hB < G) a.lse[(int64_t)b * Hq + h * G + hB] = lseB * kLn2;
+      }
+    } else {
+      const int64_t pi = (int64_t)item * G;
+#pragma unroll
+      for (int i = 0; i < C::KSTEPS; ++i) {
+        const int d0 = i * 16 + gid;
+        if (hA < G) {
+          p.w.po[(pi + hA) * D + d0] = acc[i][0] * iA;
+          p.w.po[(pi + hA) * D + d0 + 8] = acc[i][2] * iA;
+        }
+        if (hB < G) {
+          p.w.po[(pi + hB) * D + d0] = acc[i][1] * iB;
+          p.w.po[(pi + hB) * D + d0 + 8] = acc[i][3] * iB;
+        }
+      }
+      if (gid == 0) {
+        if (hA < G) p.w.plse[pi + hA] = lseA;
+        if (hB < G) p.w.plse[pi + hB] = lseB;
+      }
+    }
+    // ---- the last chunk scatters the new token's K and V rows into the pool
+    if (c == nchunks - 1) {
+      const int sl = a.out_loc[b];
+      if (sl < 0 || (int64_t)sl >= a.num_slots) {
+        if (lane == 0) set_status(p.status, kStatusSlotRange);
+      } else {
+        const int64_t r = ((int64_t)sl * Hkv + h) * D;
+        for (int e = lane; e < C::RB / 16; e += 32) {
+          ((uint4*)((__nv_bfloat16*)a.k_pool + r))[e] = ((const uint4*)knew)[e];
+          ((uint4*)((__nv_bfloat16*)a.v_pool + r))[e] = ((const uint4*)vnew)[e];
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // ---------------------------------------------------------------- merge
 template <typename T, int D, int G>
 __global__ void decode_merge_kernel(Params p) {
@@ -470,9 +760,20 @@ int validate(const rc_decode_args* a) {
 }
 
 template <typename T, int D, int G>
+struct MainKernel {
+  static constexpr int SMEM = Cfg<T, D, G>::SMEM;
+  static constexpr auto fn = decode_main_kernel<T, D, G>;
+};
+template <int D, int G>
+struct MainKernel<__nv_bfloat16, D, G> {
+  static constexpr int SMEM = MmaCfg<D>::SMEM;
+  static constexpr auto fn = decode_mma_kernel<D, G>;
+};
+
+template <typename T, int D, int G>
 int launch_t(const Params& p, cudaStream_t s) {
-  using C = Cfg<T, D, G>;
-  auto kern = decode_main_kernel<T, D, G>;
+  using C = MainKernel<T, D, G>;
+  auto kern = C::fn;
   static int blocks_per_sm = -1;
   static int num_sms = 0;
   static std::once_flag once;

@@ -253,6 +253,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
+    // slots of this lane's 4 keys of prefix tile j (invalid ones replaced by slot 0 and reported)
+    auto load_slots = [&](int j, int* sl) {
+      const int k0 = j * kN + lane * 4;
+      if (k0 + 3 < P) {
+        const int4 v4 = *(const int4*)(rt + k0);
+        sl[0] = v4.x; sl[1] = v4.y; sl[2] = v4.z; sl[3] = v4.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sl[u] = (k0 + u < P) ? rt[k0 + u] : rt[0];
+      }
+    };
+    int nxt[4] = {0, 0, 0, 0};
+    if (n_pre > 0) load_slots(0, nxt);
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
@@ -261,15 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* mk;
       const CUtensorMap* mv;
       if (j < n_pre) {
-        const int k0 = j * kN + lane * 4;
-        int sl[4];
-        if (k0 + 3 < P) {
-          const int4 v4 = *(const int4*)(rt + k0);
-          sl[0] = v4.x; sl[1] = v4.y; sl[2] = v4.z; sl[3] = v4.w;
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) sl[u] = (k0 + u < P) ? rt[k0 + u] : rt[0];
-        }
+        int sl[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (j + 1 < n_pre) load_slots(j + 1, nxt);   // in flight while this tile is issued
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (sl[u] < 0 || (int64_t)sl[u] >= a.num_slots) {
@@ -352,21 +358,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && ntiles > 0) pv(ntiles - 1);
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ scatter of the new K/V rows
+    // 64 threads copy (row, 16-byte chunk) pairs; each round issues all of a thread's loads
+    // before any store so that eight copies are in flight per thread.
     const int t = threadIdx.x - 64;
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-    for (int e = t; e < npos * 16; e += 64) {
-      const int i = i0 + (e >> 4), c = e & 15;
-      const int64_t tok = qo + i;
-      const int sl = a.out_loc[tok];
-      if (sl < 0 || (int64_t)sl >= a.num_slots) {
-        if (c == 0) set_status(p.status, kStatusSlotRange);
-        continue;
+    constexpr int kU = 8;
+    const int total = npos * 16;
+    for (int base = t; base < total; base += 64 * kU) {
+      uint4 kv[kU], vv[kU];
+      int64_t dst[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = base + u * 64;
+        dst[u] = -1;
+        if (e < total) {
+          const int i = i0 + (e >> 4), c = e & 15;
+          const int64_t tok = qo + i;
+          const int sl = a.out_loc[tok];
+          const int64_t src = (tok * Hkv + hk) * kD + c * 8;
+          kv[u] = *(const uint4*)(kn + src);
+          vv[u] = *(const uint4*)(vn + src);
+          if (sl >= 0 && (int64_t)sl < a.num_slots)
+            dst[u] = ((int64_t)sl * Hkv + hk) * kD + c * 8;
+          else if (c == 0)
+            set_status(p.status, kStatusSlotRange);
+        }
       }
-      const int64_t src = (tok * Hkv + hk) * kD + c * 8;
-      const int64_t dst = ((int64_t)sl * Hkv + hk) * kD + c * 8;
-      *(uint4*)((__nv_bfloat16*)a.k_pool + dst) = *(const uint4*)(kn + src);
-      *(uint4*)((__nv_bfloat16*)a.v_pool + dst) = *(const uint4*)(vn + src);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (dst[u] >= 0) {
+          *(uint4*)((__nv_bfloat16*)a.k_pool + dst[u]) = kv[u];
+          *(uint4*)((__nv_bfloat16*)a.v_pool + dst[u]) = vv[u];
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup
@@ -374,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int rows_used = npos * G;
     const int ipos = min(i0 + r / G, S - 1);          // this row's new-token index (clamped)
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     uint8_t* pbase = smem + SmemLayout::P;
     for (int j = 0; j < ntiles; ++j) {
@@ -406,15 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
       const float alpha = (rescale && m_run != -INFINITY) ? exp2f(m_run - m_new) : 1.f;
-      float rs = 0.f;
+      float rs = 0.f, re = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = exp2f(s[2 * c] - m_use);
         const float p1 = exp2f(s[2 * c + 1] - m_use);
         pk[c] = pack_bf16(p0, p1);
-        // the denominator sums the rounded weights P.V uses, so the weights stay normalised
+        // O is normalised by the sum of the rounded weights P.V uses (so they stay normalised);
+        // the log-sum-exp output uses the exact sum
         rs += bf16lo(pk[c]) + bf16hi(pk[c]);
+        re += p0 + p1;
       }
       // P[j&1] was read by the P.V of tile j-2; O is touched only after P.V of tile j-1
       if (j >= 2) {
@@ -440,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
       }
       l_run = l_run * alpha + rs;
+      l_exact = l_exact * alpha + re;
       m_run = m_use;
       uint8_t* prow = pbase + sb * kTileBytes;
 #pragma unroll
@@ -478,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (store && a.lse) a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_run)) * kLn2;
+      if (store && a.lse) a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
     }
   }
   // drain: every tcgen05 op issued by warp 1 has completed once o_done / s_full of the last
