@@ -9,18 +9,21 @@
 // req_to_token, rows gathered from the pool), then the new tokens (rows of k_new / v_new), the
 // causal mask applied only where a tile crosses the diagonal.
 //
-// Warp roles (256 threads):
-//   warp 0      producer: per key tile, 32 lanes each gather 4 rows x 2 column blocks with TMA
-//               tile::gather4 (box 64 columns x 1 row, 128-byte swizzle) into K and V stages;
-//   warp 1      allocates TMEM and issues every tcgen05.mma from one lane:
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3   producers: gather the key tile's K and V rows (256 B each, one slot per row) with
+//               16-byte cp.async copies straight into the 128-byte-swizzled operand layout, two
+//               rows per warp instruction (fully coalesced); completion is signalled on the
+//               stage's mbarrier with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves
+//               only 512 B per instruction and, measured here, its issue rate capped a 256-byte
+//               row gather at about 2 TB/s for the whole GPU; the copy engine path does not.)
+//   warp 4      allocates TMEM and issues every tcgen05.mma from one lane:
 //               S[j%2] = Q K_j^T (M=128, N=128, K=128; fp32 in TMEM), then O += P_{j-1} V_{j-1};
-//   warps 2-3   scatter the tile's new K/V rows into their pool slots;
-//   warps 4-7   softmax, one thread per query row (TMEM lane): scores from TMEM, online softmax
-//               in base 2 with a lazy rescale of O (only when the running max grows by > 8),
-//               P as bf16 into shared memory (the A operand of P V), epilogue O / l.
+//   warps 5-7   scatter the tile's new K/V rows into their pool slots;
+//   warps 8-11  softmax, one thread per query row (TMEM lane), two passes over the score row
+//               (max, then exp2 with the scale folded into one FMA), lazy rescale of O (only
+//               when the running max grows by > 8 in log2 units), P as bf16 into shared memory
+//               (the A operand of P V), epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
-#include <cuda.h>
-
 #include <mutex>
 
 #include "device_common.cuh"
@@ -36,7 +39,10 @@ constexpr int kN = 128;           // keys per tile
 constexpr int kStagesKV = 2;
 constexpr int kTileBytes = kM * kD * 2;   // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int kBlockBytes = kM * 128;     // 16 KB: one 64-column block of a tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kProducers = 128;          // warps 0-3
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmax0 = 256;           // first softmax thread (warps 8-11)
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
 
 struct SmemLayout {
@@ -62,13 +68,16 @@ struct TcParams {
 };
 
 // ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -162,11 +171,7 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 }
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kThreads, 1)
-    extend_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tk_pool,
-                     const __grid_constant__ CUtensorMap tv_pool,
-                     const __grid_constant__ CUtensorMap tk_new,
-                     const __grid_constant__ CUtensorMap tv_new) {
+__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte swizzled operand tiles must start on 1024-byte boundaries
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -212,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
+      mbar_init(&k_full[s], kProducers);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&v_full[s], kProducers);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 128);
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
                      smem_u32(tmem_slot))
                  : "memory");
@@ -250,67 +255,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS0 = tmem, tO = tmem + 256;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < 4) {
+    // ------------------------------------------------------------ producers (warps 0-3)
+    // Warp w fills rows [32w, 32w + 32) of each tile. Lane l resolves the source row of tile row
+    // 32w + l; one copy instruction then moves 16-byte chunk (l & 15) of rows 2i and 2i + 1.
     const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
-    // slots of this lane's 4 keys of prefix tile j (invalid ones replaced by slot 0 and reported)
-    auto load_slots = [&](int j, int* sl) {
-      const int k0 = j * kN + lane * 4;
-      if (k0 + 3 < P) {
-        const int4 v4 = *(const int4*)(rt + k0);
-        sl[0] = v4.x; sl[1] = v4.y; sl[2] = v4.z; sl[3] = v4.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sl[u] = (k0 + u < P) ? rt[k0 + u] : rt[0];
+    const __nv_bfloat16* kp = (const __nv_bfloat16*)a.k_pool;
+    const __nv_bfloat16* vp = (const __nv_bfloat16*)a.v_pool;
+    const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
+    const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
+    const int myrow = warp * 32 + lane;
+    // source row index: slot * Hkv + hk in the pool, or token * Hkv + hk in k_new / v_new
+    auto src_row = [&](int j) -> int {
+      if (j < n_pre) {
+        const int key = j * kN + myrow;
+        int sl = rt[key < P ? key : P - 1];
+        if (sl < 0 || (int64_t)sl >= a.num_slots) {
+          set_status(p.status, kStatusSlotRange);
+          sl = 0;
+        }
+        return sl * Hkv + hk;
       }
+      const int s0 = (j - n_pre) * kN + myrow;
+      return (qo + min(s0, S - 1)) * Hkv + hk;
     };
-    int nxt[4] = {0, 0, 0, 0};
-    if (n_pre > 0) load_slots(0, nxt);
+    int nxt = src_row(0);
     bool ok = true;
+    const int c = lane & 15, half = lane >> 4;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
       const uint32_t par_empty = ((j >> 1) - 1) & 1;
-      int r[4];
-      const CUtensorMap* mk;
-      const CUtensorMap* mv;
-      if (j < n_pre) {
-        int sl[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
-        if (j + 1 < n_pre) load_slots(j + 1, nxt);   // in flight while this tile is issued
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (sl[u] < 0 || (int64_t)sl[u] >= a.num_slots) {
-            set_status(p.status, kStatusSlotRange);
-            sl[u] = 0;
-          }
-          r[u] = sl[u] * Hkv + hk;
-        }
-        mk = &tk_pool;
-        mv = &tv_pool;
-      } else {
-        const int s0 = (j - n_pre) * kN + lane * 4;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) r[u] = (qo + min(s0 + u, S - 1)) * Hkv + hk;
-        mk = &tk_new;
-        mv = &tv_new;
-      }
+      const int cur = nxt;
+      const bool pre = j < n_pre;
+      if (j + 1 < ntiles) nxt = src_row(j + 1);  // in flight while this tile is issued
+      const __nv_bfloat16* kb = pre ? kp : kn;
+      const __nv_bfloat16* vb = pre ? vp : vn;
       if (j >= kStagesKV) ok = mbar_wait(&k_empty[st], par_empty, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-      __syncwarp();
-      const uint32_t kdst = sK + st * kTileBytes + lane * 4 * 128;
-      tma_gather4(kdst, mk, 0, r[0], r[1], r[2], r[3], smem_u32(&k_full[st]));
-      tma_gather4(kdst + kBlockBytes, mk, 64, r[0], r[1], r[2], r[3], smem_u32(&k_full[st]));
+      const uint32_t kdst = sK + st * kTileBytes;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int rr = 2 * i + half;
+        const int src = __shfl_sync(0xffffffffu, cur, rr);
+        cp_async16(kdst + sw128_off(warp * 32 + rr, c), kb + (int64_t)src * kD + c * 8);
+      }
+      cp_async_arrive_noinc(smem_u32(&k_full[st]));
       if (j >= kStagesKV) ok = mbar_wait(&v_empty[st], par_empty, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-      __syncwarp();
-      const uint32_t vdst = sV + st * kTileBytes + lane * 4 * 128;
-      tma_gather4(vdst, mv, 0, r[0], r[1], r[2], r[3], smem_u32(&v_full[st]));
-      tma_gather4(vdst + kBlockBytes, mv, 64, r[0], r[1], r[2], r[3], smem_u32(&v_full[st]));
+      const uint32_t vdst = sV + st * kTileBytes;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int rr = 2 * i + half;
+        const int src = __shfl_sync(0xffffffffu, cur, rr);
+        cp_async16(vdst + sw128_off(warp * 32 + rr, c), vb + (int64_t)src * kD + c * 8);
+      }
+      cp_async_arrive_noinc(smem_u32(&v_full[st]));
     }
-  } else if (warp == 1) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
     bool ok = true;
@@ -318,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pb = t & 1, st = t & 1;
       if (!mbar_wait(&p_full[pb], (t >> 1) & 1, p.status)) return false;
       if (!mbar_wait(&v_full[st], (t >> 1) & 1, p.status)) return false;
+      fence_async_smem();   // V arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -340,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && j >= 2) ok = mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      fence_async_smem();   // K arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -356,21 +362,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= 1) ok = __all_sync(0xffffffffu, pv(j - 1));
     }
     if (ok && ntiles > 0) pv(ntiles - 1);
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ scatter of the new K/V rows
-    // 64 threads copy (row, 16-byte chunk) pairs; each round issues all of a thread's loads
-    // before any store so that eight copies are in flight per thread.
-    const int t = threadIdx.x - 64;
+    // 96 threads copy (row, 16-byte chunk) pairs; each round issues all of a thread's loads
+    // before any store so that four copies are in flight per thread.
+    const int t = threadIdx.x - 160;
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-    constexpr int kU = 8;
+    constexpr int kU = 4;
     const int total = npos * 16;
-    for (int base = t; base < total; base += 64 * kU) {
+    for (int base = t; base < total; base += 96 * kU) {
       uint4 kv[kU], vv[kU];
       int64_t dst[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int e = base + u * 64;
+        const int e = base + u * 96;
         dst[u] = -1;
         if (e < total) {
           const int i = i0 + (e >> 4), c = e & 15;
@@ -395,10 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup
-    const int r = threadIdx.x - 128;                  // query row = TMEM lane
+    const int r = threadIdx.x - kSoftmax0;            // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int rows_used = npos * G;
     const int ipos = min(i0 + r / G, S - 1);          // this row's new-token index (clamped)
+    const float sc2 = p.scale2;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     uint8_t* pbase = smem + SmemLayout::P;
@@ -408,47 +415,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[128];
+      // keys [0, lim) of this tile are visible to this row
+      const int lim = j < n_pre ? min(kN, P - j * kN) : min(kN, ipos - (j - n_pre) * kN + 1);
+      const uint32_t tS = tS0 + sb * 128 + lane_off;
+      // pass 1: row max of the raw scores
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tS + c * 32, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS0 + sb * 128 + lane_off + c * 32, s + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-      // mask and scale; tile max
-      int lim;  // keys [0, lim) of this tile are visible to this row
-      if (j < n_pre) {
-        lim = min(kN, P - j * kN);
-      } else {
-        lim = min(kN, ipos - (j - n_pre) * kN + 1);
+        for (int u = 0; u < 32; ++u) mx = fmaxf(mx, c * 32 + u < lim ? v[u] : -INFINITY);
       }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = c < lim ? s[c] * p.scale2 : -INFINITY;
-        mt = fmaxf(mt, s[c]);
-      }
+      const float mt = mx * sc2;                      // sc2 > 0: max commutes with the scale
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
-      const float alpha = (rescale && m_run != -INFINITY) ? exp2f(m_run - m_new) : 1.f;
-      float rs = 0.f, re = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = exp2f(s[2 * c] - m_use);
-        const float p1 = exp2f(s[2 * c + 1] - m_use);
-        pk[c] = pack_bf16(p0, p1);
-        // O is normalised by the sum of the rounded weights P.V uses (so they stay normalised);
-        // the log-sum-exp output uses the exact sum
-        rs += bf16lo(pk[c]) + bf16hi(pk[c]);
-        re += p0 + p1;
-      }
-      // P[j&1] was read by the P.V of tile j-2; O is touched only after P.V of tile j-1
+      const float alpha = (rescale && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+      const float neg = -m_use;
+      // P[j&1] was read by the P.V of tile j-2
       if (j >= 2) {
         ok = mbar_wait(&o_done[sb], ((j >> 1) - 1) & 1, p.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
+      // pass 2: weights, written as bf16 into the P operand tile
+      float rs = 0.f, re = 0.f;
+      uint8_t* prow = pbase + sb * kTileBytes;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tS + c * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int k0 = c * 32 + 2 * u;
+          const float p0 = ex2(k0 < lim ? fmaf(v[2 * u], sc2, neg) : -INFINITY);
+          const float p1 = ex2(k0 + 1 < lim ? fmaf(v[2 * u + 1], sc2, neg) : -INFINITY);
+          pk[u] = pack_bf16(p0, p1);
+          // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp
+          // output uses the exact sum
+          rs += bf16lo(pk[u]) + bf16hi(pk[u]);
+          re += p0 + p1;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *(uint4*)(prow + sw128_off(r, c * 4 + q4)) =
+              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+      // O is touched only after the P.V of tile j-1
       const bool any_rescale = __any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0;
       if (any_rescale) {
         ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
@@ -469,11 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + rs;
       l_exact = l_exact * alpha + re;
       m_run = m_use;
-      uint8_t* prow = pbase + sb * kTileBytes;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *(uint4*)(prow + sw128_off(r, c)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[sb]);
@@ -506,53 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (store && a.lse) a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
+      if (store && a.lse)
+        a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
     }
   }
-  // drain: every tcgen05 op issued by warp 1 has completed once o_done / s_full of the last
-  // tiles were observed; make sure before freeing TMEM
+  // every tcgen05 op has completed once the softmax observed the last o_done; free TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
-}
-
-// ---------------------------------------------------------------- host side
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeFn)p;
-  });
-  return fn;
-}
-
-// rows x 128 bf16 matrix, gathered one row at a time in 64-column boxes with 128-byte swizzle
-int make_row_map(CUtensorMap* m, const void* base, int64_t rows) {
-  EncodeFn fn = encode_fn();
-  if (!fn) return fail(RC_ERR_CUDA, "extend: cuTensorMapEncodeTiled unavailable");
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(RC_ERR_CUDA, "extend: tensor map encode failed (%d)", (int)r);
-  return RC_OK;
 }
 
 }  // namespace
@@ -569,21 +547,13 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   });
   if (attr_err != cudaSuccess)
     return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(attr_err));
-  CUtensorMap mk, mv, mkn, mvn;
-  const int64_t pool_rows = a->num_slots * a->num_kv_heads;
-  const int64_t new_rows = a->num_tokens * a->num_kv_heads;
-  int rc;
-  if ((rc = make_row_map(&mk, a->k_pool, pool_rows)) != RC_OK) return rc;
-  if ((rc = make_row_map(&mv, a->v_pool, pool_rows)) != RC_OK) return rc;
-  if ((rc = make_row_map(&mkn, a->k_new, new_rows)) != RC_OK) return rc;
-  if ((rc = make_row_map(&mvn, a->v_new, new_rows)) != RC_OK) return rc;
   TcParams p;
   p.a = *a;
   p.status = status;
   p.ppt = kM / G;
   p.scale2 = a->sm_scale * kLog2e;
   dim3 grid((a->max_q_len + p.ppt - 1) / p.ppt, a->num_kv_heads, a->num_reqs);
-  extend_tc_kernel<<<grid, kThreads, SmemLayout::ALLOC, s>>>(p, mk, mv, mkn, mvn);
+  extend_tc_kernel<<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
   count_launches(1);
   return check_launch("rc_extend_attention (tensor cores)");
 }
