@@ -512,19 +512,22 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
     const __nv_bfloat16* vnew = (const __nv_bfloat16*)a.v_new + ((int64_t)b * Hkv + h) * D;
 
     // slot of the token lane `lane` (< 16) copies in stage s: -2 = the new token (also used to
-    // fill the rows past the chunk end, so every shared row holds finite values)
+    // fill the rows past the chunk end, so every shared row holds finite values). The load is
+    // only issued here; issue() checks the value, so it stays in flight for a stage.
     auto slot_of = [&](int s) -> int {
       const int pos = t0 + s * kTok + lane;
       if (lane >= kTok) return -1;
       if (pos >= t1 || pos == L - 1) return -2;
-      const int sl = rt[pos];
-      if (sl < 0 || (int64_t)sl >= a.num_slots) {
-        set_status(p.status, kStatusSlotRange);
-        return 0;
-      }
-      return sl;
+      return rt[pos];
     };
     auto issue = [&](int s, int sl) {
+      if (sl >= 0 && (int64_t)sl >= a.num_slots) {
+        set_status(p.status, kStatusSlotRange);
+        sl = 0;
+      } else if (sl < -2) {
+        set_status(p.status, kStatusSlotRange);
+        sl = 0;
+      }
       const int buf = s % kStages;
       char* kd = ring + buf * C::STAGE + lane * C::RS;
       char* vd = ring + buf * C::STAGE + kTok * C::RS + lane * C::RS;

@@ -9,7 +9,7 @@
 // req_to_token, rows gathered from the pool), then the new tokens (rows of k_new / v_new), the
 // causal mask applied only where a tile crosses the diagonal.
 //
-// Warp roles (384 threads, three warpgroups):
+// Warp roles (512 threads, four warpgroups):
 //   warps 0-3   producers: gather the key tile's K and V rows (256 B each, one slot per row) with
 //               16-byte cp.async copies straight into the 128-byte-swizzled operand layout, two
 //               rows per warp instruction (fully coalesced); completion is signalled on the
@@ -19,10 +19,11 @@
 //   warp 4      allocates TMEM and issues every tcgen05.mma from one lane:
 //               S[j%2] = Q K_j^T (M=128, N=128, K=128; fp32 in TMEM), then O += P_{j-1} V_{j-1};
 //   warps 5-7   scatter the tile's new K/V rows into their pool slots;
-//   warps 8-11  softmax, one thread per query row (TMEM lane), two passes over the score row
-//               (max, then exp2 with the scale folded into one FMA), lazy rescale of O (only
-//               when the running max grows by > 8 in log2 units), P as bf16 into shared memory
-//               (the A operand of P V), epilogue O / l.
+//   warps 8-15  softmax, two threads per query row (TMEM lane), 64 columns each: two passes
+//               over the scores (row max -- combined with the partner thread through shared
+//               memory -- then exp2 with the scale folded into one packed FMA), lazy rescale
+//               of O (only when the running max grows by > 8 in log2 units), P as bf16 into
+//               shared memory (the A operand of P V), epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
 #include <mutex>
 
@@ -39,10 +40,11 @@ constexpr int kN = 128;           // keys per tile
 constexpr int kStagesKV = 2;
 constexpr int kTileBytes = kM * kD * 2;   // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int kBlockBytes = kM * 128;     // 16 KB: one 64-column block of a tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kProducers = 128;          // warps 0-3
 constexpr int kMmaWarp = 4;
-constexpr int kSoftmax0 = 256;           // first softmax thread (warps 8-11)
+constexpr int kSoftmax0 = 256;           // first softmax thread (warps 8-15)
+constexpr int kSoftmaxThreads = 256;     // two threads per query row, 64 columns each
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
 
 struct SmemLayout {
@@ -52,8 +54,8 @@ struct SmemLayout {
   static constexpr int P = V + kStagesKV * kTileBytes;
   static constexpr int BAR = P + 2 * kTileBytes;
   // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full[2],
-  //           o_done[2]
-  static constexpr int NBAR = 16;
+  //           o_done[2], x_done[2] (softmax partner exchange), e_done (epilogue exchange)
+  static constexpr int NBAR = 19;
   static constexpr int TMEM_SLOT = BAR + NBAR * 8;
   static constexpr int TOTAL = TMEM_SLOT + 16;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base to 1024 bytes
@@ -73,6 +75,24 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -153,6 +173,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+               "r"(__float_as_uint(v))
+               : "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return __uint_as_float(r);
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -213,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint64_t* s_free = bars + 10;
   uint64_t* p_full = bars + 12;
   uint64_t* o_done = bars + 14;
+  uint64_t* x_done = bars + 16;
+  uint64_t* e_done = bars + 18;
   uint32_t* tmem_slot = (uint32_t*)(smem + SmemLayout::TMEM_SLOT);
 
   if (threadIdx.x == 0) {
@@ -222,10 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_init(&v_full[s], kProducers);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&s_free[s], kSoftmaxThreads);
+      mbar_init(&p_full[s], kSoftmaxThreads);
       mbar_init(&o_done[s], 1);
+      mbar_init(&x_done[s], kSoftmaxThreads);
     }
+    mbar_init(e_done, kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -266,10 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
     const int myrow = warp * 32 + lane;
     // source row index: slot * Hkv + hk in the pool, or token * Hkv + hk in k_new / v_new
-    auto src_row = [&](int j) -> int {
+    // raw_row(j) only issues the slot load; row_of() checks it when the tile is issued, so the
+    // load of tile j+1 stays in flight while tile j is being copied
+    auto raw_row = [&](int j) -> int {
       if (j < n_pre) {
         const int key = j * kN + myrow;
-        int sl = rt[key < P ? key : P - 1];
+        return rt[key < P ? key : P - 1];
+      }
+      return 0;
+    };
+    auto row_of = [&](int j, int raw) -> int {
+      if (j < n_pre) {
+        int sl = raw;
         if (sl < 0 || (int64_t)sl >= a.num_slots) {
           set_status(p.status, kStatusSlotRange);
           sl = 0;
@@ -279,15 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const int s0 = (j - n_pre) * kN + myrow;
       return (qo + min(s0, S - 1)) * Hkv + hk;
     };
-    int nxt = src_row(0);
+    int nxt = raw_row(0);
     bool ok = true;
     const int c = lane & 15, half = lane >> 4;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
       const uint32_t par_empty = ((j >> 1) - 1) & 1;
-      const int cur = nxt;
+      const int cur = row_of(j, nxt);
       const bool pre = j < n_pre;
-      if (j + 1 < ntiles) nxt = src_row(j + 1);  // in flight while this tile is issued
+      if (j + 1 < ntiles) nxt = raw_row(j + 1);  // in flight while this tile is issued
       const __nv_bfloat16* kb = pre ? kp : kn;
       const __nv_bfloat16* vb = pre ? vp : vn;
       if (j >= kStagesKV) ok = mbar_wait(&k_empty[st], par_empty, p.status);
@@ -339,12 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       __syncwarp();
       return true;
     };
-    for (int j = 0; j < ntiles && ok; ++j) {
+    // S = Q K_j^T into S[j & 1]; S[j & 1] is free again once the softmax has read S_{j-2}
+    auto qk = [&](int j) -> bool {
       const int st = j & 1, sb = j & 1;
-      ok = mbar_wait(&k_full[st], (j >> 1) & 1, p.status);
-      if (ok && j >= 2) ok = mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      if (!mbar_wait(&k_full[st], (j >> 1) & 1, p.status)) return false;
+      if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, p.status)) return false;
       fence_async_smem();   // K arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
@@ -359,9 +400,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         mma_commit(smem_u32(&k_empty[st]));
       }
       __syncwarp();
-      if (j >= 1) ok = __all_sync(0xffffffffu, pv(j - 1));
+      return true;
+    };
+    // two score tiles ahead of the softmax, then P.V of tile j as soon as its P is written,
+    // followed by the scores of tile j + 2 into the buffer the softmax just released
+    if (ntiles > 0) ok = __all_sync(0xffffffffu, qk(0));
+    if (ok && ntiles > 1) ok = __all_sync(0xffffffffu, qk(1));
+    for (int j = 0; j < ntiles && ok; ++j) {
+      ok = __all_sync(0xffffffffu, pv(j));
+      if (ok && j + 2 < ntiles) ok = __all_sync(0xffffffffu, qk(j + 2));
     }
-    if (ok && ntiles > 0) pv(ntiles - 1);
   } else if (warp < 8) {
     // ------------------------------------------------------------ scatter of the new K/V rows
     // 96 threads copy (row, 16-byte chunk) pairs; each round issues all of a thread's loads
@@ -400,15 +448,21 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int r = threadIdx.x - kSoftmax0;            // query row = TMEM lane
+    // ------------------------------------------------------------ softmax warpgroups
+    const int hf = (warp - 8) >> 2;                   // column half: [64 hf, 64 hf + 64)
+    const int r = (warp & 3) * 32 + lane;             // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int rows_used = npos * G;
     const int ipos = min(i0 + r / G, S - 1);          // this row's new-token index (clamped)
     const float sc2 = p.scale2;
+    const uint64_t sc2x2 = f2pack(sc2, sc2);
+    // partner exchange through spare TMEM columns (same lane, so the same quadrant): row maxima
+    // at 448 + 2 * (tile parity) + half, final sums at 452 + 2 * (which sum) + half
+    const uint32_t tX = tmem + 448 + lane_off;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     uint8_t* pbase = smem + SmemLayout::P;
+    const int c0 = hf * 64;                           // first column of this thread
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       ok = mbar_wait(&s_full[sb], (j >> 1) & 1, p.status);
@@ -417,23 +471,39 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       tc_fence_after();
       // keys [0, lim) of this tile are visible to this row
       const int lim = j < n_pre ? min(kN, P - j * kN) : min(kN, ipos - (j - n_pre) * kN + 1);
-      const uint32_t tS = tS0 + sb * 128 + lane_off;
-      // pass 1: row max of the raw scores
+      const bool full = __all_sync(0xffffffffu, lim >= c0 + 64);
+      const uint32_t tS = tS0 + sb * 128 + lane_off + c0;
+      // pass 1: row max of the raw scores, combined with the partner thread
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
         tmem_ld32(tS + c * 32, v);
         tmem_wait_ld();
+        if (full) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) mx = fmaxf(mx, c * 32 + u < lim ? v[u] : -INFINITY);
+          for (int u = 0; u < 32; ++u) mx = fmaxf(mx, v[u]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) mx = fmaxf(mx, c0 + c * 32 + u < lim ? v[u] : -INFINITY);
+        }
       }
+      tmem_st1(tX + sb * 2 + hf, mx);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&x_done[sb]);
+      ok = mbar_wait(&x_done[sb], (j >> 1) & 1, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      mx = fmaxf(mx, tmem_ld1(tX + sb * 2 + (hf ^ 1)));
+      tmem_wait_ld();
       const float mt = mx * sc2;                      // sc2 > 0: max commutes with the scale
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
       const float alpha = (rescale && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
-      const float neg = -m_use;
+      const uint64_t negx2 = f2pack(-m_use, -m_use);
       // P[j&1] was read by the P.V of tile j-2
       if (j >= 2) {
         ok = mbar_wait(&o_done[sb], ((j >> 1) - 1) & 1, p.status);
@@ -441,73 +511,91 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (!ok) break;
       }
       // pass 2: weights, written as bf16 into the P operand tile
-      float rs = 0.f, re = 0.f;
+      uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
       uint8_t* prow = pbase + sb * kTileBytes;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
         tmem_ld32(tS + c * 32, v);
         tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] = c0 + c * 32 + u < lim ? v[u] : -INFINITY;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int k0 = c * 32 + 2 * u;
-          const float p0 = ex2(k0 < lim ? fmaf(v[2 * u], sc2, neg) : -INFINITY);
-          const float p1 = ex2(k0 + 1 < lim ? fmaf(v[2 * u + 1], sc2, neg) : -INFINITY);
+          float x0, x1;
+          f2unpack(fma2(f2pack(v[2 * u], v[2 * u + 1]), sc2x2, negx2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
           pk[u] = pack_bf16(p0, p1);
           // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp
           // output uses the exact sum
-          rs += bf16lo(pk[u]) + bf16hi(pk[u]);
-          re += p0 + p1;
+          rs2 = add2(rs2, f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
+          re2 = add2(re2, f2pack(p0, p1));
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          *(uint4*)(prow + sw128_off(r, c * 4 + q4)) =
+          *(uint4*)(prow + sw128_off(r, hf * 8 + c * 4 + q4)) =
               make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
       }
       tc_fence_before();
       mbar_arrive(&s_free[sb]);
-      // O is touched only after the P.V of tile j-1
+      // O is touched only after the P.V of tile j-1; each thread rescales its half of O
       const bool any_rescale = __any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0;
       if (any_rescale) {
         ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
           float o[32];
-          tmem_ld32(tO + lane_off + c * 32, o);
+          tmem_ld32(tO + lane_off + c0 + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] *= alpha;
-          tmem_st32(tO + lane_off + c * 32, o);
+          tmem_st32(tO + lane_off + c0 + c * 32, o);
         }
         tmem_wait_st();
       }
-      l_run = l_run * alpha + rs;
-      l_exact = l_exact * alpha + re;
+      float a0, a1, b0, b1;
+      f2unpack(rs2, a0, a1);
+      f2unpack(re2, b0, b1);
+      l_run = l_run * alpha + (a0 + a1);
+      l_exact = l_exact * alpha + (b0 + b1);
       m_run = m_use;
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[sb]);
     }
-    // epilogue
+    // epilogue: full denominators from both halves, then this thread's half of the O row
     if (ok && ntiles > 0) {
       const int t = ntiles - 1;
       ok = mbar_wait(&o_done[t & 1], (t >> 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
     }
+    tmem_st1(tX + 4 + hf, l_run);
+    tmem_st1(tX + 6 + hf, l_exact);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(e_done);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(e_done, 0, p.status));
+    tc_fence_after();
+    l_run += tmem_ld1(tX + 4 + (hf ^ 1));
+    l_exact += tmem_ld1(tX + 6 + (hf ^ 1));
+    tmem_wait_ld();
     if (ok && ntiles > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const bool store = r < rows_used;
       const int i = i0 + r / G, hh = r % G;
-      __nv_bfloat16* orow = (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      __nv_bfloat16* orow =
+          (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c0;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + lane_off + c0 + c * 32, o);
         tmem_wait_ld();
         if (store) {
 #pragma unroll
@@ -520,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           }
         }
       }
-      if (store && a.lse)
+      if (store && hf == 0 && a.lse)
         a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
     }
   }
