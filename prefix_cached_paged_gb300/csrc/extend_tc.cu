@@ -10,10 +10,10 @@
 // causal mask applied only where a tile crosses the diagonal.
 //
 // Warp roles (512 threads, four warpgroups):
-//   warps 0-3   producers: gather the key tile's K and V rows (256 B each, one slot per row) with
-//               16-byte cp.async copies straight into the 128-byte-swizzled operand layout, two
-//               rows per warp instruction (fully coalesced); completion is signalled on the
-//               stage's mbarrier with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves
+//   warps 0-3   producers (0-1 for K, 2-3 for V): gather the key tile's rows (256 B each, one
+//               slot per row) with 16-byte cp.async copies straight into the 128-byte-swizzled
+//               operand layout, two rows per warp instruction (fully coalesced); completion is
+//               signalled on the stage's mbarrier with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves
 //               only 512 B per instruction and, measured here, its issue rate capped a 256-byte
 //               row gather at about 2 TB/s for the whole GPU; the copy engine path does not.)
 //   warp 4      allocates TMEM and issues every tcgen05.mma from one lane:
@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], kProducers);
+      mbar_init(&k_full[s], kProducers / 2);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], kProducers);
+      mbar_init(&v_full[s], kProducers / 2);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], kSoftmaxThreads);
@@ -291,25 +291,29 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers (warps 0-3)
-    // Warp w fills rows [32w, 32w + 32) of each tile. Lane l resolves the source row of tile row
-    // 32w + l; one copy instruction then moves 16-byte chunk (l & 15) of rows 2i and 2i + 1.
+    // Warps 0-1 load the K tiles and warps 2-3 the V tiles, each side at its own pace (a K tile
+    // only waits for the QK that last read its stage, a V tile for the P.V). Warp w covers rows
+    // [64 (w & 1), 64 (w & 1) + 64) of a tile in two halves of 32: lane l resolves the source
+    // row of tile row 64 (w & 1) + 32 h + l, and one copy instruction moves 16-byte chunk
+    // (l & 15) of two rows.
     const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
-    const __nv_bfloat16* kp = (const __nv_bfloat16*)a.k_pool;
-    const __nv_bfloat16* vp = (const __nv_bfloat16*)a.v_pool;
-    const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
-    const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-    const int myrow = warp * 32 + lane;
-    // source row index: slot * Hkv + hk in the pool, or token * Hkv + hk in k_new / v_new
-    // raw_row(j) only issues the slot load; row_of() checks it when the tile is issued, so the
-    // load of tile j+1 stays in flight while tile j is being copied
-    auto raw_row = [&](int j) -> int {
+    const bool is_v = warp >= 2;
+    const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
+    const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const uint32_t sdst = is_v ? sV : sK;
+    const int rbase = (warp & 1) * 64;
+    // raw_row(j, h) only issues the slot load; row_of() checks it when the tile is issued, so
+    // the load of tile j+1 stays in flight while tile j is being copied
+    auto raw_row = [&](int j, int h) -> int {
       if (j < n_pre) {
-        const int key = j * kN + myrow;
+        const int key = j * kN + rbase + h * 32 + lane;
         return rt[key < P ? key : P - 1];
       }
       return 0;
     };
-    auto row_of = [&](int j, int raw) -> int {
+    auto row_of = [&](int j, int h, int raw) -> int {
       if (j < n_pre) {
         int sl = raw;
         if (sl < 0 || (int64_t)sl >= a.num_slots) {
@@ -318,42 +322,31 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         return sl * Hkv + hk;
       }
-      const int s0 = (j - n_pre) * kN + myrow;
+      const int s0 = (j - n_pre) * kN + rbase + h * 32 + lane;
       return (qo + min(s0, S - 1)) * Hkv + hk;
     };
-    int nxt = raw_row(0);
+    int nxt0 = raw_row(0, 0), nxt1 = raw_row(0, 1);
     bool ok = true;
     const int c = lane & 15, half = lane >> 4;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
-      const uint32_t par_empty = ((j >> 1) - 1) & 1;
-      const int cur = row_of(j, nxt);
-      const bool pre = j < n_pre;
-      if (j + 1 < ntiles) nxt = raw_row(j + 1);  // in flight while this tile is issued
-      const __nv_bfloat16* kb = pre ? kp : kn;
-      const __nv_bfloat16* vb = pre ? vp : vn;
-      if (j >= kStagesKV) ok = mbar_wait(&k_empty[st], par_empty, p.status);
+      const int cur0 = row_of(j, 0, nxt0), cur1 = row_of(j, 1, nxt1);
+      if (j + 1 < ntiles) {  // in flight while this tile is issued
+        nxt0 = raw_row(j + 1, 0);
+        nxt1 = raw_row(j + 1, 1);
+      }
+      const __nv_bfloat16* src = j < n_pre ? pool : nsrc;
+      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j >> 1) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const uint32_t kdst = sK + st * kTileBytes;
+      const uint32_t dst = sdst + st * kTileBytes;
 #pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int rr = 2 * i + half;
-        const int src = __shfl_sync(0xffffffffu, cur, rr);
-        cp_async16(kdst + sw128_off(warp * 32 + rr, c), kb + (int64_t)src * kD + c * 8);
+      for (int i = 0; i < 32; ++i) {
+        const int rr = 2 * i + half;                       // 0..63 within this warp's rows
+        const int srow = __shfl_sync(0xffffffffu, rr < 32 ? cur0 : cur1, rr & 31);
+        cp_async16(dst + sw128_off(rbase + rr, c), src + (int64_t)srow * kD + c * 8);
       }
-      cp_async_arrive_noinc(smem_u32(&k_full[st]));
-      if (j >= kStagesKV) ok = mbar_wait(&v_empty[st], par_empty, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint32_t vdst = sV + st * kTileBytes;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int rr = 2 * i + half;
-        const int src = __shfl_sync(0xffffffffu, cur, rr);
-        cp_async16(vdst + sw128_off(warp * 32 + rr, c), vb + (int64_t)src * kD + c * 8);
-      }
-      cp_async_arrive_noinc(smem_u32(&v_full[st]));
+      cp_async_arrive_noinc(smem_u32(&full[st]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
