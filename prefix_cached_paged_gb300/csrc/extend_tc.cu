@@ -3,27 +3,36 @@
 // App. A.1: the new tokens' queries attend to the request's cached prefix KV -- gathered from
 // the paged pool through the slot table -- and causally to the new tokens' own K/V.
 //
-// One CTA = (request, KV head, tile of 128 query rows). With G = Hq / Hkv query heads per KV
-// head, a tile packs floor(128 / G) query positions x G heads, so every K/V tile loaded is used
-// by all heads of the group. Keys are processed in tiles of 128: first the prefix (slots from
-// req_to_token, rows gathered from the pool), then the new tokens (rows of k_new / v_new), the
-// causal mask applied only where a tile crosses the diagonal.
+// One CTA = (request, KV head, two tiles A and B of 128 query rows). With G = Hq / Hkv query
+// heads per KV head, a tile packs floor(128 / G) query positions x G heads, so every K/V tile
+// gathered serves all heads of the group and both query tiles. Keys are processed in tiles of
+// 128: first the prefix (slots from req_to_token, rows gathered from the pool), then the new
+// tokens (rows of k_new / v_new); the causal mask is applied only where a tile crosses the
+// diagonal, and a query tile skips key tiles that lie entirely in its future.
 //
-// Warp roles (512 threads, four warpgroups):
-//   warps 0-3   producers (0-1 for K, 2-3 for V): gather the key tile's rows (256 B each, one
-//               slot per row) with 16-byte cp.async copies straight into the 128-byte-swizzled
-//               operand layout, two rows per warp instruction (fully coalesced); completion is
-//               signalled on the stage's mbarrier with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves
-//               only 512 B per instruction and, measured here, its issue rate capped a 256-byte
-//               row gather at about 2 TB/s for the whole GPU; the copy engine path does not.)
-//   warp 4      allocates TMEM and issues every tcgen05.mma from one lane:
-//               S[j%2] = Q K_j^T (M=128, N=128, K=128; fp32 in TMEM), then O += P_{j-1} V_{j-1};
-//   warps 5-7   scatter the tile's new K/V rows into their pool slots;
-//   warps 8-15  softmax, two threads per query row (TMEM lane), 64 columns each: two passes
-//               over the scores (row max -- combined with the partner thread through shared
-//               memory -- then exp2 with the scale folded into one packed FMA), lazy rescale
-//               of O (only when the running max grows by > 8 in log2 units), P as bf16 into
-//               shared memory (the A operand of P V), epilogue O / l.
+// The two query tiles ping-pong on the tensor core: while the softmax of tile A turns its scores
+// into weights, the MMA warp runs P.V and the next Q K^T of tile B, and the other way round.
+//
+// TMEM (512 columns): S_A [0,128) S_B [128,256) scores (fp32); O_A [256,384) O_B [384,512)
+// outputs (fp32). The bf16 weights P overwrite the score columns they came from (each thread
+// writes the weights of its 64 keys as 32 packed columns at the start of its own score columns)
+// and feed P.V straight from TMEM as the A operand.
+//
+// Warp roles (640 threads):
+//   warp 0       allocates TMEM and issues every tcgen05.mma from one lane;
+//   warps 1, 2   producers for K and V: gather the key tile's rows (256 B, one slot per row)
+//                with 16-byte cp.async copies straight into the 128-byte-swizzled operand
+//                layout, two rows per instruction (fully coalesced); completion is signalled
+//                with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves 512 B per
+//                instruction and, measured here, its issue rate capped a 256-byte row gather at
+//                about 2 TB/s GPU-wide; the copy path does not.)
+//   warp 3       scatters the new tokens' K/V rows into their pool slots;
+//   warps 4-19   softmax: four groups of four warps, (query tile, column half); two threads per
+//                query row, 64 columns each. Two passes over the scores (row max, combined with
+//                the partner thread through shared memory; then exp2 with the scale folded
+//                into one packed FMA); lazy rescale of O (only when the running max grows by
+//                more than 8 in log2 units); weights rounded to bf16, normalised by the sum of
+//                the rounded weights; epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
 #include <mutex>
 
@@ -40,24 +49,25 @@ constexpr int kN = 128;           // keys per tile
 constexpr int kStagesKV = 2;
 constexpr int kTileBytes = kM * kD * 2;   // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int kBlockBytes = kM * 128;     // 16 KB: one 64-column block of a tile
-constexpr int kThreads = 512;
-constexpr int kProducers = 128;          // warps 0-3
-constexpr int kMmaWarp = 4;
-constexpr int kSoftmax0 = 256;           // first softmax thread (warps 8-15)
-constexpr int kSoftmaxThreads = 256;     // two threads per query row, 64 columns each
+constexpr int kThreads = 640;
+constexpr int kMmaWarp = 0;
+constexpr int kKWarp = 1, kVWarp = 2, kScatterWarp = 3;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kGroupThreads = 256;        // softmax threads of one query tile
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
 
 struct SmemLayout {
-  static constexpr int Q = 0;
-  static constexpr int K = Q + kTileBytes;
+  static constexpr int Q = 0;                                   // Q_A, Q_B
+  static constexpr int K = Q + 2 * kTileBytes;
   static constexpr int V = K + kStagesKV * kTileBytes;
-  static constexpr int P = V + kStagesKV * kTileBytes;
-  static constexpr int BAR = P + 2 * kTileBytes;
-  // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full[2],
-  //           o_done[2], x_done[2] (softmax partner exchange), e_done (epilogue exchange)
-  static constexpr int NBAR = 19;
+  static constexpr int BAR = V + kStagesKV * kTileBytes;
+  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] x_done[2][2] e_done[2]
+  static constexpr int NBAR = 20;
   static constexpr int TMEM_SLOT = BAR + NBAR * 8;
-  static constexpr int TOTAL = TMEM_SLOT + 16;
+  // partner exchange: row maxima [tile][parity][half][row], sums [tile][which][half][row]
+  static constexpr int XMAX = TMEM_SLOT + 16;
+  static constexpr int XSUM = XMAX + 2 * 2 * 2 * 128 * 4;
+  static constexpr int TOTAL = XSUM + 2 * 2 * 2 * 128 * 4;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base to 1024 bytes
 };
 static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
@@ -173,16 +183,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
-               "r"(__float_as_uint(v))
-               : "memory");
-}
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-  uint32_t r;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-  return __uint_as_float(r);
-}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -200,6 +200,25 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return (uint32_t)((c >> 3) * kBlockBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+
+// tcgen05.mma with the A operand in TMEM (weights) and B in shared memory (V)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
 // ---------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,24 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const rc_extend_args& a = p.a;
   const int b = blockIdx.z;
   const int hk = blockIdx.y;
-  const int qt = blockIdx.x;
   const int qo = a.qo_indptr[b];
   const int S = a.qo_indptr[b + 1] - qo;
   const int P = a.prefix_len[b];
   const int G = a.num_q_heads / a.num_kv_heads;
-  const int i0 = qt * p.ppt;
-  if (S <= 0 || i0 >= S) return;
+  const int iA = blockIdx.x * 2 * p.ppt;       // first query position of tile A
+  if (S <= 0 || iA >= S) return;
   const int row = a.req_idx[b];
   if (P < 0 || (int64_t)P + S > a.max_ctx || row < 0 || row >= a.max_reqs || qo < 0 ||
       (int64_t)qo + S > a.num_tokens) {
     if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
     return;
   }
-  const int npos = min(p.ppt, S - i0);         // query positions in this tile
-  const int kend_s = i0 + npos;                // new-token keys visible to some row: [0, kend_s)
+  const int iB = iA + p.ppt;
+  const int nposA = min(p.ppt, S - iA);
+  const int nposB = max(0, min(p.ppt, S - iB));
   const int n_pre = (P + kN - 1) / kN;
-  const int n_suf = (kend_s + kN - 1) / kN;
-  const int ntiles = n_pre + n_suf;
+  // key tiles of each query tile: the prefix, then new-token keys up to its last position
+  const int nA = n_pre + (iA + nposA + kN - 1) / kN;
+  const int nB = nposB > 0 ? n_pre + (iB + nposB + kN - 1) / kN : 0;
+  const int ntiles = max(nA, nB);
+  const int kend = nposB > 0 ? iB + nposB : iA + nposA;  // new-token keys loaded: [0, kend)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
 
@@ -233,33 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t sQ = sbase + SmemLayout::Q;
   const uint32_t sK = sbase + SmemLayout::K;
   const uint32_t sV = sbase + SmemLayout::V;
-  const uint32_t sP = sbase + SmemLayout::P;
   uint64_t* bars = (uint64_t*)(smem + SmemLayout::BAR);
   uint64_t* k_full = bars + 0;
   uint64_t* k_empty = bars + 2;
   uint64_t* v_full = bars + 4;
   uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 8;
-  uint64_t* s_free = bars + 10;
-  uint64_t* p_full = bars + 12;
-  uint64_t* o_done = bars + 14;
-  uint64_t* x_done = bars + 16;
-  uint64_t* e_done = bars + 18;
+  uint64_t* s_full = bars + 8;     // [tile]
+  uint64_t* p_full = bars + 10;    // [tile]
+  uint64_t* o_done = bars + 12;    // [tile]
+  uint64_t* x_done = bars + 14;    // [tile][parity]
+  uint64_t* e_done = bars + 18;    // [tile]
   uint32_t* tmem_slot = (uint32_t*)(smem + SmemLayout::TMEM_SLOT);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], kProducers / 2);
+      mbar_init(&k_full[s], 32);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], kProducers / 2);
+      mbar_init(&v_full[s], 32);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], kSoftmaxThreads);
-      mbar_init(&p_full[s], kSoftmaxThreads);
+      mbar_init(&p_full[s], kGroupThreads);
       mbar_init(&o_done[s], 1);
-      mbar_init(&x_done[s], kSoftmaxThreads);
+      mbar_init(&x_done[2 * s], kGroupThreads);
+      mbar_init(&x_done[2 * s + 1], kGroupThreads);
+      mbar_init(&e_done[s], kGroupThreads);
     }
-    mbar_init(e_done, kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -268,18 +288,19 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Q tile: row m = (position i0 + m / G, head hk * G + m % G); rows past the tile are zero
+  // Q tiles: row m of tile X = (position iX + m / G, head hk * G + m % G); rows past the tile
+  // are zero
   {
     const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
-    const int rows_used = npos * G;
-    for (int e = threadIdx.x; e < kM * 16; e += kThreads) {
-      const int m = e >> 4, c = e & 15;
+    for (int e = threadIdx.x; e < 2 * kM * 16; e += kThreads) {
+      const int X = e >> 11, m = (e >> 4) & 127, c = e & 15;
+      const int i0 = X ? iB : iA, np = X ? nposB : nposA;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (m < rows_used) {
+      if (m < np * G) {
         const int i = i0 + m / G, hh = m % G;
         v = *(const uint4*)(q + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c * 8);
       }
-      *(uint4*)(smem + SmemLayout::Q + sw128_off(m, c)) = v;
+      *(uint4*)(smem + SmemLayout::Q + X * kTileBytes + sw128_off(m, c)) = v;
     }
   }
   fence_async_smem();
@@ -287,148 +308,154 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
 
-  if (warp < 4) {
-    // ------------------------------------------------------------ producers (warps 0-3)
-    // Warps 0-1 load the K tiles and warps 2-3 the V tiles, each side at its own pace (a K tile
-    // only waits for the QK that last read its stage, a V tile for the P.V). Warp w covers rows
-    // [64 (w & 1), 64 (w & 1) + 64) of a tile in two halves of 32: lane l resolves the source
-    // row of tile row 64 (w & 1) + 32 h + l, and one copy instruction moves 16-byte chunk
-    // (l & 15) of two rows.
-    const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
-    const bool is_v = warp >= 2;
-    const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
-    const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
-    uint64_t* full = is_v ? v_full : k_full;
-    uint64_t* empty = is_v ? v_empty : k_empty;
-    const uint32_t sdst = is_v ? sV : sK;
-    const int rbase = (warp & 1) * 64;
-    // raw_row(j, h) only issues the slot load; row_of() checks it when the tile is issued, so
-    // the load of tile j+1 stays in flight while tile j is being copied
-    auto raw_row = [&](int j, int h) -> int {
-      if (j < n_pre) {
-        const int key = j * kN + rbase + h * 32 + lane;
-        return rt[key < P ? key : P - 1];
-      }
-      return 0;
-    };
-    auto row_of = [&](int j, int h, int raw) -> int {
-      if (j < n_pre) {
-        int sl = raw;
-        if (sl < 0 || (int64_t)sl >= a.num_slots) {
-          set_status(p.status, kStatusSlotRange);
-          sl = 0;
-        }
-        return sl * Hkv + hk;
-      }
-      const int s0 = (j - n_pre) * kN + rbase + h * 32 + lane;
-      return (qo + min(s0, S - 1)) * Hkv + hk;
-    };
-    int nxt0 = raw_row(0, 0), nxt1 = raw_row(0, 1);
-    bool ok = true;
-    const int c = lane & 15, half = lane >> 4;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j & 1;
-      const int cur0 = row_of(j, 0, nxt0), cur1 = row_of(j, 1, nxt1);
-      if (j + 1 < ntiles) {  // in flight while this tile is issued
-        nxt0 = raw_row(j + 1, 0);
-        nxt1 = raw_row(j + 1, 1);
-      }
-      const __nv_bfloat16* src = j < n_pre ? pool : nsrc;
-      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j >> 1) - 1) & 1, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const uint32_t dst = sdst + st * kTileBytes;
-#pragma unroll 4
-      for (int i = 0; i < 32; ++i) {
-        const int rr = 2 * i + half;                       // 0..63 within this warp's rows
-        const int srow = __shfl_sync(0xffffffffu, rr < 32 ? cur0 : cur1, rr & 31);
-        cp_async16(dst + sw128_off(rbase + rr, c), src + (int64_t)srow * kD + c * 8);
-      }
-      cp_async_arrive_noinc(smem_u32(&full[st]));
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kMmaWarp) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
-    bool ok = true;
-    auto pv = [&](int t) -> bool {
-      const int pb = t & 1, st = t & 1;
-      if (!mbar_wait(&p_full[pb], (t >> 1) & 1, p.status)) return false;
-      if (!mbar_wait(&v_full[st], (t >> 1) & 1, p.status)) return false;
-      fence_async_smem();   // V arrived through the generic proxy (cp.async)
-      tc_fence_after();
-      if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          // A = P (K-major over keys), B = V (MN-major: d contiguous, keys as rows)
-          const uint64_t ad = smem_desc_sw128(sP + pb * kTileBytes + (kk >> 2) * kBlockBytes +
-                                                  (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sV + st * kTileBytes + kk * 2048, kBlockBytes, 1024);
-          mma_bf16(tO, ad, bd, idv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&o_done[pb]));
-        mma_commit(smem_u32(&v_empty[st]));
-      }
-      __syncwarp();
-      return true;
-    };
-    // S = Q K_j^T into S[j & 1]; S[j & 1] is free again once the softmax has read S_{j-2}
-    auto qk = [&](int j) -> bool {
-      const int st = j & 1, sb = j & 1;
-      if (!mbar_wait(&k_full[st], (j >> 1) & 1, p.status)) return false;
-      if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, p.status)) return false;
+    // key tile j is read first by tile A (if j < nA), last by tile B (if j < nB)
+    auto qk = [&](int X, int j) -> bool {
+      const int st = j & 1;
+      const bool first = X == 0 || j >= nA;
+      if (first && !mbar_wait(&k_full[st], (j >> 1) & 1, p.status)) return false;
       fence_async_smem();   // K arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sQ + off, 16, 1024);
+          const uint64_t ad = smem_desc_sw128(sQ + X * kTileBytes + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024);
-          mma_bf16(tS0 + sb * 128, ad, bd, idq, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + X * 128, ad, bd, idq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(smem_u32(&s_full[sb]));
-        mma_commit(smem_u32(&k_empty[st]));
+        mma_commit(smem_u32(&s_full[X]));
+        if (X == 1 || j >= nB) mma_commit(smem_u32(&k_empty[st]));
       }
       __syncwarp();
       return true;
     };
-    // two score tiles ahead of the softmax, then P.V of tile j as soon as its P is written,
-    // followed by the scores of tile j + 2 into the buffer the softmax just released
-    if (ntiles > 0) ok = __all_sync(0xffffffffu, qk(0));
-    if (ok && ntiles > 1) ok = __all_sync(0xffffffffu, qk(1));
+    auto pv = [&](int X, int j) -> bool {
+      const int st = j & 1;
+      if (!mbar_wait(&p_full[X], j & 1, p.status)) return false;
+      const bool first = X == 0 || j >= nA;
+      if (first && !mbar_wait(&v_full[st], (j >> 1) & 1, p.status)) return false;
+      fence_async_smem();   // V arrived through the generic proxy (cp.async)
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t tS = tmem + X * 128;
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          // A = P from TMEM: keys [0,64) in score columns [0,32), keys [64,128) in [64,96)
+          const uint32_t at = tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          // B = V (MN-major: d contiguous, keys as rows)
+          const uint64_t bd = smem_desc_sw128(sV + st * kTileBytes + kk * 2048, kBlockBytes, 1024);
+          mma_bf16_ts(tmem + 256 + X * 128, at, bd, idv, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (j == (X ? nB : nA) - 1) mma_commit(smem_u32(&o_done[X]));
+        if (X == 1 || j >= nB) mma_commit(smem_u32(&v_empty[st]));
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = __all_sync(0xffffffffu, qk(0, 0));
+    if (ok && nB > 0) ok = __all_sync(0xffffffffu, qk(1, 0));
     for (int j = 0; j < ntiles && ok; ++j) {
-      ok = __all_sync(0xffffffffu, pv(j));
-      if (ok && j + 2 < ntiles) ok = __all_sync(0xffffffffu, qk(j + 2));
+      if (j < nA) {
+        ok = __all_sync(0xffffffffu, pv(0, j));
+        if (ok && j + 1 < nA) ok = __all_sync(0xffffffffu, qk(0, j + 1));
+      }
+      if (ok && j < nB) {
+        ok = __all_sync(0xffffffffu, pv(1, j));
+        if (ok && j + 1 < nB) ok = __all_sync(0xffffffffu, qk(1, j + 1));
+      }
     }
-  } else if (warp < 8) {
+  } else if (warp == kKWarp || warp == kVWarp) {
+    // ------------------------------------------------------------ producers (K: warp 1, V: 2)
+    // Lane l resolves the source rows of tile rows l, l+32, l+64, l+96; one copy instruction
+    // moves 16-byte chunk (l & 15) of two rows.
+    const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
+    const bool is_v = warp == kVWarp;
+    const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
+    const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const uint32_t sdst = is_v ? sV : sK;
+    // raw(j, q) only issues the slot load; rowof() checks it when the tile is issued, so the
+    // loads of tile j+1 stay in flight while tile j is being copied
+    auto raw = [&](int j, int q) -> int {
+      if (j < n_pre) {
+        const int key = j * kN + q * 32 + lane;
+        return rt[key < P ? key : P - 1];
+      }
+      return 0;
+    };
+    auto rowof = [&](int j, int q, int rv) -> int {
+      if (j < n_pre) {
+        int sl = rv;
+        if (sl < 0 || (int64_t)sl >= a.num_slots) {
+          set_status(p.status, kStatusSlotRange);
+          sl = 0;
+        }
+        return sl * Hkv + hk;
+      }
+      const int s0 = (j - n_pre) * kN + q * 32 + lane;
+      return (qo + min(s0, kend - 1)) * Hkv + hk;
+    };
+    int n0 = raw(0, 0), n1 = raw(0, 1), n2 = raw(0, 2), n3 = raw(0, 3);
+    bool ok = true;
+    const int c = lane & 15, half = lane >> 4;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j & 1;
+      const int r0 = rowof(j, 0, n0), r1 = rowof(j, 1, n1), r2 = rowof(j, 2, n2),
+                r3 = rowof(j, 3, n3);
+      if (j + 1 < ntiles) {
+        n0 = raw(j + 1, 0);
+        n1 = raw(j + 1, 1);
+        n2 = raw(j + 1, 2);
+        n3 = raw(j + 1, 3);
+      }
+      const __nv_bfloat16* src = j < n_pre ? pool : nsrc;
+      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j >> 1) - 1) & 1, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint32_t dst = sdst + st * kTileBytes;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int rq = q == 0 ? r0 : q == 1 ? r1 : q == 2 ? r2 : r3;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int rr = 2 * i + half;
+          const int srow = __shfl_sync(0xffffffffu, rq, rr);
+          cp_async16(dst + sw128_off(q * 32 + rr, c), src + (int64_t)srow * kD + c * 8);
+        }
+      }
+      cp_async_arrive_noinc(smem_u32(&full[st]));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kScatterWarp) {
     // ------------------------------------------------------------ scatter of the new K/V rows
-    // 96 threads copy (row, 16-byte chunk) pairs; each round issues all of a thread's loads
-    // before any store so that four copies are in flight per thread.
-    const int t = threadIdx.x - 160;
+    // (row, 16-byte chunk) pairs of both query tiles' positions; each round issues all of a
+    // lane's loads before any store, eight copies in flight per lane.
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-    constexpr int kU = 4;
-    const int total = npos * 16;
-    for (int base = t; base < total; base += 96 * kU) {
+    constexpr int kU = 8;
+    const int total = (nposA + nposB) * 16;
+    for (int base = lane; base < total; base += 32 * kU) {
       uint4 kv[kU], vv[kU];
       int64_t dst[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int e = base + u * 96;
+        const int e = base + u * 32;
         dst[u] = -1;
         if (e < total) {
-          const int i = i0 + (e >> 4), c = e & 15;
+          const int i = iA + (e >> 4), cc = e & 15;
           const int64_t tok = qo + i;
           const int sl = a.out_loc[tok];
-          const int64_t src = (tok * Hkv + hk) * kD + c * 8;
+          const int64_t src = (tok * Hkv + hk) * kD + cc * 8;
           kv[u] = *(const uint4*)(kn + src);
           vv[u] = *(const uint4*)(vn + src);
           if (sl >= 0 && (int64_t)sl < a.num_slots)
-            dst[u] = ((int64_t)sl * Hkv + hk) * kD + c * 8;
-          else if (c == 0)
+            dst[u] = ((int64_t)sl * Hkv + hk) * kD + cc * 8;
+          else if (cc == 0)
             set_status(p.status, kStatusSlotRange);
         }
       }
@@ -441,37 +468,40 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int hf = (warp - 8) >> 2;                   // column half: [64 hf, 64 hf + 64)
-    const int r = (warp & 3) * 32 + lane;             // query row = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int rows_used = npos * G;
-    const int ipos = min(i0 + r / G, S - 1);          // this row's new-token index (clamped)
+    // ------------------------------------------------------------ softmax groups
+    const int g = (warp - kSoftmaxWarp0) >> 2;
+    const int X = g >> 1;                             // query tile
+    const int hf = g & 1;                             // column half: [64 hf, 64 hf + 64)
+    const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;                   // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int nX = X ? nB : nA;
+    const int iX = X ? iB : iA;
+    const int rows_used = (X ? nposB : nposA) * G;
+    const int ipos = min(iX + r / G, S - 1);          // this row's new-token index (clamped)
     const float sc2 = p.scale2;
     const uint64_t sc2x2 = f2pack(sc2, sc2);
-    // partner exchange through spare TMEM columns (same lane, so the same quadrant): row maxima
-    // at 448 + 2 * (tile parity) + half, final sums at 452 + 2 * (which sum) + half
-    const uint32_t tX = tmem + 448 + lane_off;
+    const uint32_t tS = tmem + X * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + X * 128 + lane_off;
+    const int c0 = hf * 64;                           // first score column of this thread
+    float* xmax = (float*)(smem + SmemLayout::XMAX);  // [tile][parity][half][row]
+    float* xsum = (float*)(smem + SmemLayout::XSUM);  // [tile][which][half][row]
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
-    uint8_t* pbase = smem + SmemLayout::P;
-    const int c0 = hf * 64;                           // first column of this thread
-    for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(&s_full[sb], (j >> 1) & 1, p.status);
+    for (int j = 0; j < nX; ++j) {
+      ok = mbar_wait(&s_full[X], j & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       // keys [0, lim) of this tile are visible to this row
       const int lim = j < n_pre ? min(kN, P - j * kN) : min(kN, ipos - (j - n_pre) * kN + 1);
       const bool full = __all_sync(0xffffffffu, lim >= c0 + 64);
-      const uint32_t tS = tS0 + sb * 128 + lane_off + c0;
       // pass 1: row max of the raw scores, combined with the partner thread
       float mx = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32(tS + c * 32, v);
+        tmem_ld32(tS + c0 + c * 32, v);
         tmem_wait_ld();
         if (full) {
 #pragma unroll
@@ -481,35 +511,25 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           for (int u = 0; u < 32; ++u) mx = fmaxf(mx, c0 + c * 32 + u < lim ? v[u] : -INFINITY);
         }
       }
-      tmem_st1(tX + sb * 2 + hf, mx);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&x_done[sb]);
-      ok = mbar_wait(&x_done[sb], (j >> 1) & 1, p.status);
+      const int par = j & 1;
+      xmax[((X * 2 + par) * 2 + hf) * 128 + r] = mx;
+      mbar_arrive(&x_done[X * 2 + par]);
+      ok = mbar_wait(&x_done[X * 2 + par], (j >> 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      mx = fmaxf(mx, tmem_ld1(tX + sb * 2 + (hf ^ 1)));
-      tmem_wait_ld();
+      mx = fmaxf(mx, xmax[((X * 2 + par) * 2 + (hf ^ 1)) * 128 + r]);
       const float mt = mx * sc2;                      // sc2 > 0: max commutes with the scale
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
       const float alpha = (rescale && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
       const uint64_t negx2 = f2pack(-m_use, -m_use);
-      // P[j&1] was read by the P.V of tile j-2
-      if (j >= 2) {
-        ok = mbar_wait(&o_done[sb], ((j >> 1) - 1) & 1, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      // pass 2: weights, written as bf16 into the P operand tile
+      // pass 2: weights, rounded to bf16 and written over this thread's own score columns
       uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
-      uint8_t* prow = pbase + sb * kTileBytes;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32(tS + c * 32, v);
+        tmem_ld32(tS + c0 + c * 32, v);
         tmem_wait_ld();
         if (!full) {
 #pragma unroll
@@ -527,85 +547,69 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           rs2 = add2(rs2, f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
           re2 = add2(re2, f2pack(p0, p1));
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *(uint4*)(prow + sw128_off(r, hf * 8 + c * 4 + q4)) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        // columns c0 + 16c .. c0 + 16c + 15 were read in chunk 0: free to overwrite
+        tmem_st16(tS + c0 + c * 16, pk);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-      // O is touched only after the P.V of tile j-1; each thread rescales its half of O
-      const bool any_rescale = __any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0;
-      if (any_rescale) {
-        ok = mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
+      // rescale this thread's half of O: its last P.V completed before these scores did
+      if (__any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0) {
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           float o[32];
-          tmem_ld32(tO + lane_off + c0 + c * 32, o);
+          tmem_ld32(tO + c0 + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] *= alpha;
-          tmem_st32(tO + lane_off + c0 + c * 32, o);
+          tmem_st32(tO + c0 + c * 32, o);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       float a0, a1, b0, b1;
       f2unpack(rs2, a0, a1);
       f2unpack(re2, b0, b1);
       l_run = l_run * alpha + (a0 + a1);
       l_exact = l_exact * alpha + (b0 + b1);
       m_run = m_use;
-      fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[X]);
     }
     // epilogue: full denominators from both halves, then this thread's half of the O row
-    if (ok && ntiles > 0) {
-      const int t = ntiles - 1;
-      ok = mbar_wait(&o_done[t & 1], (t >> 1) & 1, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    tmem_st1(tX + 4 + hf, l_run);
-    tmem_st1(tX + 6 + hf, l_exact);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(e_done);
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(e_done, 0, p.status));
-    tc_fence_after();
-    l_run += tmem_ld1(tX + 4 + (hf ^ 1));
-    l_exact += tmem_ld1(tX + 6 + (hf ^ 1));
-    tmem_wait_ld();
-    if (ok && ntiles > 0) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const bool store = r < rows_used;
-      const int i = i0 + r / G, hh = r % G;
-      __nv_bfloat16* orow =
-          (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c0;
+    if (nX > 0) {
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
+      xsum[((X * 2 + 0) * 2 + hf) * 128 + r] = l_run;
+      xsum[((X * 2 + 1) * 2 + hf) * 128 + r] = l_exact;
+      mbar_arrive(&e_done[X]);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&e_done[X], 0, p.status));
+      l_run += xsum[((X * 2 + 0) * 2 + (hf ^ 1)) * 128 + r];
+      l_exact += xsum[((X * 2 + 1) * 2 + (hf ^ 1)) * 128 + r];
+      if (ok) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const bool store = r < rows_used;
+        const int i = iX + r / G, hh = r % G;
+        __nv_bfloat16* orow =
+            (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c0;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float o[32];
-        tmem_ld32(tO + lane_off + c0 + c * 32, o);
-        tmem_wait_ld();
-        if (store) {
+        for (int c = 0; c < 2; ++c) {
+          float o[32];
+          tmem_ld32(tO + c0 + c * 32, o);
+          tmem_wait_ld();
+          if (store) {
 #pragma unroll
-          for (int u = 0; u < 32; u += 8) {
-            *(uint4*)(orow + c * 32 + u) =
-                make_uint4(pack_bf16(o[u] * inv, o[u + 1] * inv),
-                           pack_bf16(o[u + 2] * inv, o[u + 3] * inv),
-                           pack_bf16(o[u + 4] * inv, o[u + 5] * inv),
-                           pack_bf16(o[u + 6] * inv, o[u + 7] * inv));
+            for (int u = 0; u < 32; u += 8) {
+              *(uint4*)(orow + c * 32 + u) =
+                  make_uint4(pack_bf16(o[u] * inv, o[u + 1] * inv),
+                             pack_bf16(o[u + 2] * inv, o[u + 3] * inv),
+                             pack_bf16(o[u + 4] * inv, o[u + 5] * inv),
+                             pack_bf16(o[u + 6] * inv, o[u + 7] * inv));
+            }
           }
         }
+        if (store && hf == 0 && a.lse)
+          a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
       }
-      if (store && hf == 0 && a.lse)
-        a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
     }
   }
-  // every tcgen05 op has completed once the softmax observed the last o_done; free TMEM
+  // every tcgen05 op has completed once the softmax observed o_done of both tiles; free TMEM
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -633,7 +637,7 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   p.status = status;
   p.ppt = kM / G;
   p.scale2 = a->sm_scale * kLog2e;
-  dim3 grid((a->max_q_len + p.ppt - 1) / p.ppt, a->num_kv_heads, a->num_reqs);
+  dim3 grid((a->max_q_len + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_reqs);
   extend_tc_kernel<<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
   count_launches(1);
   return check_launch("rc_extend_attention (tensor cores)");
