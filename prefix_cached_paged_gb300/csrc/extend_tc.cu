@@ -12,6 +12,9 @@
 //
 // The two query tiles ping-pong on the tensor core: while the softmax of tile A turns its scores
 // into weights, the MMA warp runs P.V and the next Q K^T of tile B, and the other way round.
+// A CTA with a single query tile (short suffixes) splits its key tiles instead: the even key
+// tiles form virtual tile 0 and the odd ones virtual tile 1, each with its own running max, sum
+// and O accumulator, merged with log-sum-exp weights at the end.
 //
 // TMEM (512 columns): S_A [0,128) S_B [128,256) scores (fp32); O_A [256,384) O_B [384,512)
 // outputs (fp32). The bf16 weights P overwrite the score columns they came from (each thread
@@ -67,7 +70,8 @@ struct SmemLayout {
   // partner exchange: row maxima [tile][parity][half][row], sums [tile][which][half][row]
   static constexpr int XMAX = TMEM_SLOT + 16;
   static constexpr int XSUM = XMAX + 2 * 2 * 2 * 128 * 4;
-  static constexpr int TOTAL = XSUM + 2 * 2 * 2 * 128 * 4;
+  static constexpr int XMRG = XSUM + 2 * 2 * 2 * 128 * 4;       // split-mode maxima [X][hf][row]
+  static constexpr int TOTAL = XMRG + 2 * 2 * 128 * 4;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base to 1024 bytes
 };
 static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
@@ -248,6 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int nB = nposB > 0 ? n_pre + (iB + nposB + kN - 1) / kN : 0;
   const int ntiles = max(nA, nB);
   const int kend = nposB > 0 ? iB + nposB : iA + nposA;  // new-token keys loaded: [0, kend)
+  // virtual tiles: pair mode (query tiles A and B, every key tile each) or split mode (query
+  // tile A only; key tile 2t + X is local tile t of virtual tile X)
+  const bool split = nposB == 0 && nA >= 2;
+  const int nt0 = split ? (nA + 1) / 2 : nA;
+  const int nt1 = split ? nA / 2 : nB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
 
@@ -278,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_init(&o_done[s], 1);
       mbar_init(&x_done[2 * s], kGroupThreads);
       mbar_init(&x_done[2 * s + 1], kGroupThreads);
-      mbar_init(&e_done[s], kGroupThreads);
+      mbar_init(&e_done[s], split ? 2 * kGroupThreads : kGroupThreads);
     }
     fence_mbar_init();
   }
@@ -312,32 +321,37 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
-    // key tile j is read first by tile A (if j < nA), last by tile B (if j < nB)
-    auto qk = [&](int X, int j) -> bool {
-      const int st = j & 1;
-      const bool first = X == 0 || j >= nA;
-      if (first && !mbar_wait(&k_full[st], (j >> 1) & 1, p.status)) return false;
+    // local tile t of virtual tile X reads key tile kt; in pair mode key tile j is read first by
+    // tile A (if j < nA) and last by tile B (if j < nB), in split mode by one virtual tile only
+    auto kt_of = [&](int X, int t) { return split ? 2 * t + X : t; };
+    auto qk = [&](int X, int t) -> bool {
+      const int kt = kt_of(X, t), st = kt & 1;
+      const bool first = split || X == 0 || kt >= nA;
+      const bool last = split || X == 1 || kt >= nB;
+      if (first && !mbar_wait(&k_full[st], (kt >> 1) & 1, p.status)) return false;
       fence_async_smem();   // K arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
+        const uint32_t qsrc = sQ + (split ? 0 : X) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sQ + X * kTileBytes + off, 16, 1024);
+          const uint64_t ad = smem_desc_sw128(qsrc + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024);
           mma_bf16(tmem + X * 128, ad, bd, idq, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&s_full[X]));
-        if (X == 1 || j >= nB) mma_commit(smem_u32(&k_empty[st]));
+        if (last) mma_commit(smem_u32(&k_empty[st]));
       }
       __syncwarp();
       return true;
     };
-    auto pv = [&](int X, int j) -> bool {
-      const int st = j & 1;
-      if (!mbar_wait(&p_full[X], j & 1, p.status)) return false;
-      const bool first = X == 0 || j >= nA;
-      if (first && !mbar_wait(&v_full[st], (j >> 1) & 1, p.status)) return false;
+    auto pv = [&](int X, int t) -> bool {
+      const int kt = kt_of(X, t), st = kt & 1;
+      if (!mbar_wait(&p_full[X], t & 1, p.status)) return false;
+      const bool first = split || X == 0 || kt >= nA;
+      const bool last = split || X == 1 || kt >= nB;
+      if (first && !mbar_wait(&v_full[st], (kt >> 1) & 1, p.status)) return false;
       fence_async_smem();   // V arrived through the generic proxy (cp.async)
       tc_fence_after();
       if (lane == 0) {
@@ -348,24 +362,24 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           const uint32_t at = tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
           // B = V (MN-major: d contiguous, keys as rows)
           const uint64_t bd = smem_desc_sw128(sV + st * kTileBytes + kk * 2048, kBlockBytes, 1024);
-          mma_bf16_ts(tmem + 256 + X * 128, at, bd, idv, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 256 + X * 128, at, bd, idv, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        if (j == (X ? nB : nA) - 1) mma_commit(smem_u32(&o_done[X]));
-        if (X == 1 || j >= nB) mma_commit(smem_u32(&v_empty[st]));
+        if (t == (X ? nt1 : nt0) - 1) mma_commit(smem_u32(&o_done[X]));
+        if (last) mma_commit(smem_u32(&v_empty[st]));
       }
       __syncwarp();
       return true;
     };
     bool ok = __all_sync(0xffffffffu, qk(0, 0));
-    if (ok && nB > 0) ok = __all_sync(0xffffffffu, qk(1, 0));
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (j < nA) {
-        ok = __all_sync(0xffffffffu, pv(0, j));
-        if (ok && j + 1 < nA) ok = __all_sync(0xffffffffu, qk(0, j + 1));
+    if (ok && nt1 > 0) ok = __all_sync(0xffffffffu, qk(1, 0));
+    for (int t = 0; t < max(nt0, nt1) && ok; ++t) {
+      if (t < nt0) {
+        ok = __all_sync(0xffffffffu, pv(0, t));
+        if (ok && t + 1 < nt0) ok = __all_sync(0xffffffffu, qk(0, t + 1));
       }
-      if (ok && j < nB) {
-        ok = __all_sync(0xffffffffu, pv(1, j));
-        if (ok && j + 1 < nB) ok = __all_sync(0xffffffffu, qk(1, j + 1));
+      if (ok && t < nt1) {
+        ok = __all_sync(0xffffffffu, pv(1, t));
+        if (ok && t + 1 < nt1) ok = __all_sync(0xffffffffu, qk(1, t + 1));
       }
     }
   } else if (warp == kKWarp || warp == kVWarp) {
@@ -475,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const int quad = warp & 3;                        // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;                   // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int nX = X ? nB : nA;
-    const int iX = X ? iB : iA;
-    const int rows_used = (X ? nposB : nposA) * G;
+    const int nX = X ? nt1 : nt0;
+    const int iX = (X && !split) ? iB : iA;
+    const int rows_used = ((X && !split) ? nposB : nposA) * G;
     const int ipos = min(iX + r / G, S - 1);          // this row's new-token index (clamped)
     const float sc2 = p.scale2;
     const uint64_t sc2x2 = f2pack(sc2, sc2);
@@ -493,8 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // keys [0, lim) of this tile are visible to this row
-      const int lim = j < n_pre ? min(kN, P - j * kN) : min(kN, ipos - (j - n_pre) * kN + 1);
+      // keys [0, lim) of key tile kt are visible to this row (lim <= 0: none)
+      const int kt = split ? 2 * j + X : j;
+      const int lim = kt < n_pre ? min(kN, P - kt * kN) : min(kN, ipos - (kt - n_pre) * kN + 1);
       const bool full = __all_sync(0xffffffffu, lim >= c0 + 64);
       // pass 1: row max of the raw scores, combined with the partner thread
       float mx = -INFINITY;
@@ -523,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
       const float alpha = (rescale && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
-      const uint64_t negx2 = f2pack(-m_use, -m_use);
+      // a row with no visible key so far keeps m = -inf; subtract 0 so masked scores give 0
+      const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+      const uint64_t negx2 = f2pack(-m_sub, -m_sub);
       // pass 2: weights, rounded to bf16 and written over this thread's own score columns
       uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
 #pragma unroll 1
@@ -573,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_arrive(&p_full[X]);
     }
     // epilogue: full denominators from both halves, then this thread's half of the O row
-    if (nX > 0) {
+    if (nX > 0 && !split) {
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
       xsum[((X * 2 + 0) * 2 + hf) * 128 + r] = l_run;
       xsum[((X * 2 + 1) * 2 + hf) * 128 + r] = l_exact;
@@ -606,6 +623,52 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         if (store && hf == 0 && a.lse)
           a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
+      }
+    } else if (split) {
+      // merge the two virtual tiles: every softmax thread publishes its row max and half sums;
+      // thread (X, hf) then writes columns [64 hf + 32 X, 64 hf + 32 X + 32) of the merged row
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
+      float* xm = (float*)(smem + SmemLayout::XMRG);     // [X][hf][row] row maxima
+      xm[(X * 2 + hf) * 128 + r] = m_run;
+      xsum[((X * 2 + 0) * 2 + hf) * 128 + r] = l_run;
+      xsum[((X * 2 + 1) * 2 + hf) * 128 + r] = l_exact;
+      mbar_arrive(&e_done[0]);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&e_done[0], 0, p.status));
+      if (ok) {
+        // sums published as xsum[((virtual tile * 2 + which) * 2 + half) * 128 + row],
+        // which = 0 for the rounded-weight sum, 1 for the exact sum
+        auto xs = [&](int vt, int which, int h) { return xsum[((vt * 2 + which) * 2 + h) * 128 + r]; };
+        const float m0 = xm[(0 * 2 + 0) * 128 + r], m1 = xm[(1 * 2 + 0) * 128 + r];
+        const float L0 = xs(0, 0, 0) + xs(0, 0, 1), E0 = xs(0, 1, 0) + xs(0, 1, 1);
+        const float L1 = xs(1, 0, 0) + xs(1, 0, 1), E1 = xs(1, 1, 0) + xs(1, 1, 1);
+        const float M = fmaxf(m0, m1);
+        const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
+        const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+        const float lt = w0 * L0 + w1 * L1;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float a0 = w0 * inv, a1 = w1 * inv;
+        tc_fence_after();
+        const int col = c0 + 32 * X;
+        float o0[32], o1[32];
+        tmem_ld32(tmem + 256 + lane_off + col, o0);
+        tmem_ld32(tmem + 384 + lane_off + col, o1);
+        tmem_wait_ld();
+        const bool store = r < rows_used;
+        const int i = iA + r / G, hh = r % G;
+        if (store) {
+          __nv_bfloat16* orow =
+              (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + col;
+#pragma unroll
+          for (int u = 0; u < 32; u += 8) {
+            float v8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v8[k] = o0[u + k] * a0 + o1[u + k] * a1;
+            *(uint4*)(orow + u) = make_uint4(pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
+                                             pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+          }
+          if (X == 0 && hf == 0 && a.lse)
+            a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (M + log2f(w0 * E0 + w1 * E1)) * kLn2;
+        }
       }
     }
   }
