@@ -17,25 +17,25 @@
 // and O accumulator, merged with log-sum-exp weights at the end.
 //
 // TMEM (512 columns): S_A [0,128) S_B [128,256) scores (fp32); O_A [256,384) O_B [384,512)
-// outputs (fp32). The bf16 weights P overwrite the score columns they came from (each thread
-// writes the weights of its 64 keys as 32 packed columns at the start of its own score columns)
-// and feed P.V straight from TMEM as the A operand.
+// outputs (fp32). The bf16 weights P overwrite the first 64 columns of the scores they came from
+// (two weights per 32-bit column) and feed P.V straight from TMEM as the A operand.
 //
-// Warp roles (640 threads):
+// Warp roles (512 threads):
 //   warp 0       allocates TMEM and issues every tcgen05.mma from one lane;
-//   warps 1, 2   producers for K and V: gather the key tile's rows (256 B, one slot per row)
-//                with 16-byte cp.async copies straight into the 128-byte-swizzled operand
-//                layout, two rows per instruction (fully coalesced); completion is signalled
-//                with cp.async.mbarrier.arrive.noinc. (TMA tile::gather4 moves 512 B per
-//                instruction and, measured here, its issue rate capped a 256-byte row gather at
-//                about 2 TB/s GPU-wide; the copy path does not.)
-//   warp 3       scatters the new tokens' K/V rows into their pool slots;
-//   warps 4-19   softmax: four groups of four warps, (query tile, column half); two threads per
-//                query row, 64 columns each. Two passes over the scores (row max, combined with
-//                the partner thread through shared memory; then exp2 with the scale folded
-//                into one packed FMA); lazy rescale of O (only when the running max grows by
-//                more than 8 in log2 units); weights rounded to bf16, normalised by the sum of
-//                the rounded weights; epilogue O / l.
+//   warps 1-4    producers, two for K and two for V, each filling half of a key tile's rows
+//                (256 B, one slot per row) with 16-byte cp.async copies straight into the
+//                128-byte-swizzled operand layout, two rows per instruction (fully coalesced);
+//                completion is signalled with cp.async.mbarrier.arrive.noinc. (TMA
+//                tile::gather4 moves 512 B per instruction and, measured here, its issue rate
+//                capped a 256-byte row gather at about 2 TB/s GPU-wide; the copy path does not.
+//                The copy path is itself bound by instruction issue, hence two warps per
+//                operand and one shuffled row pointer per copy.)
+//   warps 5-7    scatter the new tokens' K/V rows into their pool slots;
+//   warps 8-11   softmax of query tile A, warps 12-15 of tile B: one thread per query row holds
+//                the row's 128 scores in registers; one pass (row max, then exp2 with the scale
+//                folded into one packed FMA); lazy rescale of O (only when the running max
+//                grows by more than 8 in log2 units); weights rounded to bf16, normalised by
+//                the sum of the rounded weights; epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
 #include <mutex>
 
@@ -52,11 +52,19 @@ constexpr int kN = 128;           // keys per tile
 constexpr int kStagesKV = 2;
 constexpr int kTileBytes = kM * kD * 2;   // 32 KB: one 128 x 128 bf16 operand tile
 constexpr int kBlockBytes = kM * 128;     // 16 KB: one 64-column block of a tile
-constexpr int kThreads = 640;
+constexpr int kThreads = 512;
 constexpr int kMmaWarp = 0;
-constexpr int kKWarp = 1, kVWarp = 2, kScatterWarp = 3;
-constexpr int kSoftmaxWarp0 = 4;
-constexpr int kGroupThreads = 256;        // softmax threads of one query tile
+constexpr int kProdWarps = 2;             // producer warps per operand
+constexpr int kKWarp0 = 1, kVWarp0 = kKWarp0 + kProdWarps;
+constexpr int kScatterWarp0 = kVWarp0 + kProdWarps, kScatterWarps = 3;
+constexpr int kSoftmaxWarp0 = kScatterWarp0 + kScatterWarps;
+static_assert(kSoftmaxWarp0 == 8 && kThreads == 32 * (kSoftmaxWarp0 + 8), "warp roles");
+constexpr int kGroupThreads = 128;        // softmax threads of one query tile (one per row)
+// control warpgroups (warps 0-7) give registers up, the softmax warpgroups (8-15) take them
+constexpr int kRegsLaunch = 128, kRegsControl = 64, kRegsSoftmax = 192;
+static_assert(kThreads * kRegsLaunch <= 65536, "register file");
+static_assert(256 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "a register split above the launch allocation never completes");
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
 
 struct SmemLayout {
@@ -64,14 +72,12 @@ struct SmemLayout {
   static constexpr int K = Q + 2 * kTileBytes;
   static constexpr int V = K + kStagesKV * kTileBytes;
   static constexpr int BAR = V + kStagesKV * kTileBytes;
-  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] x_done[2][2] e_done[2]
-  static constexpr int NBAR = 20;
+  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] e_done q_full
+  static constexpr int NBAR = 16;
   static constexpr int TMEM_SLOT = BAR + NBAR * 8;
-  // partner exchange: row maxima [tile][parity][half][row], sums [tile][which][half][row]
-  static constexpr int XMAX = TMEM_SLOT + 16;
-  static constexpr int XSUM = XMAX + 2 * 2 * 2 * 128 * 4;
-  static constexpr int XMRG = XSUM + 2 * 2 * 2 * 128 * 4;       // split-mode maxima [X][hf][row]
-  static constexpr int TOTAL = XMRG + 2 * 2 * 128 * 4;
+  // split-mode merge: row maxima, rounded and exact sums of each virtual tile [X][row]
+  static constexpr int XMRG = TMEM_SLOT + 16;
+  static constexpr int TOTAL = XMRG + 3 * 2 * 128 * 4;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base to 1024 bytes
 };
 static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
@@ -86,6 +92,11 @@ struct TcParams {
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// 16-byte copy that reads `bytes` (0 or 16) from global memory and zero-fills the rest
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
@@ -213,13 +224,32 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum));
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+// Ties 32 registers written by tcgen05.ld to a point after tcgen05.wait::ld, so that no use of
+// them is scheduled before the wait.
+__device__ __forceinline__ void reg_fence32(float* v) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
+                 "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
+                 "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
+                 "+f"(v[30]), "+f"(v[31]));
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -272,23 +302,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint64_t* s_full = bars + 8;     // [tile]
   uint64_t* p_full = bars + 10;    // [tile]
   uint64_t* o_done = bars + 12;    // [tile]
-  uint64_t* x_done = bars + 14;    // [tile][parity]
-  uint64_t* e_done = bars + 18;    // [tile]
+  uint64_t* e_done = bars + 14;    // split-mode merge
+  uint64_t* q_full = bars + 15;    // both Q tiles in shared memory
   uint32_t* tmem_slot = (uint32_t*)(smem + SmemLayout::TMEM_SLOT);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 32);
+      mbar_init(&k_full[s], 32 * kProdWarps);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 32);
+      mbar_init(&v_full[s], 32 * kProdWarps);
       mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], kGroupThreads);
       mbar_init(&o_done[s], 1);
-      mbar_init(&x_done[2 * s], kGroupThreads);
-      mbar_init(&x_done[2 * s + 1], kGroupThreads);
-      mbar_init(&e_done[s], split ? 2 * kGroupThreads : kGroupThreads);
     }
+    mbar_init(e_done, 2 * kGroupThreads);
+    mbar_init(q_full, kThreads);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -298,28 +327,37 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // Q tiles: row m of tile X = (position iX + m / G, head hk * G + m % G); rows past the tile
-  // are zero
+  // are zero-filled. Copied asynchronously (every thread, 16 bytes at a time); the MMA warp
+  // waits on q_full, so the copies overlap TMEM allocation and the first K/V loads.
   {
     const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
-    for (int e = threadIdx.x; e < 2 * kM * 16; e += kThreads) {
+    const uint32_t sQ0 = smem_u32(smem) + SmemLayout::Q;
+#pragma unroll
+    for (int k = 0; k < 2 * kM * 16 / kThreads; ++k) {
+      const int e = threadIdx.x + k * kThreads;
       const int X = e >> 11, m = (e >> 4) & 127, c = e & 15;
       const int i0 = X ? iB : iA, np = X ? nposB : nposA;
-      uint4 v = make_uint4(0, 0, 0, 0);
+      const __nv_bfloat16* src = q;
+      uint32_t bytes = 0;
       if (m < np * G) {
         const int i = i0 + m / G, hh = m % G;
-        v = *(const uint4*)(q + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c * 8);
+        src = q + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c * 8;
+        bytes = 16;
       }
-      *(uint4*)(smem + SmemLayout::Q + X * kTileBytes + sw128_off(m, c)) = v;
+      cp_async16_zfill(sQ0 + X * kTileBytes + sw128_off(m, c), src, bytes);
     }
   }
-  fence_async_smem();
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();   // barrier initialisation and the TMEM address are visible from here
   tc_fence_after();
+  cp_async_arrive_noinc(smem_u32(q_full));
   const uint32_t tmem = *tmem_slot;
-
+  // register split (each role branch starts with its setmaxnreg, so that its code is compiled
+  // for its own budget): launched with kRegsLaunch per thread; the control warpgroup (warps 0-3)
+  // gives registers up, the two softmax warpgroups take them
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
     // local tile t of virtual tile X reads key tile kt; in pair mode key tile j is read first by
     // tile A (if j < nA) and last by tile B (if j < nB), in split mode by one virtual tile only
@@ -358,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const uint32_t tS = tmem + X * 128;
 #pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk) {
-          // A = P from TMEM: keys [0,64) in score columns [0,32), keys [64,128) in [64,96)
-          const uint32_t at = tS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          // A = P from TMEM: keys [16 kk, 16 kk + 16) in score columns [8 kk, 8 kk + 8)
+          const uint32_t at = tS + kk * 8;
           // B = V (MN-major: d contiguous, keys as rows)
           const uint64_t bd = smem_desc_sw128(sV + st * kTileBytes + kk * 2048, kBlockBytes, 1024);
           mma_bf16_ts(tmem + 256 + X * 128, at, bd, idv, (t > 0 || kk > 0) ? 1u : 0u);
@@ -370,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       __syncwarp();
       return true;
     };
-    bool ok = __all_sync(0xffffffffu, qk(0, 0));
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.status));
+    fence_async_smem();   // Q arrived through the generic proxy (cp.async)
+    if (ok) ok = __all_sync(0xffffffffu, qk(0, 0));
     if (ok && nt1 > 0) ok = __all_sync(0xffffffffu, qk(1, 0));
     for (int t = 0; t < max(nt0, nt1) && ok; ++t) {
       if (t < nt0) {
@@ -382,83 +422,92 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (ok && t + 1 < nt1) ok = __all_sync(0xffffffffu, qk(1, t + 1));
       }
     }
-  } else if (warp == kKWarp || warp == kVWarp) {
-    // ------------------------------------------------------------ producers (K: warp 1, V: 2)
-    // Lane l resolves the source rows of tile rows l, l+32, l+64, l+96; one copy instruction
-    // moves 16-byte chunk (l & 15) of two rows.
+  } else if (warp < kScatterWarp0) {
+    // ------------------------------------------------------------ producers (K: warps 1-2, V: 3-4)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    // Producer w of an operand fills tile rows [64 w, 64 w + 64): lane l resolves rows
+    // 64 w + l and 64 w + 32 + l to a row pointer; one copy instruction then moves 16-byte chunk
+    // (l & 15) of two rows, the row pointer taken from its owner lane by a shuffle.
     const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
-    const bool is_v = warp == kVWarp;
+    const bool is_v = warp >= kVWarp0;
+    const int w = warp - (is_v ? kVWarp0 : kKWarp0);
+    constexpr int kRowsPerWarp = kN / kProdWarps;
+    constexpr int kGroups = kRowsPerWarp / 32;
     const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
     const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
     uint64_t* full = is_v ? v_full : k_full;
     uint64_t* empty = is_v ? v_empty : k_empty;
-    const uint32_t sdst = is_v ? sV : sK;
-    // raw(j, q) only issues the slot load; rowof() checks it when the tile is issued, so the
+    const int c = lane & 15, half = lane >> 4;
+    // destination of row 2 i + half (i = 0..15) of a 32-row group, chunk c: the swizzle term
+    // repeats every four values of i; the row term adds 1024 bytes per four
+    uint32_t d4[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) d4[m] = sw128_off(2 * m + half, c);
+    const uint32_t sbuf = (is_v ? sV : sK) + (uint32_t)(w * kRowsPerWarp * 128);
+    // raw(j, q) only issues the slot load; rowptr() checks it when the tile is issued, so the
     // loads of tile j+1 stay in flight while tile j is being copied
     auto raw = [&](int j, int q) -> int {
       if (j < n_pre) {
-        const int key = j * kN + q * 32 + lane;
+        const int key = j * kN + w * kRowsPerWarp + q * 32 + lane;
         return rt[key < P ? key : P - 1];
       }
       return 0;
     };
-    auto rowof = [&](int j, int q, int rv) -> int {
+    auto rowptr = [&](int j, int q, int rv) -> const __nv_bfloat16* {
       if (j < n_pre) {
         int sl = rv;
         if (sl < 0 || (int64_t)sl >= a.num_slots) {
           set_status(p.status, kStatusSlotRange);
           sl = 0;
         }
-        return sl * Hkv + hk;
+        return pool + ((int64_t)sl * Hkv + hk) * kD;
       }
-      const int s0 = (j - n_pre) * kN + q * 32 + lane;
-      return (qo + min(s0, kend - 1)) * Hkv + hk;
+      const int s0 = (j - n_pre) * kN + w * kRowsPerWarp + q * 32 + lane;
+      return nsrc + ((int64_t)(qo + min(s0, kend - 1)) * Hkv + hk) * kD;
     };
-    int n0 = raw(0, 0), n1 = raw(0, 1), n2 = raw(0, 2), n3 = raw(0, 3);
+    static_assert(kGroups == 2, "two 32-row groups per producer warp");
+    int n0 = raw(0, 0), n1 = raw(0, 1);
     bool ok = true;
-    const int c = lane & 15, half = lane >> 4;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
-      const int r0 = rowof(j, 0, n0), r1 = rowof(j, 1, n1), r2 = rowof(j, 2, n2),
-                r3 = rowof(j, 3, n3);
+      const __nv_bfloat16* p0 = rowptr(j, 0, n0);
+      const __nv_bfloat16* p1 = rowptr(j, 1, n1);
       if (j + 1 < ntiles) {
         n0 = raw(j + 1, 0);
         n1 = raw(j + 1, 1);
-        n2 = raw(j + 1, 2);
-        n3 = raw(j + 1, 3);
       }
-      const __nv_bfloat16* src = j < n_pre ? pool : nsrc;
       if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j >> 1) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const uint32_t dst = sdst + st * kTileBytes;
+      const uint32_t dst = sbuf + st * kTileBytes;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int rq = q == 0 ? r0 : q == 1 ? r1 : q == 2 ? r2 : r3;
-#pragma unroll 4
+      for (int q = 0; q < kGroups; ++q) {
+        const uint64_t rp = (uint64_t)(q == 0 ? p0 : p1);
+#pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int rr = 2 * i + half;
-          const int srow = __shfl_sync(0xffffffffu, rq, rr);
-          cp_async16(dst + sw128_off(q * 32 + rr, c), src + (int64_t)srow * kD + c * 8);
+          const __nv_bfloat16* src =
+              (const __nv_bfloat16*)__shfl_sync(0xffffffffu, rp, 2 * i + half) + c * 8;
+          cp_async16(dst + q * 32 * 128 + (i >> 2) * 1024 + d4[i & 3], src);
         }
       }
       cp_async_arrive_noinc(smem_u32(&full[st]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kScatterWarp) {
+  } else if (warp < kSoftmaxWarp0) {
     // ------------------------------------------------------------ scatter of the new K/V rows
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     // (row, 16-byte chunk) pairs of both query tiles' positions; each round issues all of a
-    // lane's loads before any store, eight copies in flight per lane.
+    // lane's loads before any store, four copies in flight per lane.
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
-    constexpr int kU = 8;
+    constexpr int kU = 4;
     const int total = (nposA + nposB) * 16;
-    for (int base = lane; base < total; base += 32 * kU) {
+    for (int base = (warp - kScatterWarp0) * 32 + lane; base < total; base += 32 * kScatterWarps * kU) {
       uint4 kv[kU], vv[kU];
       int64_t dst[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int e = base + u * 32;
+        const int e = base + u * 32 * kScatterWarps;
         dst[u] = -1;
         if (e < total) {
           const int i = iA + (e >> 4), cc = e & 15;
@@ -483,9 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------------------ softmax groups
-    const int g = (warp - kSoftmaxWarp0) >> 2;
-    const int X = g >> 1;                             // query tile
-    const int hf = g & 1;                             // column half: [64 hf, 64 hf + 64)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int X = (warp - kSoftmaxWarp0) >> 2;        // query tile (virtual tile in split mode)
     const int quad = warp & 3;                        // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;                   // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -497,9 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const uint64_t sc2x2 = f2pack(sc2, sc2);
     const uint32_t tS = tmem + X * 128 + lane_off;
     const uint32_t tO = tmem + 256 + X * 128 + lane_off;
-    const int c0 = hf * 64;                           // first score column of this thread
-    float* xmax = (float*)(smem + SmemLayout::XMAX);  // [tile][parity][half][row]
-    float* xsum = (float*)(smem + SmemLayout::XSUM);  // [tile][which][half][row]
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     for (int j = 0; j < nX; ++j) {
@@ -510,30 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // keys [0, lim) of key tile kt are visible to this row (lim <= 0: none)
       const int kt = split ? 2 * j + X : j;
       const int lim = kt < n_pre ? min(kN, P - kt * kN) : min(kN, ipos - (kt - n_pre) * kN + 1);
-      const bool full = __all_sync(0xffffffffu, lim >= c0 + 64);
-      // pass 1: row max of the raw scores, combined with the partner thread
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tS + c0 + c * 32, v);
-        tmem_wait_ld();
-        if (full) {
+      float v[kN];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) mx = fmaxf(mx, v[u]);
-        } else {
+      for (int c = 0; c < kN / 32; ++c) tmem_ld32(tS + c * 32, v + c * 32);
+      tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 32; ++u) mx = fmaxf(mx, c0 + c * 32 + u < lim ? v[u] : -INFINITY);
-        }
+      for (int c = 0; c < kN / 32; ++c) reg_fence32(v + c * 32);
+      if (!__all_sync(0xffffffffu, lim >= kN)) {
+#pragma unroll
+        for (int u = 0; u < kN; ++u) v[u] = u < lim ? v[u] : -INFINITY;
       }
-      const int par = j & 1;
-      xmax[((X * 2 + par) * 2 + hf) * 128 + r] = mx;
-      mbar_arrive(&x_done[X * 2 + par]);
-      ok = mbar_wait(&x_done[X * 2 + par], (j >> 1) & 1, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      mx = fmaxf(mx, xmax[((X * 2 + par) * 2 + (hf ^ 1)) * 128 + r]);
-      const float mt = mx * sc2;                      // sc2 > 0: max commutes with the scale
+      // row max of the raw scores: four running three-input maxima
+      float m4[4] = {fmaxf(v[0], v[1]), fmaxf(v[2], v[3]), fmaxf(v[4], v[5]), fmaxf(v[6], v[7])};
+#pragma unroll
+      for (int u = 8; u < kN; u += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], v[u + 2 * k], v[u + 2 * k + 1]);
+      }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float mt = mx * sc2;                   // sc2 > 0: max commutes with the scale
       const float m_new = fmaxf(m_run, mt);
       const bool rescale = m_new > m_run + kRescaleThreshold;  // also true for the first tile
       const float m_use = rescale ? m_new : m_run;
@@ -541,22 +581,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // a row with no visible key so far keeps m = -inf; subtract 0 so masked scores give 0
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
       const uint64_t negx2 = f2pack(-m_sub, -m_sub);
-      // pass 2: weights, rounded to bf16 and written over this thread's own score columns
+      // weights, rounded to bf16, two per column in the first 64 score columns
       uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tS + c0 + c * 32, v);
-        tmem_wait_ld();
-        if (!full) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = c0 + c * 32 + u < lim ? v[u] : -INFINITY;
-        }
-        uint32_t pk[16];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 32; ++u) {
           float x0, x1;
-          f2unpack(fma2(f2pack(v[2 * u], v[2 * u + 1]), sc2x2, negx2), x0, x1);
+          f2unpack(fma2(f2pack(v[64 * h + 2 * u], v[64 * h + 2 * u + 1]), sc2x2, negx2), x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
           pk[u] = pack_bf16(p0, p1);
           // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp
@@ -564,19 +597,19 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           rs2 = add2(rs2, f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
           re2 = add2(re2, f2pack(p0, p1));
         }
-        // columns c0 + 16c .. c0 + 16c + 15 were read in chunk 0: free to overwrite
-        tmem_st16(tS + c0 + c * 16, pk);
+        tmem_st32u(tS + 32 * h, pk);
       }
-      // rescale this thread's half of O: its last P.V completed before these scores did
+      // rescale O: the last P.V of this tile completed before these scores did
       if (__any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0) {
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kD / 32; ++c) {
           float o[32];
-          tmem_ld32(tO + c0 + c * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
+          reg_fence32(o);
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] *= alpha;
-          tmem_st32(tO + c0 + c * 32, o);
+          tmem_st32(tO + c * 32, o);
         }
       }
       tmem_wait_st();
@@ -589,27 +622,21 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       tc_fence_before();
       mbar_arrive(&p_full[X]);
     }
-    // epilogue: full denominators from both halves, then this thread's half of the O row
     if (nX > 0 && !split) {
+      // epilogue: O / l for this thread's row
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
-      xsum[((X * 2 + 0) * 2 + hf) * 128 + r] = l_run;
-      xsum[((X * 2 + 1) * 2 + hf) * 128 + r] = l_exact;
-      mbar_arrive(&e_done[X]);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&e_done[X], 0, p.status));
-      l_run += xsum[((X * 2 + 0) * 2 + (hf ^ 1)) * 128 + r];
-      l_exact += xsum[((X * 2 + 1) * 2 + (hf ^ 1)) * 128 + r];
       if (ok) {
         tc_fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const bool store = r < rows_used;
         const int i = iX + r / G, hh = r % G;
-        __nv_bfloat16* orow =
-            (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c0;
+        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD;
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kD / 32; ++c) {
           float o[32];
-          tmem_ld32(tO + c0 + c * 32, o);
+          tmem_ld32(tO + c * 32, o);
           tmem_wait_ld();
+          reg_fence32(o);
           if (store) {
 #pragma unroll
             for (int u = 0; u < 32; u += 8) {
@@ -621,54 +648,56 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
             }
           }
         }
-        if (store && hf == 0 && a.lse)
+        if (store && a.lse)
           a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
       }
     } else if (split) {
-      // merge the two virtual tiles: every softmax thread publishes its row max and half sums;
-      // thread (X, hf) then writes columns [64 hf + 32 X, 64 hf + 32 X + 32) of the merged row
+      // merge the two virtual tiles: every softmax thread publishes its row max and sums;
+      // thread (X, row) then writes columns [64 X, 64 X + 64) of the merged row
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
-      float* xm = (float*)(smem + SmemLayout::XMRG);     // [X][hf][row] row maxima
-      xm[(X * 2 + hf) * 128 + r] = m_run;
-      xsum[((X * 2 + 0) * 2 + hf) * 128 + r] = l_run;
-      xsum[((X * 2 + 1) * 2 + hf) * 128 + r] = l_exact;
-      mbar_arrive(&e_done[0]);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&e_done[0], 0, p.status));
+      float* xm = (float*)(smem + SmemLayout::XMRG);     // [X][row] maxima
+      float* xl = xm + 2 * 128;                          // [X][row] rounded-weight sums
+      float* xe = xl + 2 * 128;                          // [X][row] exact sums
+      xm[X * 128 + r] = m_run;
+      xl[X * 128 + r] = l_run;
+      xe[X * 128 + r] = l_exact;
+      mbar_arrive(e_done);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(e_done, 0, p.status));
       if (ok) {
-        // sums published as xsum[((virtual tile * 2 + which) * 2 + half) * 128 + row],
-        // which = 0 for the rounded-weight sum, 1 for the exact sum
-        auto xs = [&](int vt, int which, int h) { return xsum[((vt * 2 + which) * 2 + h) * 128 + r]; };
-        const float m0 = xm[(0 * 2 + 0) * 128 + r], m1 = xm[(1 * 2 + 0) * 128 + r];
-        const float L0 = xs(0, 0, 0) + xs(0, 0, 1), E0 = xs(0, 1, 0) + xs(0, 1, 1);
-        const float L1 = xs(1, 0, 0) + xs(1, 0, 1), E1 = xs(1, 1, 0) + xs(1, 1, 1);
+        const float m0 = xm[r], m1 = xm[128 + r];
         const float M = fmaxf(m0, m1);
         const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
         const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-        const float lt = w0 * L0 + w1 * L1;
+        const float lt = w0 * xl[r] + w1 * xl[128 + r];
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const float a0 = w0 * inv, a1 = w1 * inv;
         tc_fence_after();
-        const int col = c0 + 32 * X;
-        float o0[32], o1[32];
-        tmem_ld32(tmem + 256 + lane_off + col, o0);
-        tmem_ld32(tmem + 384 + lane_off + col, o1);
-        tmem_wait_ld();
         const bool store = r < rows_used;
         const int i = iA + r / G, hh = r % G;
-        if (store) {
-          __nv_bfloat16* orow =
-              (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + col;
+        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col = 64 * X + 32 * c;
+          float o0[32], o1[32];
+          tmem_ld32(tmem + 256 + lane_off + col, o0);
+          tmem_ld32(tmem + 384 + lane_off + col, o1);
+          tmem_wait_ld();
+          reg_fence32(o0);
+          reg_fence32(o1);
+          if (store) {
 #pragma unroll
-          for (int u = 0; u < 32; u += 8) {
-            float v8[8];
+            for (int u = 0; u < 32; u += 8) {
+              float v8[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v8[k] = o0[u + k] * a0 + o1[u + k] * a1;
-            *(uint4*)(orow + u) = make_uint4(pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
-                                             pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+              for (int k = 0; k < 8; ++k) v8[k] = o0[u + k] * a0 + o1[u + k] * a1;
+              *(uint4*)(orow + col + u) = make_uint4(pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
+                                                     pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+            }
           }
-          if (X == 0 && hf == 0 && a.lse)
-            a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (M + log2f(w0 * E0 + w1 * E1)) * kLn2;
         }
+        if (store && X == 0 && a.lse)
+          a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] =
+              (M + log2f(w0 * xe[r] + w1 * xe[128 + r])) * kLn2;
       }
     }
   }
@@ -689,12 +718,20 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   if (G > kM) return fail(RC_ERR_INVALID, "extend (tensor cores): group size %d > 128", G);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int launch_regs = 0;
   std::call_once(once, []() {
     attr_err = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SmemLayout::ALLOC);
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, extend_tc_kernel);
+    if (attr_err == cudaSuccess) launch_regs = fa.numRegs;
   });
   if (attr_err != cudaSuccess)
     return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(attr_err));
+  // the softmax warpgroups' setmaxnreg.inc only completes if the launch allocation covers the split
+  if (launch_regs < kRegsLaunch)
+    return fail(RC_ERR_CUDA, "extend (tensor cores): kernel built with %d registers per thread, "
+                "the register split needs %d", launch_regs, kRegsLaunch);
   TcParams p;
   p.a = *a;
   p.status = status;
