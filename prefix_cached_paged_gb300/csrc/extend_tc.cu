@@ -61,7 +61,7 @@ constexpr int kSoftmaxWarp0 = kScatterWarp0 + kScatterWarps;
 static_assert(kSoftmaxWarp0 == 8 && kThreads == 32 * (kSoftmaxWarp0 + 8), "warp roles");
 constexpr int kGroupThreads = 128;        // softmax threads of one query tile (one per row)
 // control warpgroups (warps 0-7) give registers up, the softmax warpgroups (8-15) take them
-constexpr int kRegsLaunch = 128, kRegsControl = 64, kRegsSoftmax = 192;
+constexpr int kRegsLaunch = 128, kRegsControl = 72, kRegsSoftmax = 184;
 static_assert(kThreads * kRegsLaunch <= 65536, "register file");
 static_assert(256 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "a register split above the launch allocation never completes");
@@ -72,8 +72,8 @@ struct SmemLayout {
   static constexpr int K = Q + 2 * kTileBytes;
   static constexpr int V = K + kStagesKV * kTileBytes;
   static constexpr int BAR = V + kStagesKV * kTileBytes;
-  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] e_done q_full
-  static constexpr int NBAR = 16;
+  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] e_done q_full drain
+  static constexpr int NBAR = 4 * kStagesKV + 9;
   static constexpr int TMEM_SLOT = BAR + NBAR * 8;
   // split-mode merge: row maxima, rounded and exact sums of each virtual tile [X][row]
   static constexpr int XMRG = TMEM_SLOT + 16;
@@ -240,16 +240,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      "r"(v[15])
       : "memory");
 }
 
@@ -295,29 +292,34 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t sK = sbase + SmemLayout::K;
   const uint32_t sV = sbase + SmemLayout::V;
   uint64_t* bars = (uint64_t*)(smem + SmemLayout::BAR);
-  uint64_t* k_full = bars + 0;
-  uint64_t* k_empty = bars + 2;
-  uint64_t* v_full = bars + 4;
-  uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 8;     // [tile]
-  uint64_t* p_full = bars + 10;    // [tile]
-  uint64_t* o_done = bars + 12;    // [tile]
-  uint64_t* e_done = bars + 14;    // split-mode merge
-  uint64_t* q_full = bars + 15;    // both Q tiles in shared memory
+  uint64_t* k_full = bars;                      // [stage]
+  uint64_t* k_empty = k_full + kStagesKV;       // [stage]
+  uint64_t* v_full = k_empty + kStagesKV;       // [stage]
+  uint64_t* v_empty = v_full + kStagesKV;       // [stage]
+  uint64_t* s_full = v_empty + kStagesKV;       // [tile]
+  uint64_t* p_full = s_full + 2;                // [tile]
+  uint64_t* o_done = p_full + 2;                // [tile]
+  uint64_t* e_done = o_done + 2;                // split-mode merge
+  uint64_t* q_full = e_done + 1;                // both Q tiles in shared memory
+  uint64_t* drain = q_full + 1;                 // every issued MMA has completed
+  static_assert(4 * kStagesKV + 9 == SmemLayout::NBAR, "barrier count");
   uint32_t* tmem_slot = (uint32_t*)(smem + SmemLayout::TMEM_SLOT);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStagesKV; ++s) {
       mbar_init(&k_full[s], 32 * kProdWarps);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 32 * kProdWarps);
       mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], kGroupThreads);
       mbar_init(&o_done[s], 1);
     }
     mbar_init(e_done, 2 * kGroupThreads);
     mbar_init(q_full, kThreads);
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   {
     const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
     const uint32_t sQ0 = smem_u32(smem) + SmemLayout::Q;
+    static_assert(2 * kM * 16 % kThreads == 0, "every Q chunk is copied");
 #pragma unroll
     for (int k = 0; k < 2 * kM * 16 / kThreads; ++k) {
       const int e = threadIdx.x + k * kThreads;
@@ -358,18 +361,19 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
-    // local tile t of virtual tile X reads key tile kt; in pair mode key tile j is read first by
-    // tile A (if j < nA) and last by tile B (if j < nB), in split mode by one virtual tile only
-    auto kt_of = [&](int X, int t) { return split ? 2 * t + X : t; };
-    auto qk = [&](int X, int t) -> bool {
-      const int kt = kt_of(X, t), st = kt & 1;
-      const bool first = split || X == 0 || kt >= nA;
-      const bool last = split || X == 1 || kt >= nB;
-      if (first && !mbar_wait(&k_full[st], (kt >> 1) & 1, p.status)) return false;
-      fence_async_smem();   // K arrived through the generic proxy (cp.async)
-      tc_fence_after();
-      if (lane == 0) {
+    // One thread runs the whole schedule (waits, fences, MMAs, commits).
+    if (lane == 0) {
+      const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
+      // local tile t of virtual tile X reads key tile kt; in pair mode key tile j is read first
+      // by tile A (if j < nA) and last by tile B (if j < nB), in split mode by one virtual tile
+      auto kt_of = [&](int X, int t) { return split ? 2 * t + X : t; };
+      auto qk = [&](int X, int t) -> bool {
+        const int kt = kt_of(X, t), st = kt % kStagesKV;
+        const bool first = split || X == 0 || kt >= nA;
+        const bool last = split || X == 1 || kt >= nB;
+        if (first && !mbar_wait(&k_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+        fence_async_smem();   // K arrived through the generic proxy (cp.async)
+        tc_fence_after();
         const uint32_t qsrc = sQ + (split ? 0 : X) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -380,19 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         mma_commit(smem_u32(&s_full[X]));
         if (last) mma_commit(smem_u32(&k_empty[st]));
-      }
-      __syncwarp();
-      return true;
-    };
-    auto pv = [&](int X, int t) -> bool {
-      const int kt = kt_of(X, t), st = kt & 1;
-      if (!mbar_wait(&p_full[X], t & 1, p.status)) return false;
-      const bool first = split || X == 0 || kt >= nA;
-      const bool last = split || X == 1 || kt >= nB;
-      if (first && !mbar_wait(&v_full[st], (kt >> 1) & 1, p.status)) return false;
-      fence_async_smem();   // V arrived through the generic proxy (cp.async)
-      tc_fence_after();
-      if (lane == 0) {
+        return true;
+      };
+      auto pv = [&](int X, int t) -> bool {
+        const int kt = kt_of(X, t), st = kt % kStagesKV;
+        if (!mbar_wait(&p_full[X], t & 1, p.status)) return false;
+        const bool first = split || X == 0 || kt >= nA;
+        const bool last = split || X == 1 || kt >= nB;
+        if (first && !mbar_wait(&v_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+        fence_async_smem();   // V arrived through the generic proxy (cp.async)
+        tc_fence_after();
         const uint32_t tS = tmem + X * 128;
 #pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk) {
@@ -404,24 +405,27 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
         if (t == (X ? nt1 : nt0) - 1) mma_commit(smem_u32(&o_done[X]));
         if (last) mma_commit(smem_u32(&v_empty[st]));
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, p.status);
+      fence_async_smem();   // Q arrived through the generic proxy (cp.async)
+      if (ok) ok = qk(0, 0);
+      if (ok && nt1 > 0) ok = qk(1, 0);
+      for (int t = 0; t < max(nt0, nt1) && ok; ++t) {
+        if (t < nt0) {
+          ok = pv(0, t);
+          if (ok && t + 1 < nt0) ok = qk(0, t + 1);
+        }
+        if (ok && t < nt1) {
+          ok = pv(1, t);
+          if (ok && t + 1 < nt1) ok = qk(1, t + 1);
+        }
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, p.status));
-    fence_async_smem();   // Q arrived through the generic proxy (cp.async)
-    if (ok) ok = __all_sync(0xffffffffu, qk(0, 0));
-    if (ok && nt1 > 0) ok = __all_sync(0xffffffffu, qk(1, 0));
-    for (int t = 0; t < max(nt0, nt1) && ok; ++t) {
-      if (t < nt0) {
-        ok = __all_sync(0xffffffffu, pv(0, t));
-        if (ok && t + 1 < nt0) ok = __all_sync(0xffffffffu, qk(0, t + 1));
-      }
-      if (ok && t < nt1) {
-        ok = __all_sync(0xffffffffu, pv(1, t));
-        if (ok && t + 1 < nt1) ok = __all_sync(0xffffffffu, qk(1, t + 1));
-      }
+      // every MMA issued above completes before TMEM is freed, also when a wait gave up early
+      mma_commit(smem_u32(drain));
+      mbar_wait(drain, 0, p.status);
     }
+    __syncwarp();
   } else if (warp < kScatterWarp0) {
     // ------------------------------------------------------------ producers (K: warps 1-2, V: 3-4)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -469,14 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     int n0 = raw(0, 0), n1 = raw(0, 1);
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
-      const int st = j & 1;
+      const int st = j % kStagesKV;
       const __nv_bfloat16* p0 = rowptr(j, 0, n0);
       const __nv_bfloat16* p1 = rowptr(j, 1, n1);
       if (j + 1 < ntiles) {
         n0 = raw(j + 1, 0);
         n1 = raw(j + 1, 1);
       }
-      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j >> 1) - 1) & 1, p.status);
+      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j / kStagesKV) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const uint32_t dst = sbuf + st * kTileBytes;
@@ -584,12 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // weights, rounded to bf16, two per column in the first 64 score columns
       uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+      for (int h = 0; h < kN / 32; ++h) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
+        for (int u = 0; u < 16; ++u) {
           float x0, x1;
-          f2unpack(fma2(f2pack(v[64 * h + 2 * u], v[64 * h + 2 * u + 1]), sc2x2, negx2), x0, x1);
+          f2unpack(fma2(f2pack(v[32 * h + 2 * u], v[32 * h + 2 * u + 1]), sc2x2, negx2), x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
           pk[u] = pack_bf16(p0, p1);
           // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           rs2 = add2(rs2, f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
           re2 = add2(re2, f2pack(p0, p1));
         }
-        tmem_st32u(tS + 32 * h, pk);
+        tmem_st16u(tS + 16 * h, pk);
       }
       // rescale O: the last P.V of this tile completed before these scores did
       if (__any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0) {
