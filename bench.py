@@ -35,6 +35,70 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "source": "fallback"}
 
 
+# DRAM traffic per launch from one ncu capture (`--write-traffic`), tied to the kernel sources it
+# was taken on: a figure whose source file has changed since is reported as null
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_fork_mixed_step.json")
+TRAFFIC_SOURCES = {"extend": "prefix_cached_paged_gb300/csrc/extend_tc.cu",
+                   "decode": "prefix_cached_paged_gb300/csrc/decode.cu"}
+# kernels whose launches make up one call of each entry point
+TRAFFIC_KERNELS = {"extend": ("extend_tc_kernel",),
+                   "decode": ("decode_plan_kernel", "decode_mma_kernel", "decode_merge_kernel")}
+
+
+def source_hash(rel):
+    import hashlib
+    return hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest()
+
+
+def stored_traffic():
+    """{"extend": bytes per call or None, "decode": ...}; None where no capture matches the
+    current kernel source."""
+    out = {k: None for k in TRAFFIC_SOURCES}
+    if not os.path.exists(TRAFFIC_FILE):
+        return out
+    d = json.load(open(TRAFFIC_FILE))
+    for k, rel in TRAFFIC_SOURCES.items():
+        e = d.get(k)
+        if e and e.get("source_sha256") == source_hash(rel):
+            out[k] = e["dram_bytes_per_call"]
+    return out
+
+
+def write_traffic(csv_path, command):
+    """Summarise an ncu --csv capture of dram__bytes_read.sum and dram__bytes_write.sum into
+    TRAFFIC_FILE: per entry point, the mean DRAM bytes of each of its kernels, summed per call."""
+    import csv
+    import collections
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    h = rows[hi]
+    ids, ki, mi, ui, vi = (h.index(c) for c in ("ID", "Kernel Name", "Metric Name",
+                                                 "Metric Unit", "Metric Value"))
+    per_launch = collections.defaultdict(lambda: [None, 0.0])
+    for r in rows[hi + 1:]:
+        if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        e = per_launch[r[ids]]
+        e[0] = r[ki].split("(")[0].split("::")[-1].split("<")[0]
+        e[1] += float(r[vi].replace(",", "")) * scale[r[ui]]
+    by_kernel = collections.defaultdict(list)
+    for name, b in per_launch.values():
+        by_kernel[name].append(b)
+    out = {"command": command, "metrics": "dram__bytes_read.sum + dram__bytes_write.sum"}
+    for k, names in TRAFFIC_KERNELS.items():
+        if all(n in by_kernel for n in names):
+            out[k] = {"source_sha256": source_hash(TRAFFIC_SOURCES[k]),
+                      "dram_bytes_per_call": round(sum(float(np.mean(by_kernel[n]))
+                                                       for n in names)),
+                      "per_kernel": {n: {"launches": len(by_kernel[n]),
+                                         "mean_bytes": round(float(np.mean(by_kernel[n])))}
+                                     for n in names}}
+    os.makedirs(os.path.dirname(TRAFFIC_FILE), exist_ok=True)
+    json.dump(out, open(TRAFFIC_FILE, "w"), indent=1)
+    print(json.dumps(out))
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -52,8 +116,11 @@ def dist_init():
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:   # host-only runs (tests of the replica plumbing)
+            dist.init_process_group("gloo")
     return rank, world, local
 
 
@@ -68,7 +135,8 @@ def max_over_ranks(x, world):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -321,6 +389,7 @@ def bench_ours(args, rank, world, local):
                        "extend, D2H of its output; same for decode"}
 
     pk = peaks()
+    traffic = stored_traffic()
     dec_frac = dec_gbs / world / pk["hbm_gbs"]
     ext_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     # dominant kernel by time: decode (3 launches per call: plan, split-K main, merge)
@@ -332,13 +401,13 @@ def bench_ours(args, rank, world, local):
                 "achieved": round(per_launch_dec_bytes / (dec_call_ms * 1e-3) / 1e9, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(per_launch_dec_bytes / (dec_call_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-                "traffic": args.traffic_decode, "peak_source": pk["source"] + " hbm_gbs"}
+                "traffic": traffic["decode"], "peak_source": pk["source"] + " hbm_gbs"}
     per_launch_ext = ext_flops / (args.steps * m.layers)
     roof_ext = {"kernel": "extend_attention", "bound": "tensor",
                 "achieved": round(per_launch_ext / (ext_call_ms * 1e-3) / 1e12, 2),
                 "peak": ext_peak, "unit": "TFLOP/s",
                 "frac": round(per_launch_ext / (ext_call_ms * 1e-3) / 1e12 / ext_peak, 4),
-                "traffic": args.traffic_extend,
+                "traffic": traffic["extend"],
                 "peak_source": pk["source"] + " bf16_tflops_sustained"}
     cpu = cpu_baseline(ctx, args) if (rank == 0 and world == 1 and args.cpu_baseline) else None
     out = {
@@ -538,9 +607,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
-    ap.add_argument("--traffic-decode", type=float, default=None)
-    ap.add_argument("--traffic-extend", type=float, default=None)
+    ap.add_argument("--write-traffic", metavar="NCU_CSV", default=None,
+                    help="summarise an ncu capture of DRAM bytes into the traffic file and exit")
+    ap.add_argument("--traffic-command", default="",
+                    help="the command line the capture was taken with (recorded with it)")
     args = ap.parse_args()
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.traffic_command)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_init()
