@@ -224,7 +224,7 @@ typedef struct rc_decode_args {
   int32_t head_dim;
   int32_t max_reqs;          /* rows of req_to_token; every req_idx must be below it */
   int32_t max_ctx;           /* columns of req_to_token */
-  int32_t kv_chunk;          /* tokens per split, multiple of 64; 0 = library default */
+  int32_t kv_chunk;          /* tokens per split, multiple of 64; 0 = library default (512) */
   int64_t max_total_tokens;  /* >= sum of seq_len (host-known; sizes workspace and grid) */
   int64_t num_slots;
   float sm_scale;
@@ -239,6 +239,22 @@ typedef struct rc_decode_args {
   void* v_pool;
   void* o;
   float* lse;
+  /* Optional shared-context groups; num_groups = 0 computes every request on its own. Group g
+   * lists the requests group_members[group_indptr[g] .. group_indptr[g+1]), the first being the
+   * leader, whose req_to_token rows hold the same slots at positions [0, group_shared[g]) -- the
+   * KV of a prefix they share in the radix tree. The chunks wholly inside that range are read once
+   * for the whole group, the members' queries stacked next to each other (the shared-prefix
+   * stacking of the paper digest's related work, Sec. 7, applied to decode); every member still
+   * gets its own partial state per chunk, so the outputs are those of the per-request definition.
+   * Contract: each request is in at most one group; a group has at most 8 / (Hq / Hkv) members;
+   * group_shared[g] <= seq_len[m] - 1 for every member m. Breaking it is reported through the
+   * device status word (RC_ERR_DEVICE at the next check); slots that differ inside the shared
+   * range give the non-leading members the leader's KV there, never an out-of-range access.
+   * Stacking applies to bf16; the fp32 path ignores the groups. Device int32 arrays. */
+  int32_t num_groups;
+  const int32_t* group_indptr;   /* [num_groups + 1] */
+  const int32_t* group_members;  /* [group_indptr[num_groups]] request indices */
+  const int32_t* group_shared;   /* [num_groups] tokens of shared context */
 } rc_decode_args;
 /* Workspace bytes rc_decode_attention needs for these arguments (device memory, 256-B aligned,
  * no initialisation needed). */

@@ -216,9 +216,14 @@ def extend_attention(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, r
 
 
 def _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool, o,
-                 lse, sm_scale, max_total_tokens, kv_chunk):
+                 lse, sm_scale, max_total_tokens, kv_chunk, groups=None):
     B, Hq, d = q.shape
-    return RcDecodeArgs(
+    g = dict(num_groups=0, group_indptr=0, group_members=0, group_shared=0)
+    if groups is not None:
+        indptr, members, shared = groups
+        g = dict(num_groups=int(shared.numel()), group_indptr=indptr.data_ptr(),
+                 group_members=members.data_ptr(), group_shared=shared.data_ptr())
+    return RcDecodeArgs(**g,
         dtype=_dtype_code(q), num_reqs=B, num_q_heads=Hq, num_kv_heads=k_new.shape[1],
         head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], kv_chunk=int(kv_chunk),
         max_total_tokens=int(max_total_tokens), num_slots=k_pool.shape[0],
@@ -244,14 +249,58 @@ def decode_workspace_bytes(q, k_new, req_to_token, k_pool, *, max_total_tokens, 
 
 def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
                      o, workspace, *, sm_scale, max_total_tokens, kv_chunk=0, lse=None,
-                     stream=None):
+                     groups=None, stream=None):
     """Split-K decode attention of one layer (see rc_decode_attention). workspace: a uint8 CUDA
-    tensor of at least decode_workspace_bytes(...) bytes."""
+    tensor of at least decode_workspace_bytes(...) bytes. groups: optional shared-context groups
+    (indptr, members, shared), int32 CUDA tensors, as built by shared_context_groups()."""
     a = _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
-                     o, lse, sm_scale, max_total_tokens, kv_chunk)
+                     o, lse, sm_scale, max_total_tokens, kv_chunk, groups)
     check(lib().rc_decode_attention(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "rc_decode_attention")
+
+
+DEFAULT_KV_CHUNK = 512   # tokens per split-K chunk when kv_chunk = 0 (rc.h)
+
+
+def shared_context_groups(rows, lengths, group_size: int, min_shared: int):
+    """Host-side grouping for decode: requests whose slot rows start with the same slots share
+    that prefix's KV. rows: int32 [B, >= max(lengths)] slot rows, lengths: context tokens per
+    request. Greedy: the first request of each same-first-slot bucket leads; the others with the
+    longest common slot prefix join it, up to group_size members, as long as that prefix is at
+    least min_shared tokens; a group's shared length is its members' smallest common prefix.
+    Returns (indptr, members, shared) int32 numpy arrays (no groups: three empty arrays)."""
+    rows = np.asarray(rows)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    B = len(lengths)
+    indptr, members, shared = [0], [], []
+    if group_size < 2 or B < 2:
+        return (np.zeros(1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.int32))
+    eligible = np.flatnonzero(lengths >= max(min_shared, 1))
+    buckets = {}
+    for b in eligible:
+        buckets.setdefault(int(rows[b, 0]), []).append(int(b))
+
+    def lcp(x, y):
+        n = int(min(lengths[x], lengths[y]))
+        diff = np.flatnonzero(rows[x, :n] != rows[y, :n])
+        return int(diff[0]) if diff.size else n
+
+    for rest in buckets.values():
+        while len(rest) >= 2:
+            lead = rest[0]
+            cand = sorted(((lcp(lead, m), m) for m in rest[1:]), reverse=True)
+            take = [(l, m) for l, m in cand[:group_size - 1] if l >= min_shared]
+            if not take:
+                rest = rest[1:]
+                continue
+            members += [lead] + [m for _, m in take]
+            shared.append(min(l for l, _ in take))
+            indptr.append(len(members))
+            used = {lead} | {m for _, m in take}
+            rest = [m for m in rest if m not in used]
+    return (np.asarray(indptr, np.int32), np.asarray(members, np.int32),
+            np.asarray(shared, np.int32))
 
 
 STATIC_SCRATCH_BYTES = 32 << 20

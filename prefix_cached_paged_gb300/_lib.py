@@ -79,7 +79,9 @@ class RcDecodeArgs(ctypes.Structure):
                 ("max_ctx", _I32), ("kv_chunk", _I32), ("max_total_tokens", _I64), ("num_slots", _I64),
                 ("sm_scale", ctypes.c_float), ("q", _P), ("k_new", _P), ("v_new", _P),
                 ("out_loc", _P), ("seq_len", _P), ("req_idx", _P), ("req_to_token", _P),
-                ("k_pool", _P), ("v_pool", _P), ("o", _P), ("lse", _P)]
+                ("k_pool", _P), ("v_pool", _P), ("o", _P), ("lse", _P),
+                ("num_groups", _I32), ("group_indptr", _P), ("group_members", _P),
+                ("group_shared", _P)]
 
 
 _lib = None

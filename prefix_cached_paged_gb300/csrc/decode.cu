@@ -31,10 +31,11 @@ constexpr int kDefaultChunk = 512;
 
 struct Workspace {
   int* njobs;     // [0]: jobs written, [1]: item counter
-  int* jbase;     // [B+1]
-  int2* jobs;     // [max_jobs] (request, chunk)
-  float* plse;    // [max_items * G]
-  float* po;      // [max_items * G * D]
+  int* pbase;     // [B+1]: request b's partial states are slots pbase[b] + chunk
+  int* group_of;  // [B]: shared-context group of each request, -1 for none
+  int4* jobs;     // [max_jobs] (request, chunk, group of a stacked chunk or -1, 0)
+  float* plse;    // [max_jobs * Hkv * G]
+  float* po;      // [max_jobs * Hkv * G * D]
   int64_t max_jobs;
 };
 
@@ -46,10 +47,12 @@ Workspace carve(void* base, int B, int G, int D, int64_t max_jobs, int Hkv, size
   size_t off = 0;
   w.njobs = (int*)(p + off);
   off += align256(2 * sizeof(int));
-  w.jbase = (int*)(p + off);
+  w.pbase = (int*)(p + off);
   off += align256((size_t)(B + 1) * sizeof(int));
-  w.jobs = (int2*)(p + off);
-  off += align256((size_t)max_jobs * sizeof(int2));
+  w.group_of = (int*)(p + off);
+  off += align256((size_t)B * sizeof(int));
+  w.jobs = (int4*)(p + off);
+  off += align256((size_t)max_jobs * sizeof(int4));
   const int64_t max_items = max_jobs * Hkv;
   w.plse = (float*)(p + off);
   off += align256((size_t)max_items * G * sizeof(float));
@@ -64,20 +67,68 @@ struct Params {
   rc_decode_args a;
   Workspace w;
   int chunk;
+  int use_groups;    // stack the shared chunks of the argument's groups (bf16)
+  int max_members;   // 8 / G: query columns of one MMA tile
   int* status;
 };
 
 // ---------------------------------------------------------------- plan
+// Exclusive scan of one int per thread over the block; returns this thread's prefix and adds the
+// block total to *running (all threads see the same value afterwards).
+__device__ int block_excl_scan(int x, int* warp_sums, int* running) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int v = x;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int t = lane < nw ? warp_sums[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_sums[lane] = t;  // inclusive
+  }
+  __syncthreads();
+  const int excl = *running + (wid ? warp_sums[wid - 1] : 0) + v - x;
+  __syncthreads();
+  if (threadIdx.x == 0) *running += warp_sums[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+// One CTA. Every request gets ceil(L / chunk) partial-state slots (pbase); the job list holds
+// its chunks, except that a group's chunks wholly inside the shared context appear once, as the
+// leader's stacked jobs.
 __global__ void decode_plan_kernel(Params p) {
   __shared__ int warp_sums[32];
-  __shared__ int running_s;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  __shared__ int run_p, run_j;
+  const int tid = threadIdx.x;
   const int B = p.a.num_reqs;
-  if (tid == 0) running_s = 0;
+  if (tid == 0) run_p = run_j = 0;
+  for (int b = tid; b < B; b += blockDim.x) p.w.group_of[b] = -1;
+  __syncthreads();
+  if (p.use_groups) {
+    for (int g = tid; g < p.a.num_groups; g += blockDim.x) {
+      const int m0 = p.a.group_indptr[g], m1 = p.a.group_indptr[g + 1];
+      if (m0 < 0 || m1 < m0 || m1 - m0 > p.max_members) {
+        set_status(p.status, kStatusPosRange);
+        continue;
+      }
+      for (int i = m0; i < m1; ++i) {
+        const int b = p.a.group_members[i];
+        if (b < 0 || b >= B || atomicCAS(&p.w.group_of[b], -1, g) != -1)
+          set_status(p.status, kStatusPosRange);   // out of range, or in two groups
+      }
+    }
+  }
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + tid;
-    int n = 0;
+    int n = 0, first = 0, nj = 0, g = -1, sc = 0;
     if (b < B) {
       const int L = p.a.seq_len[b];
       const int row = p.a.req_idx[b];
@@ -85,42 +136,33 @@ __global__ void decode_plan_kernel(Params p) {
         set_status(p.status, kStatusPosRange);
       } else {
         n = (L + p.chunk - 1) / p.chunk;
+        g = p.w.group_of[b];
+        if (g >= 0) {
+          const int sh = p.a.group_shared[g];
+          if (sh < 0 || sh > L - 1) set_status(p.status, kStatusPosRange);
+          sc = min(max(sh, 0), L - 1) / p.chunk;   // stacked chunks: wholly inside [0, sh)
+          // the leader runs the stacked chunks for the whole group, the others skip them
+          if (p.a.group_members[p.a.group_indptr[g]] != b) first = sc;
+        }
+        nj = n - first;
       }
     }
-    // block exclusive scan of n
-    int x = n;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-      int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
-      }
-      warp_sums[lane] = s;  // inclusive
-    }
-    __syncthreads();
-    const int excl = running_s + (wid ? warp_sums[wid - 1] : 0) + x - n;
+    const int pb = block_excl_scan(n, warp_sums, &run_p);
+    const int jb = block_excl_scan(nj, warp_sums, &run_j);
     if (b < B) {
-      p.w.jbase[b] = excl;
-      for (int c = 0; c < n; ++c) {
-        if (excl + c < p.w.max_jobs)
-          p.w.jobs[excl + c] = make_int2(b, c);
+      p.w.pbase[b] = pb;
+      for (int k = 0; k < nj; ++k) {
+        const int c = first + k;
+        if (jb + k < p.w.max_jobs && pb + n <= p.w.max_jobs)
+          p.w.jobs[jb + k] = make_int4(b, c, (g >= 0 && c < sc) ? g : -1, 0);
         else
           set_status(p.status, kStatusPosRange);
       }
     }
-    __syncthreads();
-    if (tid == 0) running_s += warp_sums[(blockDim.x >> 5) - 1];
-    __syncthreads();
   }
   if (tid == 0) {
-    p.w.jbase[B] = running_s;
-    p.w.njobs[0] = (int)min((int64_t)running_s, p.w.max_jobs);
+    p.w.pbase[B] = run_p;
+    p.w.njobs[0] = (int)min((int64_t)run_j, p.w.max_jobs);
     p.w.njobs[1] = 0;
   }
 }
@@ -218,8 +260,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_main_kernel(Params p) {
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item >= n_items) break;
     const int job = item / Hkv, h = item - job * Hkv;
-    const int2 bc = p.w.jobs[job];
+    const int4 bc = p.w.jobs[job];
     const int b = bc.x, c = bc.y;
+    const int64_t pslot = (int64_t)p.w.pbase[b] + c;   // partial-state slot of (b, c)
     const int L = a.seq_len[b];
     const int row = a.req_idx[b];
     const int t0 = c * p.chunk;
@@ -389,7 +432,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_main_kernel(Params p) {
         for (int k = 0; k < C::DPL; ++k) o[k] = Elem<T>::from_f(acc[g][k] * inv);
         if (a.lse && lane == 0) a.lse[(int64_t)b * Hq + hq] = lse2 * kLn2;
       } else {
-        const int64_t pi = (int64_t)item * G + g;
+        const int64_t pi = (pslot * Hkv + h) * G + g;
         float* po = p.w.po + pi * D + lane * C::DPL;
 #pragma unroll
         for (int k = 0; k < C::DPL; ++k) po[k] = acc[g][k] * inv;
@@ -499,8 +542,20 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item >= n_items) break;
     const int job = item / Hkv, h = item - job * Hkv;
-    const int2 bc = p.w.jobs[job];
+    const int4 bc = p.w.jobs[job];
     const int b = bc.x, c = bc.y;
+    const int64_t pslot = (int64_t)p.w.pbase[b] + c;   // partial-state slot of (b, c)
+    // a stacked chunk of a shared-context group: the leader's rows serve every member; query
+    // column n of the MMA tile is member n / G, head n % G
+    const int grp = bc.z;
+    int nm = 1;
+    const int32_t* mem = nullptr;
+    if (grp >= 0) {
+      const int m0 = a.group_indptr[grp];
+      nm = min(a.group_indptr[grp + 1] - m0, 8 / G);
+      mem = a.group_members + m0;
+    }
+    const int ncols = grp >= 0 ? nm * G : G;
     const int L = a.seq_len[b];
     const int row = a.req_idx[b];
     const int t0 = c * p.chunk;
@@ -552,14 +607,23 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
       issue(s, next_slot);
       next_slot = slot_of(s + 1);
     }
-    // Q^T fragments: column n = gid is query head h*G + gid (zero for gid >= G)
+    // Q^T fragments: column n = gid is query head h*G + gid of request b (zero for gid >= G),
+    // or, for a stacked chunk, head h*G + gid % G of member gid / G
     uint32_t qb[C::KSTEPS][2];
     {
-      const __nv_bfloat16* qg = (const __nv_bfloat16*)a.q + ((int64_t)b * Hq + h * G + gid) * D;
+      int qb_req = b, qh = gid;
+      bool qv = gid < ncols;
+      if (grp >= 0 && qv) {
+        qb_req = mem[gid / G];
+        qh = gid % G;
+        qv = qb_req >= 0 && qb_req < a.num_reqs;
+      }
+      const __nv_bfloat16* qg =
+          (const __nv_bfloat16*)a.q + ((int64_t)(qv ? qb_req : 0) * Hq + h * G + (qv ? qh : 0)) * D;
 #pragma unroll
       for (int kk = 0; kk < C::KSTEPS; ++kk) {
-        qb[kk][0] = gid < G ? *(const uint32_t*)(qg + kk * 16 + tig * 2) : 0u;
-        qb[kk][1] = gid < G ? *(const uint32_t*)(qg + kk * 16 + tig * 2 + 8) : 0u;
+        qb[kk][0] = qv ? *(const uint32_t*)(qg + kk * 16 + tig * 2) : 0u;
+        qb[kk][1] = qv ? *(const uint32_t*)(qg + kk * 16 + tig * 2 + 8) : 0u;
       }
     }
     float acc[C::KSTEPS][4];
@@ -652,7 +716,36 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
     const float iA = l0 > 0.f ? 1.f / l0 : 0.f, iB = l1 > 0.f ? 1.f / l1 : 0.f;
     const float lseA = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
     const float lseB = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
-    if (nchunks == 1) {
+    if (grp >= 0) {
+      // stacked chunk: column n's partial state goes to member n / G's slot for this chunk
+      int64_t piA = -1, piB = -1;
+      auto pidx = [&](int col) -> int64_t {
+        if (col >= ncols) return -1;
+        const int bm = mem[col / G];
+        if (bm < 0 || bm >= a.num_reqs) return -1;
+        const int64_t ps = (int64_t)p.w.pbase[bm] + c;
+        if (ps >= p.w.max_jobs) return -1;
+        return (ps * Hkv + h) * G + col % G;
+      };
+      piA = pidx(hA);
+      piB = pidx(hB);
+#pragma unroll
+      for (int i = 0; i < C::KSTEPS; ++i) {
+        const int d0 = i * 16 + gid;
+        if (piA >= 0) {
+          p.w.po[piA * D + d0] = acc[i][0] * iA;
+          p.w.po[piA * D + d0 + 8] = acc[i][2] * iA;
+        }
+        if (piB >= 0) {
+          p.w.po[piB * D + d0] = acc[i][1] * iB;
+          p.w.po[piB * D + d0 + 8] = acc[i][3] * iB;
+        }
+      }
+      if (gid == 0) {
+        if (piA >= 0) p.w.plse[piA] = lseA;
+        if (piB >= 0) p.w.plse[piB] = lseB;
+      }
+    } else if (nchunks == 1) {
       __nv_bfloat16* o = (__nv_bfloat16*)a.o + ((int64_t)b * Hq + h * G) * D;
 #pragma unroll
       for (int i = 0; i < C::KSTEPS; ++i) {
@@ -671,7 +764,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
         if (hB < G) a.lse[(int64_t)b * Hq + h * G + hB] = lseB * kLn2;
       }
     } else {
-      const int64_t pi = (int64_t)item * G;
+      const int64_t pi = (pslot * Hkv + h) * G;
 #pragma unroll
       for (int i = 0; i < C::KSTEPS; ++i) {
         const int d0 = i * 16 + gid;
@@ -690,7 +783,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
       }
     }
     // ---- the last chunk scatters the new token's K and V rows into the pool
-    if (c == nchunks - 1) {
+    if (grp < 0 && c == nchunks - 1) {
       const int sl = a.out_loc[b];
       if (sl < 0 || (int64_t)sl >= a.num_slots) {
         if (lane == 0) set_status(p.status, kStatusSlotRange);
@@ -719,7 +812,7 @@ __global__ void decode_merge_kernel(Params p) {
   if (nchunks == 1) return;
   const int Hkv = a.num_kv_heads;
   const int h = hq / G, g = hq - h * G;
-  const int j0 = p.w.jbase[b];
+  const int j0 = p.w.pbase[b];
   if ((int64_t)j0 + nchunks > p.w.max_jobs) return;
   float M = -INFINITY;
   for (int c = 0; c < nchunks; ++c) M = fmaxf(M, p.w.plse[((int64_t)(j0 + c) * Hkv + h) * G + g]);
@@ -759,6 +852,10 @@ int validate(const rc_decode_args* a) {
                "rc_decode_attention: bad sizes");
   RC_CHECK_ARG(a->kv_chunk == 0 || (a->kv_chunk > 0 && a->kv_chunk % 64 == 0),
                "rc_decode_attention: kv_chunk %d", a->kv_chunk);
+  RC_CHECK_ARG(a->num_groups >= 0, "rc_decode_attention: num_groups %d", a->num_groups);
+  RC_CHECK_ARG(a->num_groups == 0 ||
+                   (a->group_indptr && a->group_members && a->group_shared),
+               "rc_decode_attention: group arrays are NULL");
   return RC_OK;
 }
 
@@ -845,6 +942,8 @@ extern "C" int rc_decode_attention(const rc_decode_args* a, void* workspace,
   rc::Params p{};
   p.a = *a;
   p.chunk = chunk;
+  p.use_groups = (a->dtype == RC_DTYPE_BF16 && a->num_groups > 0) ? 1 : 0;
+  p.max_members = 8 / G;
   p.w = rc::carve(workspace, a->num_reqs, G, a->head_dim, rc::max_jobs_for(a, chunk),
                   a->num_kv_heads, &need);
   RC_CHECK_ARG(workspace_bytes >= need, "rc_decode_attention: workspace %zu bytes < %zu needed",

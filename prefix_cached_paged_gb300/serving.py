@@ -21,7 +21,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import decode_attention, decode_workspace_bytes, extend_attention
+from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
+               shared_context_groups)
 from .runtime import DeviceKV, HostCache, Plan
 
 
@@ -50,11 +51,13 @@ class DecodeBatch:
     dev_seq_len: object = None
     dev_req_idx: object = None
     dev_out_loc: object = None
+    groups: object = None   # device (indptr, members, shared) of shared-context groups, or None
+    num_groups: int = 0
 
 
 class Engine:
     def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
-                 max_ctx, initial_order=None, device="cuda", kv_chunk=0):
+                 max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True):
         self.layers = layers
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
         self.sm_scale = 1.0 / float(np.sqrt(head_dim))
@@ -63,6 +66,8 @@ class Engine:
                             device)
         self.max_ctx = max_ctx
         self.kv_chunk = kv_chunk
+        # decode reads a context prefix that several requests share once for all of them
+        self.share_decode = share_decode
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
 
@@ -111,8 +116,18 @@ class Engine:
         row_ids = self._take_rows(len(contexts))
         self.dev.write_rows(row_ids, plan.rows, plan.lengths)
         self._decode_plan = plan
-        return DecodeBatch(row_ids, plan.nodes, plan.lengths.astype(np.int32),
-                           np.zeros(len(contexts), np.int32))
+        batch = DecodeBatch(row_ids, plan.nodes, plan.lengths.astype(np.int32),
+                            np.zeros(len(contexts), np.int32))
+        if self.share_decode:
+            # the contexts' slots never change while they decode (new tokens get new slots), so
+            # the groups hold for the whole batch
+            G = self.n_q_heads // self.n_kv_heads
+            indptr, members, shared = shared_context_groups(
+                plan.rows, plan.lengths, 8 // G, self.kv_chunk or DEFAULT_KV_CHUNK)
+            if len(shared):
+                batch.groups = tuple(self.dev.upload_i32([indptr, members, shared]))
+                batch.num_groups = len(shared)
+        return batch
 
     def decode_step(self, batch: DecodeBatch, new_slots=None) -> DecodeBatch:
         """Append one token per request: allocate its slot (evicting if needed) unless given,
@@ -145,7 +160,7 @@ class Engine:
         decode_attention(q, k_new, v_new, batch.dev_out_loc, batch.dev_seq_len,
                          batch.dev_req_idx, self.dev.req_to_token, self.dev.k[layer],
                          self.dev.v[layer], o, ws, sm_scale=self.sm_scale, max_total_tokens=mt,
-                         kv_chunk=self.kv_chunk, lse=lse)
+                         kv_chunk=self.kv_chunk, lse=lse, groups=batch.groups)
 
     def decode_end(self, batch: DecodeBatch):
         for n in batch.nodes:

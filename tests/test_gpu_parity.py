@@ -257,3 +257,77 @@ def test_multi_turn_decode_unshared_twin_sampled():
     rng = np.random.default_rng(3)
     _check_decode(w, db, outs, seqs, _sample_units(rng, 256, 1, 8, 24))
     _status_clear()
+
+
+# ---------------------------------------------------------------- decode over shared contexts
+def _families(seed, spec):
+    """Requests in families: family f has a shared prefix of spec[f][0] tokens and one member per
+    entry of spec[f][1], whose own tokens follow (the decode token is the last one)."""
+    seqs = []
+    for f, (ls, owns) in enumerate(spec):
+        shared = synth.tokens(seed, 500 + f, ls)
+        for i, lo in enumerate(owns):
+            own = synth.tokens(seed, 900 + 37 * f + i, lo)
+            seqs.append(np.concatenate([shared, own]).astype(np.int32))
+    return seqs
+
+
+_FAMILY_SPEC = [(700, [1, 5, 300]), (1300, [2, 2, 2, 2, 2, 2, 2, 2, 9]), (64, [3, 40]),
+                (2100, [1, 700]), (40, [30]), (1030, [1])]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,chunk,dtype", [(8, 8, 128, 0, "bf16"), (8, 8, 128, 64, "bf16"),
+                                                  (16, 8, 64, 256, "bf16"),
+                                                  (16, 4, 128, 192, "bf16"),
+                                                  (16, 2, 128, 0, "bf16"), (4, 4, 128, 64, "f32")])
+def test_decode_shared_context_groups(Hq, Hkv, d, chunk, dtype):
+    """Groups of requests over a shared prefix: the stacked kernel matches the oracle, and it is
+    bit-identical to decoding every request on its own (stacking changes no arithmetic)."""
+    import torch
+    m = W.Model(1, Hq, Hkv, d, dtype, 8)
+    seqs = _families(8, _FAMILY_SPEC)
+    w = W.Workload("dec_shared", m, 20_000, synth.permutation(8, 20_000), max_ctx=2816)
+    runs = {}
+    for share in (True, False):
+        eng = H.make_engine(w, max_reqs=32, kv_chunk=chunk, share_decode=share)
+        H.run_cache_phase(eng, m, [s[:-1] for s in seqs])
+        db, o = H.run_decode(eng, m, seqs, lse=True)
+        runs[share] = (eng, db, o)
+        _status_clear()
+    eng, db, o = runs[True]
+    # groups form wherever a KV head's query heads leave room for two requests in a tile
+    assert (db.num_groups > 0) == (8 // (Hq // Hkv) >= 2)
+    _check_decode(w, db, o, seqs, [(i, 0, h) for i in range(len(seqs)) for h in range(Hkv)])
+    _decode_scatter(eng, w, seqs, db)
+    (og, lg), (ou, lu) = o[0], runs[False][2][0]
+    assert torch.equal(og, ou) and torch.equal(lg, lu)
+
+
+def test_decode_group_contract_breaches_are_reported():
+    """A request in two groups, or a shared length past a member's context, is reported through
+    the device status word; every access stays in range."""
+    import prefix_cached_paged_gb300 as rc
+    m = W.Model(1, 8, 8, 128, "bf16", 9)
+    seqs = _families(9, [(600, [3, 4, 5])])
+    w = W.Workload("dec_breach", m, 4000, None, max_ctx=640)
+    eng = H.make_engine(w, max_reqs=8, kv_chunk=64, share_decode=False)
+    H.run_cache_phase(eng, m, [s[:-1] for s in seqs])
+    db, _ = H.run_decode(eng, m, seqs)
+    _status_clear()
+    from synth import device as sdev
+    import torch
+    h = np.array([synth.prefix_hashes(m.seed, s)[-1] for s in seqs], dtype=np.uint64)
+    q, k, v = H.dense_qkv(m, sdev.hashes_to_device(h), 0, len(seqs))
+    o = torch.empty_like(q)
+    mt = int(db.seq_len.sum())
+    ws = eng.workspace(q, k, mt)
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    bad = [((dev([0, 2, 4]), dev([0, 1, 1, 2]), dev([512, 512]))),     # request 1 twice
+           ((dev([0, 3]), dev([0, 1, 2]), dev([int(db.seq_len.max())])))]  # shared past a context
+    for groups in bad:
+        rc.decode_attention(q, k, v, db.dev_out_loc, db.dev_seq_len, db.dev_req_idx,
+                            eng.dev.req_to_token, eng.dev.k[0], eng.dev.v[0], o, ws,
+                            sm_scale=eng.sm_scale, max_total_tokens=mt, kv_chunk=64,
+                            groups=groups)
+        torch.cuda.synchronize()
+        assert rc.device_status() != 0

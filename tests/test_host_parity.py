@@ -174,3 +174,59 @@ def test_fork_mixed_steps_host_match_oracle():
         pc.finish(pp)
         oc.extend_finish(ext, op)
         np.testing.assert_array_equal(oc.tree.dump(), pc.tree.dump())
+
+
+# ---------------------------------------------------------------- decode grouping (host)
+def _lcp(a, b, n):
+    d = np.flatnonzero(a[:n] != b[:n])
+    return int(d[0]) if d.size else n
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_shared_context_groups_are_valid(seed):
+    """Every group: disjoint members, 2..cap of them, rows identical over the shared length, the
+    shared length is the smallest common prefix with the leader and at least min_shared, and
+    no longer than any member's context."""
+    from prefix_cached_paged_gb300 import shared_context_groups
+    rng = np.random.default_rng(seed)
+    B, W_ = 40, 300
+    rows = rng.integers(0, 10_000, (B, W_)).astype(np.int32)
+    lengths = rng.integers(1, W_ + 1, B)
+    # families: copy a leader's prefix of random length into some requests
+    for b in range(B):
+        if rng.random() < 0.7:
+            src = int(rng.integers(0, B))
+            n = int(rng.integers(0, W_))
+            rows[b, :n] = rows[src, :n]
+    cap = int(rng.choice([2, 4, 8]))
+    min_shared = int(rng.choice([1, 16, 64]))
+    indptr, members, shared = shared_context_groups(rows, lengths, cap, min_shared)
+    assert indptr[0] == 0 and len(indptr) == len(shared) + 1
+    assert len(set(members.tolist())) == len(members)            # each request at most once
+    for g in range(len(shared)):
+        mem = members[indptr[g]:indptr[g + 1]]
+        assert 2 <= len(mem) <= cap
+        sh = int(shared[g])
+        assert sh >= min_shared
+        lead = mem[0]
+        assert sh == min(_lcp(rows[lead], rows[x], int(min(lengths[lead], lengths[x])))
+                         for x in mem[1:])
+        for x in mem:
+            assert sh <= lengths[x]
+            np.testing.assert_array_equal(rows[x, :sh], rows[lead, :sh])
+
+
+def test_shared_context_groups_find_families():
+    """Four families of three requests over long shared prefixes and four loners: each family
+    becomes one group whose shared length is its prefix."""
+    from prefix_cached_paged_gb300 import shared_context_groups
+    rng = np.random.default_rng(7)
+    rows = rng.integers(0, 1 << 30, (16, 900)).astype(np.int32)
+    lengths = np.full(16, 900)
+    for f in range(4):
+        for i in (1, 2):
+            rows[3 * f + i, :500 + 100 * f] = rows[3 * f, :500 + 100 * f]
+    indptr, members, shared = shared_context_groups(rows, lengths, 8, 64)
+    got = sorted((tuple(sorted(members[indptr[g]:indptr[g + 1]].tolist())), int(shared[g]))
+                 for g in range(len(shared)))
+    assert got == [((0, 1, 2), 500), ((3, 4, 5), 600), ((6, 7, 8), 700), ((9, 10, 11), 800)]
