@@ -478,6 +478,12 @@ struct MmaCfg {
   static_assert(kTok == 16, "one m16 tile of tokens per stage");
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -518,7 +524,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
   char* ring = smem + wid * C::WARP_BYTES;
   uint64_t* bars = (uint64_t*)(ring + C::RING);
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 32);   // one copy-arrival per lane
     fence_mbar_init();
   }
   __syncwarp();
@@ -575,6 +581,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
       if (pos >= t1 || pos == L - 1) return -2;
       return rt[pos];
     };
+    // Stage s: the warp copies the 16 tokens' K and V rows with 16-byte cp.async (lane l moves
+    // chunk l % CPR of rows l / CPR, l / CPR + RPI, ...), each row pointer taken by a shuffle
+    // from the lane that loaded that token's slot; completion is one arrival per lane.
     auto issue = [&](int s, int sl) {
       if (sl >= 0 && (int64_t)sl >= a.num_slots) {
         set_status(p.status, kStatusSlotRange);
@@ -584,21 +593,27 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
         sl = 0;
       }
       const int buf = s % kStages;
-      char* kd = ring + buf * C::STAGE + lane * C::RS;
-      char* vd = ring + buf * C::STAGE + kTok * C::RS + lane * C::RS;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[buf], kTok * 2u * C::RB);
-      __syncwarp();
-      if (lane < kTok) {
-        const __nv_bfloat16* ks = knew;
-        const __nv_bfloat16* vs = vnew;
-        if (sl >= 0) {
-          const int64_t r = ((int64_t)sl * Hkv + h) * D;
-          ks = kpool + r;
-          vs = vpool + r;
-        }
-        bulk_g2s(kd, ks, C::RB, &bars[buf]);
-        bulk_g2s(vd, vs, C::RB, &bars[buf]);
+      const __nv_bfloat16* ks = knew;
+      const __nv_bfloat16* vs = vnew;
+      if (sl >= 0) {
+        const int64_t r = ((int64_t)sl * Hkv + h) * D;
+        ks = kpool + r;
+        vs = vpool + r;
       }
+      constexpr int CPR = C::RB / 16;   // 16-byte chunks per row
+      constexpr int RPI = 32 / CPR;     // rows per copy instruction
+      const int cc = lane % CPR, rsub = lane / CPR;
+      const uint32_t kd = ring_s + buf * C::STAGE + cc * 16;
+      const uint32_t vd = kd + kTok * C::RS;
+#pragma unroll
+      for (int i = 0; i < kTok / RPI; ++i) {
+        const int t = i * RPI + rsub;
+        const char* kp = (const char*)__shfl_sync(0xffffffffu, (uint64_t)ks, t);
+        const char* vp = (const char*)__shfl_sync(0xffffffffu, (uint64_t)vs, t);
+        cp_async16(kd + t * C::RS, kp + cc * 16);
+        cp_async16(vd + t * C::RS, vp + cc * 16);
+      }
+      cp_async_arrive_noinc(smem_u32(&bars[buf]));
     };
 
     int next_slot = slot_of(0);
@@ -702,8 +717,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
       __syncwarp();
     }
     if (!ok) {
-      for (int s = 0; s < kStages; ++s)
-        mbar_wait(&bars[s], (phases >> s) & 1u, p.status, 100000000ull);
+      asm volatile("cp.async.wait_all;" ::: "memory");   // no copy lands after the exit
       return;
     }
     // ---- epilogue: full denominators per head, then O^T columns -> output rows
