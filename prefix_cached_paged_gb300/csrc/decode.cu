@@ -2,19 +2,24 @@
 // token attends to the KV of all previous tokens; paper digest App. A.1 decoding).
 //
 // Design (HBM-bound: every context token's K and V row is read once per KV head):
-//   * plan kernel (1 CTA): cuts each request's context into chunks of kv_chunk tokens and writes
-//     the job list (request, chunk) with per-request offsets into the workspace;
+//   * plan kernel (1 CTA): cuts each request's context into chunks of kv_chunk tokens, gives
+//     every (request, chunk) a partial-state slot and writes the job list; the chunks of a
+//     shared-context group that lie wholly inside its shared prefix are listed once, as the
+//     leader's stacked jobs (see rc_decode_args);
 //   * main kernel (persistent, #SMs x occupancy CTAs of 4 warps): every warp is an independent
 //     worker that takes (job, KV head) items from an atomic counter. For an item it streams the
 //     chunk's K and V rows (one contiguous row of head_dim elements per token) from the pool into
-//     a private 3-stage shared-memory ring with cp.async.bulk on mbarriers, the slot indices
-//     prefetched one stage ahead. All G = Hq/Hkv query heads of the KV head are computed from
-//     each row, so the KV is read once. Scores: lanes (token, half of head_dim) with a one-step
-//     shuffle; online softmax in base 2 (scale * log2 e folded into q); P.V: each lane owns
-//     head_dim/32 output columns of every query head. The new token's K/V come from k_new/v_new
-//     (and are scattered to the pool by the last chunk's item), so no read races the scatter;
+//     a private 2-stage shared-memory ring of 16-token stages, the slot indices prefetched one
+//     stage ahead. bf16 (decode_mma_kernel): 16-byte cp.async from all lanes, mma.sync m16n8k16
+//     with the tokens as M and the query columns (G heads, or G heads of each stacked group
+//     member) as N. fp32 (decode_main_kernel): cp.async.bulk rows, scores by lanes (token, half
+//     of head_dim) with a one-step shuffle, P.V with each lane owning head_dim/32 output
+//     columns of every query head. Online softmax in base 2 (scale * log2 e folded in). The new
+//     token's K/V come from k_new/v_new (and are scattered to the pool by the last chunk's
+//     item), so no read races the scatter;
 //   * a request with one chunk writes its output directly; otherwise each chunk writes
-//     (O normalised, log2-sum-exp) to the workspace and the merge kernel combines them.
+//     (O normalised, log2-sum-exp) to its slot in the workspace and the merge kernel combines
+//     them.
 #include <algorithm>
 #include <mutex>
 
@@ -25,7 +30,7 @@ namespace rc {
 namespace {
 
 constexpr int kTok = 16;     // tokens per stage
-constexpr int kStages = 3;   // ring depth per warp
+constexpr int kStages = 2;   // ring depth per warp (two: 3 CTAs of 4 warps fit an SM)
 constexpr int kWarps = 4;    // warps per CTA
 constexpr int kDefaultChunk = 512;
 
