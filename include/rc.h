@@ -204,7 +204,27 @@ typedef struct rc_extend_args {
   void* v_pool;
   void* o;
   float* lse;
+  /* Optional prefix stacking (the shared-prefix query stacking of the paper digest's related
+   * work, Sec. 7; num_groups = 0 disables it). Group g is the run of consecutive requests
+   * [group_range[2g], group_range[2g+1]) whose req_to_token rows hold the same slots at
+   * positions [0, group_shared[g]), a prefix they all matched. A first pass attends the
+   * members' new-token queries, stacked, to those keys -- each K/V tile gathered once for the
+   * whole group -- and keeps every row's partial result (normalised O in o, its log-sum-exp in
+   * the workspace); the per-request pass then covers the keys from group_shared[g] on and
+   * merges the two with log-sum-exp weights. Outputs are those of the definition above.
+   * Contract: ranges ascending and disjoint; group_shared[g] >= 1 and <= prefix_len[b] of
+   * every member; max_group_rows >= the new tokens of every group. Breaches are reported
+   * through the device status word and never leave the given buffers. bf16 only (the fp32 path
+   * ignores the groups). Device int32 arrays; workspace >= rc_extend_workspace_bytes bytes,
+   * 16-byte aligned, used only when num_groups > 0. */
+  int32_t num_groups;
+  int32_t max_group_rows;
+  const int32_t* group_range;   /* [2 * num_groups] */
+  const int32_t* group_shared;  /* [num_groups] */
+  void* workspace;
+  size_t workspace_bytes;
 } rc_extend_args;
+int rc_extend_workspace_bytes(const rc_extend_args* args, size_t* out_bytes);
 int rc_extend_attention(const rc_extend_args* args, void* stream);
 
 /* Decode attention (paper digest App. A.1; RadixAttention explainer: each generated token

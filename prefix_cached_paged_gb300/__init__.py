@@ -191,10 +191,19 @@ def slot_table_write(req_to_token, seg_row, seg_col, seg_indptr, values, stream=
 
 
 def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
-                 k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len):
+                 k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len, stack=None,
+                 workspace=None):
     T, Hq, d = q.shape
     Hkv = k_new.shape[1]
-    return RcExtendArgs(
+    g = {}
+    if stack is not None:
+        ranges, shared, max_rows = stack
+        g = dict(num_groups=int(shared.numel()), max_group_rows=int(max_rows),
+                 group_range=ranges.data_ptr(), group_shared=shared.data_ptr(),
+                 workspace=0 if workspace is None else workspace.data_ptr(),
+                 workspace_bytes=0 if workspace is None else
+                 workspace.numel() * workspace.element_size())
+    return RcExtendArgs(**g,
         dtype=_dtype_code(q), num_reqs=prefix_len.numel(), num_q_heads=Hq, num_kv_heads=Hkv,
         head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
         max_prefix_len=int(max_prefix_len), num_tokens=T, num_slots=k_pool.shape[0],
@@ -205,13 +214,25 @@ def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_t
         v_pool=v_pool.data_ptr(), o=o.data_ptr(), lse=0 if lse is None else lse.data_ptr())
 
 
+def extend_workspace_bytes(num_tokens: int, num_q_heads: int) -> int:
+    """Workspace of the stacked prefix pass (rc_extend_workspace_bytes)."""
+    a = RcExtendArgs(num_tokens=int(num_tokens), num_q_heads=int(num_q_heads))
+    n = ctypes.c_size_t()
+    check(lib().rc_extend_workspace_bytes(ctypes.byref(a), ctypes.byref(n)),
+          "rc_extend_workspace_bytes")
+    return int(n.value)
+
+
 def extend_attention(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
                      k_pool, v_pool, o, *, sm_scale, max_q_len, max_prefix_len, lse=None,
-                     stream=None):
+                     stack=None, workspace=None, stream=None):
     """Extend attention of one layer (see rc_extend_attention). k_pool / v_pool are this layer's
-    planes [num_slots, Hkv, d]."""
+    planes [num_slots, Hkv, d]. stack: optional prefix-stacking groups (ranges, shared,
+    max_group_rows) -- int32 CUDA tensors and an int, as built by prefix_stacking_groups() --
+    with a uint8 CUDA workspace of extend_workspace_bytes(T, Hq) bytes."""
     a = _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,
-                     k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len)
+                     k_pool, v_pool, o, lse, sm_scale, max_q_len, max_prefix_len, stack,
+                     workspace)
     check(lib().rc_extend_attention(ctypes.byref(a), _stream(stream)), "rc_extend_attention")
 
 
@@ -261,6 +282,73 @@ def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k
 
 
 DEFAULT_KV_CHUNK = 512   # tokens per split-K chunk when kv_chunk = 0 (rc.h)
+
+
+# Cost model of one extend CTA, calibrated on GB300 (fork, two-level and few-shot replays):
+# about 2.15 us per 128-key tile for a pair of query tiles (half that for a lone tile, whose
+# key tiles split across the two softmax groups), 10 us of fixed cost per CTA, 1 us to merge.
+_T_TILE_US, _C_CTA_US, _C_MERGE_US = 2.15, 10.0, 1.0
+
+
+def _extend_cost_us(P, S, key0, ppt, merge):
+    """Estimated CTA-time of one request's per-request pass over keys [key0, P) and its S new
+    tokens, ppt query positions per tile."""
+    if S <= 0:
+        return 0.0
+    tiles = -(-(P - key0) // 128) + -(-S // 128)
+    pairs = -(-S // (2 * ppt))
+    per = tiles * (_T_TILE_US if S > ppt else _T_TILE_US / 2)
+    return pairs * (per + _C_CTA_US + (_C_MERGE_US if merge else 0.0))
+
+
+def stacking_pays(prefix_len, new_len, shared: int, group: int) -> bool:
+    """Whether a stacked prefix pass over `shared` keys for these requests (one group of
+    consecutive requests) is estimated to save at least 10% of their extend time. It pays when
+    stacking fills query tiles that short suffixes leave mostly empty; with long suffixes or
+    many query heads per KV head the tiles are full already and the extra per-request pass
+    only adds CTAs."""
+    ppt = max(128 // group, 1)
+    P = [int(x) for x in prefix_len]
+    S = [int(x) for x in new_len]
+    alone = sum(_extend_cost_us(p, s, 0, ppt, False) for p, s in zip(P, S))
+    U = sum(S)
+    if U <= 0:
+        return False
+    stacked_tiles = -(-shared // 128)
+    first = -(-U // (2 * ppt)) * (stacked_tiles * (_T_TILE_US if U > ppt else _T_TILE_US / 2)
+                                 + _C_CTA_US)
+    second = sum(_extend_cost_us(p, s, shared, ppt, True) for p, s in zip(P, S))
+    return first + second < 0.9 * alone
+
+
+def prefix_stacking_groups(rows, prefix_len, new_len, min_shared: int):
+    """Host-side grouping for extend: runs of consecutive requests whose slot rows hold the same
+    slots over at least min_shared of their matched prefixes. A run grows while the next
+    request agrees with the run's first over min_shared or more positions; its shared length is
+    the smallest such agreement. Returns (ranges [2 G], shared [G], max_group_rows) -- ranges as
+    (first, end) request pairs, max_group_rows the largest total of new tokens of a group."""
+    rows = np.asarray(rows)
+    P = np.asarray(prefix_len, dtype=np.int64)
+    S = np.asarray(new_len, dtype=np.int64)
+    B = len(P)
+    ranges, shared, max_rows = [], [], 0
+    b = 0
+    while b < B:
+        e, sh = b + 1, int(P[b])
+        while e < B:
+            n = int(min(sh, P[e]))
+            diff = np.flatnonzero(rows[b, :n] != rows[e, :n])
+            agree = int(diff[0]) if diff.size else n
+            if agree < min_shared:
+                break
+            sh = agree
+            e += 1
+        if e - b >= 2 and sh >= min_shared and int(S[b:e].sum()) > 0:
+            ranges += [b, e]
+            shared.append(sh)
+            max_rows = max(max_rows, int(S[b:e].sum()))
+        b = e
+    return np.asarray(ranges, np.int32), np.asarray(shared, np.int32), max_rows
 
 
 def shared_context_groups(rows, lengths, group_size: int, min_shared: int):

@@ -43,6 +43,7 @@ SIGNATURES = {
     "rc_radix_match_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P, _P]),
     "rc_radix_insert_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
     "rc_slot_table_write": (ctypes.c_int, [_P, _P]),
+    "rc_extend_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "rc_extend_attention": (ctypes.c_int, [_P, _P]),
     "rc_decode_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "rc_decode_attention": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
@@ -70,7 +71,9 @@ class RcExtendArgs(ctypes.Structure):
                 ("num_slots", _I64), ("sm_scale", ctypes.c_float), ("q", _P), ("k_new", _P),
                 ("v_new", _P), ("out_loc", _P), ("qo_indptr", _P), ("prefix_len", _P),
                 ("req_idx", _P), ("req_to_token", _P), ("k_pool", _P), ("v_pool", _P),
-                ("o", _P), ("lse", _P)]
+                ("o", _P), ("lse", _P), ("num_groups", _I32), ("max_group_rows", _I32),
+                ("group_range", _P), ("group_shared", _P), ("workspace", _P),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class RcDecodeArgs(ctypes.Structure):

@@ -5,6 +5,16 @@
 #include "extend_common.h"
 #include "host_common.h"
 
+extern "C" int rc_extend_workspace_bytes(const rc_extend_args* a, size_t* out_bytes) {
+  RC_CHECK_ARG(a != nullptr && out_bytes != nullptr, "rc_extend_workspace_bytes: NULL argument");
+  RC_CHECK_ARG(a->num_tokens >= 0 && a->num_q_heads > 0,
+               "rc_extend_workspace_bytes: bad sizes");
+  // one fp32 log-sum-exp per (token, query head) for the stacked pass's partial results
+  *out_bytes = ((size_t)a->num_tokens * (size_t)a->num_q_heads * sizeof(float) + 255) &
+               ~(size_t)255;
+  return RC_OK;
+}
+
 extern "C" int rc_extend_attention(const rc_extend_args* a, void* stream) {
   RC_CHECK_ARG(a != nullptr, "rc_extend_attention: args is NULL");
   RC_CHECK_ARG(a->dtype == RC_DTYPE_BF16 || a->dtype == RC_DTYPE_F32,
@@ -27,6 +37,17 @@ extern "C" int rc_extend_attention(const rc_extend_args* a, void* stream) {
                        (uintptr_t)a->k_pool | (uintptr_t)a->v_pool | (uintptr_t)a->o |
                        (uintptr_t)a->req_to_token;
   RC_CHECK_ARG((al & 15) == 0, "rc_extend_attention: tensors must be 16-byte aligned");
+  RC_CHECK_ARG(a->num_groups >= 0, "rc_extend_attention: num_groups %d", a->num_groups);
+  if (a->num_groups > 0 && a->dtype == RC_DTYPE_BF16) {
+    RC_CHECK_ARG(a->group_range && a->group_shared && a->max_group_rows > 0,
+                 "rc_extend_attention: stacking groups need group_range, group_shared and "
+                 "max_group_rows");
+    size_t need = 0;
+    rc_extend_workspace_bytes(a, &need);
+    RC_CHECK_ARG(a->workspace && ((uintptr_t)a->workspace & 15) == 0 && a->workspace_bytes >= need,
+                 "rc_extend_attention: stacking needs a 16-byte aligned workspace of %zu bytes",
+                 need);
+  }
   int* st = rc::device_status_ptr();
   if (!st) return rc::fail(RC_ERR_CUDA, "rc_extend_attention: no device status word");
   cudaStream_t s = (cudaStream_t)stream;

@@ -61,10 +61,15 @@ constexpr int kSoftmaxWarp0 = kScatterWarp0 + kScatterWarps;
 static_assert(kSoftmaxWarp0 == 8 && kThreads == 32 * (kSoftmaxWarp0 + 8), "warp roles");
 constexpr int kGroupThreads = 128;        // softmax threads of one query tile (one per row)
 // control warpgroups (warps 0-7) give registers up, the softmax warpgroups (8-15) take them
-constexpr int kRegsLaunch = 128, kRegsControl = 72, kRegsSoftmax = 184;
-static_assert(kThreads * kRegsLaunch <= 65536, "register file");
-static_assert(256 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
-              "a register split above the launch allocation never completes");
+// The kernel exists twice: without prefix-stacking support, and with it (the stacked pass and
+// the merge in the epilogue need a few more registers in the softmax warps).
+constexpr int kRegsLaunch = 128;
+template <bool kStack> struct Regs {
+  static constexpr int control = kStack ? 64 : 72, softmax = kStack ? 192 : 184;
+  static_assert(kThreads * kRegsLaunch <= 65536, "register file");
+  static_assert(256 * control + 256 * softmax <= kThreads * kRegsLaunch,
+                "a register split above the launch allocation never completes");
+};
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
 
 struct SmemLayout {
@@ -85,9 +90,23 @@ static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
 struct TcParams {
   rc_extend_args a;
   int* status;
-  int ppt;        // query positions per tile
-  float scale2;   // sm_scale * log2(e)
+  int ppt;           // query positions per tile
+  float scale2;      // sm_scale * log2(e)
+  int pass;          // 0: one request per CTA z; 1: stacked prefix pass, one group per CTA z
+  float* lse_part;   // [T, Hq] log2-sum-exp of the stacked pass's partial results
 };
+
+// Shared length of the group holding request b (ranges ascending and disjoint), 0 if none.
+__device__ __forceinline__ int group_shared_of(const rc_extend_args& a, int b) {
+  int lo = 0, hi = a.num_groups - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (b < a.group_range[2 * mid]) hi = mid - 1;
+    else if (b >= a.group_range[2 * mid + 1]) lo = mid + 1;
+    else return a.group_shared[mid];
+  }
+  return 0;
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -251,32 +270,74 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
 }
 
 // ---------------------------------------------------------------- the kernel
+template <bool kStack>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr int kRegsControl = Regs<kStack>::control, kRegsSoftmax = Regs<kStack>::softmax;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte swizzled operand tiles must start on 1024-byte boundaries
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const rc_extend_args& a = p.a;
-  const int b = blockIdx.z;
   const int hk = blockIdx.y;
-  const int qo = a.qo_indptr[b];
-  const int S = a.qo_indptr[b + 1] - qo;
-  const int P = a.prefix_len[b];
   const int G = a.num_q_heads / a.num_kv_heads;
   const int iA = blockIdx.x * 2 * p.ppt;       // first query position of tile A
-  if (S <= 0 || iA >= S) return;
-  const int row = a.req_idx[b];
-  if (P < 0 || (int64_t)P + S > a.max_ctx || row < 0 || row >= a.max_reqs || qo < 0 ||
-      (int64_t)qo + S > a.num_tokens) {
-    if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
-    return;
+  // The CTA's rows and keys. Per-request pass: request b's new tokens against keys
+  // [kstart, P) of its prefix -- kstart the shared length of its stacking group, 0 outside
+  // groups -- and causally its own new tokens. Stacked pass: the new tokens of group g's
+  // members, stacked in batch order, against keys [0, shared) only.
+  const bool stacked = kStack && p.pass == 1;
+  int b, qo, S, P, row, kstart = 0;
+  if (stacked) {
+    const int g = blockIdx.z;
+    const int b0 = a.group_range[2 * g], b1 = a.group_range[2 * g + 1];
+    if (b0 < 0 || b1 <= b0 || b1 > a.num_reqs) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && hk == 0) set_status(p.status, kStatusPosRange);
+      return;
+    }
+    b = b0;
+    qo = a.qo_indptr[b0];
+    S = a.qo_indptr[b1] - qo;
+    P = a.group_shared[g];
+    row = a.req_idx[b0];
+    if (threadIdx.x == 0 && blockIdx.x == 0 && hk == 0) {
+      for (int bb = b0; bb < b1; ++bb)   // every member matched the shared prefix
+        if (a.prefix_len[bb] < P) set_status(p.status, kStatusPosRange);
+    }
+    if (S <= 0 || iA >= S) return;
+    if (P < 1 || P > a.prefix_len[b0] || P > a.max_ctx || row < 0 || row >= a.max_reqs ||
+        qo < 0 || (int64_t)qo + S > a.num_tokens) {
+      if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
+      return;
+    }
+  } else {
+    b = blockIdx.z;
+    qo = a.qo_indptr[b];
+    S = a.qo_indptr[b + 1] - qo;
+    P = a.prefix_len[b];
+    if (S <= 0 || iA >= S) return;
+    row = a.req_idx[b];
+    if (P < 0 || (int64_t)P + S > a.max_ctx || row < 0 || row >= a.max_reqs || qo < 0 ||
+        (int64_t)qo + S > a.num_tokens) {
+      if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
+      return;
+    }
+    if (kStack && a.num_groups > 0) {
+      kstart = group_shared_of(a, b);
+      if (kstart < 0 || kstart > P) {
+        if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
+        kstart = 0;
+      }
+    }
   }
+  // rows merged with the stacked pass's partial result in the epilogue
+  const bool merge = kStack && !stacked && kstart > 0;
   const int iB = iA + p.ppt;
   const int nposA = min(p.ppt, S - iA);
   const int nposB = max(0, min(p.ppt, S - iB));
-  const int n_pre = (P + kN - 1) / kN;
-  // key tiles of each query tile: the prefix, then new-token keys up to its last position
-  const int nA = n_pre + (iA + nposA + kN - 1) / kN;
-  const int nB = nposB > 0 ? n_pre + (iB + nposB + kN - 1) / kN : 0;
+  const int n_pre = (P - kstart + kN - 1) / kN;     // prefix key tiles: keys [kstart, P)
+  // key tiles of each query tile: the prefix, then (per-request pass) new-token keys up to its
+  // last position
+  const int nA = n_pre + (stacked ? 0 : (iA + nposA + kN - 1) / kN);
+  const int nB = nposB > 0 ? n_pre + (stacked ? 0 : (iB + nposB + kN - 1) / kN) : 0;
   const int ntiles = max(nA, nB);
   const int kend = nposB > 0 ? iB + nposB : iA + nposA;  // new-token keys loaded: [0, kend)
   // virtual tiles: pair mode (query tiles A and B, every key tile each) or split mode (query
@@ -286,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int nt1 = split ? nA / 2 : nB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+  (void)b;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + SmemLayout::Q;
@@ -452,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     // loads of tile j+1 stay in flight while tile j is being copied
     auto raw = [&](int j, int q) -> int {
       if (j < n_pre) {
-        const int key = j * kN + w * kRowsPerWarp + q * 32 + lane;
+        const int key = kstart + j * kN + w * kRowsPerWarp + q * 32 + lane;
         return rt[key < P ? key : P - 1];
       }
       return 0;
@@ -505,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
     constexpr int kU = 4;
-    const int total = (nposA + nposB) * 16;
+    const int total = stacked ? 0 : (nposA + nposB) * 16;   // the stacked pass writes no K/V
     for (int base = (warp - kScatterWarp0) * 32 + lane; base < total; base += 32 * kScatterWarps * kU) {
       uint4 kv[kU], vv[kU];
       int64_t dst[kU];
@@ -558,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       tc_fence_after();
       // keys [0, lim) of key tile kt are visible to this row (lim <= 0: none)
       const int kt = split ? 2 * j + X : j;
-      const int lim = kt < n_pre ? min(kN, P - kt * kN) : min(kN, ipos - (kt - n_pre) * kN + 1);
+      const int lim = kt < n_pre ? min(kN, P - kstart - kt * kN)
+                                 : min(kN, ipos - (kt - n_pre) * kN + 1);
       float v[kN];
 #pragma unroll
       for (int c = 0; c < kN / 32; ++c) tmem_ld32(tS + c * 32, v + c * 32);
@@ -626,15 +689,51 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       tc_fence_before();
       mbar_arrive(&p_full[X]);
     }
+    // The row's result over this pass's keys is (O, lse2): O the accumulator(s) times `scale`,
+    // lse2 its log2-sum-exp. The stacked pass stores it as a partial (O in o, lse2 in the
+    // workspace); a group member's per-request pass merges it with that partial, weights
+    // 2^(lse2 - M) and 2^(lse_p - M); every other row is final as it is.
+    auto combine = [&](int64_t rowidx, float lse2, float& fs, float& fp, float& lse_out) {
+      fs = 1.f;
+      fp = 0.f;
+      lse_out = lse2;
+      if (merge) {
+        const float lp = p.lse_part[rowidx];
+        const float M = fmaxf(lse2, lp);
+        const float es = ex2(lse2 - M), ep = ex2(lp - M);
+        const float inv = 1.f / (es + ep);
+        fs = es * inv;
+        fp = ep * inv;
+        lse_out = M + log2f(es + ep);
+      }
+    };
+    // 8 output columns: acc * scale (+ fp * the partial already in o) -> bf16
+    auto store8 = [&](__nv_bfloat16* dst, const float* acc, float scale, float fp) {
+      float v8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v8[k] = acc[k] * scale;
+      if (merge) {
+        const uint4 old = *(const uint4*)dst;
+        v8[0] += fp * bf16lo(old.x); v8[1] += fp * bf16hi(old.x);
+        v8[2] += fp * bf16lo(old.y); v8[3] += fp * bf16hi(old.y);
+        v8[4] += fp * bf16lo(old.z); v8[5] += fp * bf16hi(old.z);
+        v8[6] += fp * bf16lo(old.w); v8[7] += fp * bf16hi(old.w);
+      }
+      *(uint4*)dst = make_uint4(pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
+                                pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+    };
     if (nX > 0 && !split) {
       // epilogue: O / l for this thread's row
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
       if (ok) {
         tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const bool store = r < rows_used;
         const int i = iX + r / G, hh = r % G;
-        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD;
+        const int64_t rowidx = (int64_t)(qo + i) * Hq + hk * G + hh;
+        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + rowidx * kD;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        float fs = 1.f, fp = 0.f, lse2 = m_run + log2f(l_exact);
+        if (store) combine(rowidx, lse2, fs, fp, lse2);
 #pragma unroll 1
         for (int c = 0; c < kD / 32; ++c) {
           float o[32];
@@ -643,17 +742,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           reg_fence32(o);
           if (store) {
 #pragma unroll
-            for (int u = 0; u < 32; u += 8) {
-              *(uint4*)(orow + c * 32 + u) =
-                  make_uint4(pack_bf16(o[u] * inv, o[u + 1] * inv),
-                             pack_bf16(o[u + 2] * inv, o[u + 3] * inv),
-                             pack_bf16(o[u + 4] * inv, o[u + 5] * inv),
-                             pack_bf16(o[u + 6] * inv, o[u + 7] * inv));
-            }
+            for (int u = 0; u < 32; u += 8) store8(orow + c * 32 + u, o + u, inv * fs, fp);
           }
         }
-        if (store && a.lse)
-          a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] = (m_run + log2f(l_exact)) * kLn2;
+        if (store) {
+          if (stacked) p.lse_part[rowidx] = lse2;
+          else if (a.lse) a.lse[rowidx] = lse2 * kLn2;
+        }
       }
     } else if (split) {
       // merge the two virtual tiles: every softmax thread publishes its row max and sums;
@@ -674,11 +769,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const float w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
         const float lt = w0 * xl[r] + w1 * xl[128 + r];
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float a0 = w0 * inv, a1 = w1 * inv;
         tc_fence_after();
         const bool store = r < rows_used;
         const int i = iA + r / G, hh = r % G;
-        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD;
+        const int64_t rowidx = (int64_t)(qo + i) * Hq + hk * G + hh;
+        __nv_bfloat16* orow = (__nv_bfloat16*)a.o + rowidx * kD;
+        float fs = 1.f, fp = 0.f, lse2 = M + log2f(w0 * xe[r] + w1 * xe[128 + r]);
+        if (store) combine(rowidx, lse2, fs, fp, lse2);
+        const float a0 = w0 * inv * fs, a1 = w1 * inv * fs;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           const int col = 64 * X + 32 * c;
@@ -694,14 +792,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
               float v8[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k) v8[k] = o0[u + k] * a0 + o1[u + k] * a1;
-              *(uint4*)(orow + col + u) = make_uint4(pack_bf16(v8[0], v8[1]), pack_bf16(v8[2], v8[3]),
-                                                     pack_bf16(v8[4], v8[5]), pack_bf16(v8[6], v8[7]));
+              store8(orow + col + u, v8, 1.f, fp);
             }
           }
         }
-        if (store && X == 0 && a.lse)
-          a.lse[(int64_t)(qo + i) * Hq + hk * G + hh] =
-              (M + log2f(w0 * xe[r] + w1 * xe[128 + r])) * kLn2;
+        if (store && X == 0) {
+          if (stacked) p.lse_part[rowidx] = lse2;
+          else if (a.lse) a.lse[rowidx] = lse2 * kLn2;
+        }
       }
     }
   }
@@ -720,30 +818,56 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   if (a->head_dim != kD) return fail(RC_ERR_INVALID, "extend (tensor cores): head_dim must be 128");
   const int G = a->num_q_heads / a->num_kv_heads;
   if (G > kM) return fail(RC_ERR_INVALID, "extend (tensor cores): group size %d > 128", G);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int launch_regs = 0;
-  std::call_once(once, []() {
-    attr_err = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SmemLayout::ALLOC);
+  // per instantiation: opt in to the shared memory, and check that the launch allocation
+  // covers the register split (the softmax warpgroups' setmaxnreg.inc would never return)
+  struct Setup {
+    cudaError_t err = cudaSuccess;
+    int regs = 0;
+  };
+  auto setup = [](auto kern) {
+    Setup st;
+    st.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SmemLayout::ALLOC);
     cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, extend_tc_kernel);
-    if (attr_err == cudaSuccess) launch_regs = fa.numRegs;
+    if (st.err == cudaSuccess) st.err = cudaFuncGetAttributes(&fa, kern);
+    if (st.err == cudaSuccess) st.regs = fa.numRegs;
+    return st;
+  };
+  static std::once_flag once;
+  static Setup s_plain, s_stack;
+  std::call_once(once, [&]() {
+    s_plain = setup(extend_tc_kernel<false>);
+    s_stack = setup(extend_tc_kernel<true>);
   });
-  if (attr_err != cudaSuccess)
-    return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(attr_err));
-  // the softmax warpgroups' setmaxnreg.inc only completes if the launch allocation covers the split
-  if (launch_regs < kRegsLaunch)
-    return fail(RC_ERR_CUDA, "extend (tensor cores): kernel built with %d registers per thread, "
-                "the register split needs %d", launch_regs, kRegsLaunch);
+  for (const Setup* st : {&s_plain, &s_stack}) {
+    if (st->err != cudaSuccess)
+      return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(st->err));
+    if (st->regs < kRegsLaunch)
+      return fail(RC_ERR_CUDA, "extend (tensor cores): kernel built with %d registers per "
+                  "thread, the register split needs %d", st->regs, kRegsLaunch);
+  }
   TcParams p;
   p.a = *a;
   p.status = status;
   p.ppt = kM / G;
   p.scale2 = a->sm_scale * kLog2e;
+  p.lse_part = (float*)a->workspace;
+  int launches = 0;
+  if (a->num_groups > 0) {
+    // stacked prefix pass first: every group member's partial result is in place before the
+    // per-request pass merges it (same stream)
+    p.pass = 1;
+    dim3 g1((a->max_group_rows + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_groups);
+    extend_tc_kernel<true><<<g1, kThreads, SmemLayout::ALLOC, s>>>(p);
+    ++launches;
+  }
+  p.pass = 0;
   dim3 grid((a->max_q_len + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_reqs);
-  extend_tc_kernel<<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
-  count_launches(1);
+  if (a->num_groups > 0)
+    extend_tc_kernel<true><<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
+  else
+    extend_tc_kernel<false><<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
+  count_launches(launches + 1);
   return check_launch("rc_extend_attention (tensor cores)");
 }
 

@@ -22,7 +22,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
-               shared_context_groups)
+               extend_workspace_bytes, prefix_stacking_groups, shared_context_groups,
+               stacking_pays)
 from .runtime import DeviceKV, HostCache, Plan
 
 
@@ -36,6 +37,8 @@ class ExtendBatch:
     out_loc: object        # device int32 [T]
     max_q_len: int
     max_prefix_len: int
+    stack: object = None       # (device ranges, device shared, max_group_rows) or None
+    workspace: object = None   # device scratch of the stacked pass
 
     @property
     def num_tokens(self) -> int:
@@ -55,9 +58,14 @@ class DecodeBatch:
     num_groups: int = 0
 
 
+# shortest shared prefix worth a stacked pass: two key tiles
+STACK_MIN_SHARED = 256
+
+
 class Engine:
     def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
-                 max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True):
+                 max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True,
+                 stack_extend=True):
         self.layers = layers
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
         self.sm_scale = 1.0 / float(np.sqrt(head_dim))
@@ -68,6 +76,10 @@ class Engine:
         self.kv_chunk = kv_chunk
         # decode reads a context prefix that several requests share once for all of them
         self.share_decode = share_decode
+        # extend stacks the new tokens of consecutive requests over a prefix they share, where
+        # that is estimated to pay (True), for every group found ("always"), or never (False)
+        self.stack_extend = stack_extend
+        self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
 
@@ -89,14 +101,37 @@ class Engine:
         qo, pl, ri, ol = self.dev.upload_i32([plan.qo_indptr, plan.prefix_len, row_ids,
                                               plan.out_loc])
         S = plan.lengths - plan.prefix_len
-        return ExtendBatch(plan, row_ids, qo, pl, ri, ol, int(S.max()) if B else 0,
-                           int(plan.prefix_len.max()) if B else 0)
+        batch = ExtendBatch(plan, row_ids, qo, pl, ri, ol, int(S.max()) if B else 0,
+                            int(plan.prefix_len.max()) if B else 0)
+        if self.stack_extend and B > 1:
+            ranges, shared, max_rows = prefix_stacking_groups(plan.rows, plan.prefix_len, S,
+                                                              STACK_MIN_SHARED)
+            # keep the groups whose stacked pass is estimated to pay
+            G = self.n_q_heads // self.n_kv_heads
+            keep = [g for g in range(len(shared))
+                    if self.stack_extend == "always" or stacking_pays(
+                        plan.prefix_len[ranges[2 * g]:ranges[2 * g + 1]],
+                        S[ranges[2 * g]:ranges[2 * g + 1]], int(shared[g]), G)]
+            ranges = ranges.reshape(-1, 2)[keep].reshape(-1)
+            shared = shared[keep]
+            max_rows = max([int(S[ranges[2 * g]:ranges[2 * g + 1]].sum())
+                            for g in range(len(shared))], default=0)
+            if len(shared):
+                r, sh = self.dev.upload_i32([ranges, shared])
+                batch.stack = (r, sh, max_rows)
+                need = extend_workspace_bytes(plan.num_tokens, self.n_q_heads)
+                if self._ext_ws is None or self._ext_ws.numel() < need:
+                    self._ext_ws = self.dev.torch.empty(need, dtype=self.dev.torch.uint8,
+                                                        device=self.dev.device)
+                batch.workspace = self._ext_ws
+        return batch
 
     def extend_layer(self, batch: ExtendBatch, layer: int, q, k_new, v_new, o, lse=None):
         extend_attention(q, k_new, v_new, batch.out_loc, batch.qo_indptr, batch.prefix_len,
                          batch.req_idx, self.dev.req_to_token, self.dev.k[layer],
                          self.dev.v[layer], o, sm_scale=self.sm_scale,
-                         max_q_len=batch.max_q_len, max_prefix_len=batch.max_prefix_len, lse=lse)
+                         max_q_len=batch.max_q_len, max_prefix_len=batch.max_prefix_len, lse=lse,
+                         stack=batch.stack, workspace=batch.workspace)
 
     def extend_end(self, batch: ExtendBatch, keep_locked: bool = False):
         ends, dups = self.host.finish(batch.plan, keep_locked=keep_locked)

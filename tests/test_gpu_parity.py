@@ -331,3 +331,74 @@ def test_decode_group_contract_breaches_are_reported():
                             groups=groups)
         torch.cuda.synchronize()
         assert rc.device_status() != 0
+
+
+# ---------------------------------------------------------------- extend: prefix stacking (E3b)
+def _stack_families(seed, spec):
+    """Consecutive requests per family: family f shares spec[f][0] cached tokens; member i adds
+    spec[f][1][i] = (private cached tokens, new tokens). Returns (cache seqs, extend seqs)."""
+    cache, ext = [], []
+    for f, (ls, mem) in enumerate(spec):
+        shared = synth.tokens(seed, 700 + f, ls)
+        cache.append(shared)
+        for i, (priv, new) in enumerate(mem):
+            own = synth.tokens(seed, 1200 + 31 * f + i, priv + new)
+            full = np.concatenate([shared, own]).astype(np.int32)
+            if priv:
+                cache.append(full[:ls + priv])
+            ext.append(full)
+    return cache, ext
+
+
+_STACK_SPEC = [(700, [(0, 40), (0, 1), (30, 200), (0, 130)]),   # private parts, long and 1-row
+               (300, [(0, 5), (0, 7)]),                          # stacked tile in split mode
+               (2000, [(0, 50)] * 6),                            # few-shot like
+               (100, [(0, 20), (0, 20)]),                        # shared below the threshold
+               (900, [(5, 60)])]                                 # alone
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 2), (16, 8)])
+def test_extend_prefix_stacking(Hq, Hkv):
+    """Stacked prefix pass + per-request pass with merge: every unit within tolerance of the
+    oracle, and the engine without stacking too."""
+    m = W.Model(1, Hq, Hkv, 128, "bf16", 11)
+    cache, ext = _stack_families(11, _STACK_SPEC)
+    w = W.Workload("ext_stack", m, 40_000, synth.permutation(11, 40_000), max_ctx=3008)
+    for stack in (True, False):
+        eng = H.make_engine(w, max_reqs=64, stack_extend="always" if stack else False)
+        for c in cache:
+            H.run_cache_phase(eng, m, [c])
+        b, outs = H.run_extend_phase(eng, m, ext, lse=True)
+        if stack:
+            assert b.stack is not None and int(b.stack[1].numel()) == 3   # three stacked groups
+        _status_clear()
+        units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
+        _check_extend(w, b, outs, ext, units)
+
+
+def test_extend_stacking_contract_breach_is_reported():
+    """A shared length past a member's matched prefix is reported through the status word."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    from synth import device as sdev
+    m = W.Model(1, 8, 8, 128, "bf16", 12)
+    cache, ext = _stack_families(12, [(600, [(0, 30), (0, 40)])])
+    w = W.Workload("ext_breach", m, 4000, None, max_ctx=704)
+    eng = H.make_engine(w, max_reqs=8, stack_extend=False)
+    for c in cache:
+        H.run_cache_phase(eng, m, [c])
+    b = eng.extend_begin(ext)
+    h = H.new_token_hashes(m, ext, b.plan.prefix_len)
+    q, k, v = H.dense_qkv(m, sdev.hashes_to_device(h), 0, b.num_tokens)
+    o = torch.empty_like(q)
+    ws = torch.empty(rc.extend_workspace_bytes(b.num_tokens, m.n_q_heads), dtype=torch.uint8,
+                     device="cuda")
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    stack = (dev([0, 2]), dev([650]), 70)      # 650 > the matched prefix of 600
+    rc.extend_attention(q, k, v, b.out_loc, b.qo_indptr, b.prefix_len, b.req_idx,
+                        eng.dev.req_to_token, eng.dev.k[0], eng.dev.v[0], o,
+                        sm_scale=eng.sm_scale, max_q_len=b.max_q_len,
+                        max_prefix_len=b.max_prefix_len, stack=stack, workspace=ws)
+    torch.cuda.synchronize()
+    assert rc.device_status() != 0
+    eng.extend_end(b)

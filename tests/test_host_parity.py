@@ -230,3 +230,52 @@ def test_shared_context_groups_find_families():
     got = sorted((tuple(sorted(members[indptr[g]:indptr[g + 1]].tolist())), int(shared[g]))
                  for g in range(len(shared)))
     assert got == [((0, 1, 2), 500), ((3, 4, 5), 600), ((6, 7, 8), 700), ((9, 10, 11), 800)]
+
+
+# ---------------------------------------------------------------- extend stacking groups (host)
+@pytest.mark.parametrize("seed", range(12))
+def test_prefix_stacking_groups_are_valid(seed):
+    """Ranges ascending and disjoint, at least two requests each, rows identical over the shared
+    length, which is at least min_shared, within every member's prefix, and the smallest
+    agreement with the run's first request; max_group_rows bounds each group's new tokens."""
+    from prefix_cached_paged_gb300 import prefix_stacking_groups
+    rng = np.random.default_rng(100 + seed)
+    B, W_ = 30, 400
+    rows = rng.integers(0, 10_000, (B, W_)).astype(np.int32)
+    P = rng.integers(0, W_, B)
+    S = rng.integers(0, 50, B)
+    for b in range(1, B):
+        if rng.random() < 0.6:
+            n = int(rng.integers(0, W_))
+            rows[b, :n] = rows[b - 1, :n]
+    min_shared = int(rng.choice([1, 32, 128]))
+    ranges, shared, max_rows = prefix_stacking_groups(rows, P, S, min_shared)
+    assert len(ranges) == 2 * len(shared)
+    prev_end = 0
+    for g in range(len(shared)):
+        b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
+        assert prev_end <= b0 and b1 - b0 >= 2
+        prev_end = b1
+        sh = int(shared[g])
+        assert sh >= min_shared
+        assert int(S[b0:b1].sum()) <= max_rows
+        agree = []
+        for b in range(b0, b1):
+            assert sh <= P[b]
+            np.testing.assert_array_equal(rows[b, :sh], rows[b0, :sh])
+            if b > b0:
+                n = int(min(P[b0], P[b]))
+                d = np.flatnonzero(rows[b0, :n] != rows[b, :n])
+                agree.append(int(d[0]) if d.size else n)
+        assert sh == min(agree + [int(P[b0])])
+
+
+def test_stacking_policy_on_the_measured_workloads():
+    """The calibrated cost model stacks the few-shot batch (50-token suffixes over 2000 shared
+    tokens, MHA) and leaves the fork step (200-token suffixes) and the two-level GQA batch alone,
+    as their measurements with stacking forced on showed."""
+    from prefix_cached_paged_gb300 import stacking_pays
+    assert stacking_pays([2000] * 64, [50] * 64, 2000, 1)
+    assert not stacking_pays([1500] * 5, [200] * 5, 1500, 1)
+    v = np.random.default_rng(0).integers(1, 99, 64)
+    assert not stacking_pays(1000 + v, (100 - v) + 20, 1000, 8)
