@@ -390,6 +390,65 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // ---- producer state (warps 1-4). Producer w of an operand fills tile rows [64 w, 64 w + 64):
+  // lane l resolves rows 64 w + l and 64 w + 32 + l to a row pointer; one copy instruction then
+  // moves 16-byte chunk (l & 15) of two rows, the row pointer taken from its owner lane by a
+  // shuffle.
+  const bool producer = warp >= kKWarp0 && warp < kScatterWarp0;
+  const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
+  const bool is_v = warp >= kVWarp0;
+  const int w = warp - (is_v ? kVWarp0 : kKWarp0);
+  constexpr int kRowsPerWarp = kN / kProdWarps;
+  constexpr int kGroups = kRowsPerWarp / 32;
+  static_assert(kGroups == 2, "two 32-row groups per producer warp");
+  const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
+  const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
+  uint64_t* full = is_v ? v_full : k_full;
+  uint64_t* empty = is_v ? v_empty : k_empty;
+  const int c = lane & 15, half = lane >> 4;
+  // destination of row 2 i + half (i = 0..15) of a 32-row group, chunk c: the swizzle term
+  // repeats every four values of i; the row term adds 1024 bytes per four
+  uint32_t d4[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) d4[m] = sw128_off(2 * m + half, c);
+  const uint32_t sbuf = (is_v ? sV : sK) + (uint32_t)(w * kRowsPerWarp * 128);
+  // raw(j, q) only issues the slot load; rowptr() checks it when the tile is issued, so the
+  // loads of tile j+1 stay in flight while tile j is being copied
+  auto raw = [&](int j, int q) -> int {
+    if (j < n_pre) {
+      const int key = kstart + j * kN + w * kRowsPerWarp + q * 32 + lane;
+      return rt[key < P ? key : P - 1];
+    }
+    return 0;
+  };
+  auto rowptr = [&](int j, int q, int rv) -> const __nv_bfloat16* {
+    if (j < n_pre) {
+      int sl = rv;
+      if (sl < 0 || (int64_t)sl >= a.num_slots) {
+        set_status(p.status, kStatusSlotRange);
+        sl = 0;
+      }
+      return pool + ((int64_t)sl * Hkv + hk) * kD;
+    }
+    const int s0 = (j - n_pre) * kN + w * kRowsPerWarp + q * 32 + lane;
+    return nsrc + ((int64_t)(qo + min(s0, kend - 1)) * Hkv + hk) * kD;
+  };
+  auto copy_tile = [&](int j, const __nv_bfloat16* p0, const __nv_bfloat16* p1) {
+    const uint32_t dst = sbuf + (j % kStagesKV) * kTileBytes;
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) {
+      const uint64_t rp = (uint64_t)(q == 0 ? p0 : p1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat16* src =
+            (const __nv_bfloat16*)__shfl_sync(0xffffffffu, rp, 2 * i + half) + c * 8;
+        cp_async16(dst + q * 32 * 128 + (i >> 2) * 1024 + d4[i & 3], src);
+      }
+    }
+  };
+  // stage 0 is free at the start: the first key tile's copies go out before the setup barrier
+  if (producer && ntiles > 0) copy_tile(0, rowptr(0, 0, raw(0, 0)), rowptr(0, 1, raw(0, 1)));
+
   // Q tiles: row m of tile X = (position iX + m / G, head hk * G + m % G); rows past the tile
   // are zero-filled. Copied asynchronously (every thread, 16 bytes at a time); the MMA warp
   // waits on q_full, so the copies overlap TMEM allocation and the first K/V loads.
@@ -491,50 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   } else if (warp < kScatterWarp0) {
     // ------------------------------------------------------------ producers (K: warps 1-2, V: 3-4)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    // Producer w of an operand fills tile rows [64 w, 64 w + 64): lane l resolves rows
-    // 64 w + l and 64 w + 32 + l to a row pointer; one copy instruction then moves 16-byte chunk
-    // (l & 15) of two rows, the row pointer taken from its owner lane by a shuffle.
-    const int32_t* rt = a.req_to_token + (int64_t)row * a.max_ctx;
-    const bool is_v = warp >= kVWarp0;
-    const int w = warp - (is_v ? kVWarp0 : kKWarp0);
-    constexpr int kRowsPerWarp = kN / kProdWarps;
-    constexpr int kGroups = kRowsPerWarp / 32;
-    const __nv_bfloat16* pool = (const __nv_bfloat16*)(is_v ? a.v_pool : a.k_pool);
-    const __nv_bfloat16* nsrc = (const __nv_bfloat16*)(is_v ? a.v_new : a.k_new);
-    uint64_t* full = is_v ? v_full : k_full;
-    uint64_t* empty = is_v ? v_empty : k_empty;
-    const int c = lane & 15, half = lane >> 4;
-    // destination of row 2 i + half (i = 0..15) of a 32-row group, chunk c: the swizzle term
-    // repeats every four values of i; the row term adds 1024 bytes per four
-    uint32_t d4[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) d4[m] = sw128_off(2 * m + half, c);
-    const uint32_t sbuf = (is_v ? sV : sK) + (uint32_t)(w * kRowsPerWarp * 128);
-    // raw(j, q) only issues the slot load; rowptr() checks it when the tile is issued, so the
-    // loads of tile j+1 stay in flight while tile j is being copied
-    auto raw = [&](int j, int q) -> int {
-      if (j < n_pre) {
-        const int key = kstart + j * kN + w * kRowsPerWarp + q * 32 + lane;
-        return rt[key < P ? key : P - 1];
-      }
-      return 0;
-    };
-    auto rowptr = [&](int j, int q, int rv) -> const __nv_bfloat16* {
-      if (j < n_pre) {
-        int sl = rv;
-        if (sl < 0 || (int64_t)sl >= a.num_slots) {
-          set_status(p.status, kStatusSlotRange);
-          sl = 0;
-        }
-        return pool + ((int64_t)sl * Hkv + hk) * kD;
-      }
-      const int s0 = (j - n_pre) * kN + w * kRowsPerWarp + q * 32 + lane;
-      return nsrc + ((int64_t)(qo + min(s0, kend - 1)) * Hkv + hk) * kD;
-    };
-    static_assert(kGroups == 2, "two 32-row groups per producer warp");
-    int n0 = raw(0, 0), n1 = raw(0, 1);
+    // tile 0 was issued before the barrier; its arrival (which also covers this thread's Q
+    // chunks) can only follow the barrier initialisation
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
+    if (ntiles > 0) cp_async_arrive_noinc(smem_u32(&full[0]));
+    int n0 = ntiles > 1 ? raw(1, 0) : 0, n1 = ntiles > 1 ? raw(1, 1) : 0;
+    for (int j = 1; j < ntiles && ok; ++j) {
       const int st = j % kStagesKV;
       const __nv_bfloat16* p0 = rowptr(j, 0, n0);
       const __nv_bfloat16* p1 = rowptr(j, 1, n1);
@@ -545,17 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j / kStagesKV) - 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const uint32_t dst = sbuf + st * kTileBytes;
-#pragma unroll
-      for (int q = 0; q < kGroups; ++q) {
-        const uint64_t rp = (uint64_t)(q == 0 ? p0 : p1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat16* src =
-              (const __nv_bfloat16*)__shfl_sync(0xffffffffu, rp, 2 * i + half) + c * 8;
-          cp_async16(dst + q * 32 * 128 + (i >> 2) * 1024 + d4[i & 3], src);
-        }
-      }
+      copy_tile(j, p0, p1);
       cp_async_arrive_noinc(smem_u32(&full[st]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
