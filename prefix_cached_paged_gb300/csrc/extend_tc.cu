@@ -492,8 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const int kt = kt_of(X, t), st = kt % kStagesKV;
         const bool first = split || X == 0 || kt >= nA;
         const bool last = split || X == 1 || kt >= nB;
-        if (first && !mbar_wait(&k_full[st], (kt / kStagesKV) & 1, p.status)) return false;
-        fence_async_smem();   // K arrived through the generic proxy (cp.async)
+        if (first) {
+          if (!mbar_wait(&k_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+          // K arrived through the generic proxy (cp.async); one fence covers every later
+          // MMA this thread issues on the stage
+          fence_async_smem();
+        }
         tc_fence_after();
         const uint32_t qsrc = sQ + (split ? 0 : X) * kTileBytes;
 #pragma unroll
@@ -512,8 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (!mbar_wait(&p_full[X], t & 1, p.status)) return false;
         const bool first = split || X == 0 || kt >= nA;
         const bool last = split || X == 1 || kt >= nB;
-        if (first && !mbar_wait(&v_full[st], (kt / kStagesKV) & 1, p.status)) return false;
-        fence_async_smem();   // V arrived through the generic proxy (cp.async)
+        if (first) {
+          if (!mbar_wait(&v_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+          fence_async_smem();   // V arrived through the generic proxy (cp.async)
+        }
         tc_fence_after();
         const uint32_t tS = tmem + X * 128;
 #pragma unroll
