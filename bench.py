@@ -620,6 +620,103 @@ def bench_replay(args, rank, world, local):
             "clocks": clk, "gpu_launches": rc.launch_count() - launches0}
 
 
+def bench_queue(args, rank, world, local):
+    """Cache-aware scheduling on the program queue: the whole queue served batch by batch through
+    the engine (schedule -> plan + slot table -> extend kernel -> insert) under
+    longest-shared-prefix-first and under first-come-first-served, the same admission rule for
+    both. One pass over the queue is a step (fresh engine each time). Timed: the host calls
+    (schedule, plan, slot-table upload, insert; perf_counter) and the extend kernels (CUDA
+    events); the synthetic q / k / v fills between them are not."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    from synth import device as sdev
+    from synth import workloads as W
+    from tests import harness as H
+
+    pq = W.program_queue()
+    m = pq.workload.model
+    prompt = int(sum(len(s) for s in pq.seqs))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    launches = 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    for name, policy in (("lspf", rc.RC_SCHED_LSPF), ("fcfs", rc.RC_SCHED_FCFS)):
+        runs = []
+        for rep in range(args.warmup + args.steps):
+            eng = H.make_engine(pq.workload, max_reqs=pq.max_batch + 8)
+            waiting = list(range(len(pq.seqs)))
+            host_s = gpu_ms = flops = 0.0
+            steps = computed = evicted = 0
+            l0 = rc.launch_count()
+            while waiting:
+                t0 = time.perf_counter()
+                idx = eng.host.schedule([pq.seqs[i] for i in waiting], pq.max_batch,
+                                        pq.max_new_tokens, policy=policy)
+                if not idx:
+                    raise RuntimeError("program queue: no request fits the pool")
+                ids = [waiting[i] for i in idx]
+                batch = [pq.seqs[i] for i in ids]
+                b = eng.extend_begin(batch)
+                host_s += time.perf_counter() - t0
+                T = b.num_tokens
+                h = H.new_token_hashes(m, batch, b.plan.prefix_len)
+                q, k, v = H.dense_qkv(m, sdev.hashes_to_device(h), 0, T)
+                o = torch.empty_like(q)
+                ev0.record()
+                eng.extend_layer(b, 0, q, k, v, o)
+                ev1.record()
+                torch.cuda.synchronize()
+                gpu_ms += ev0.elapsed_time(ev1)
+                Pl = b.plan.prefix_len.astype(np.int64)
+                flops += extend_flops(Pl, b.plan.lengths - Pl, m.n_q_heads, m.head_dim)
+                computed += T
+                evicted += int(b.plan.evicted)
+                t0 = time.perf_counter()
+                eng.extend_end(b)
+                for i in sorted(idx, reverse=True):
+                    waiting.pop(i)
+                host_s += time.perf_counter() - t0
+                steps += 1
+            assert rc.device_status() == 0
+            if rep >= args.warmup:
+                runs.append((host_s * 1e3, gpu_ms, flops, steps, computed, evicted))
+                launches += rc.launch_count() - l0
+        host_ms = float(np.mean([r[0] for r in runs]))
+        g_ms = float(np.mean([r[1] for r in runs]))
+        _, _, flops, steps, computed, evicted = runs[0]
+        out[name] = {"batches": steps, "computed_tokens": computed, "evicted_tokens": evicted,
+                     "hit_rate": round(1 - computed / prompt, 4),
+                     "host_ms": round(host_ms, 3), "extend_gpu_ms": round(g_ms, 3),
+                     "extend_tflops": round(flops / (g_ms * 1e-3) / 1e12, 1),
+                     "prompt_tokens_per_s": round(prompt / ((host_ms + g_ms) * 1e-3), 1)}
+    clk = clocks.stop()
+    pk = peaks()
+    lo = out["lspf"]
+    val = lo["prompt_tokens_per_s"]
+    return {"metric": METRIC, "value": val, "unit": "prompt tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(lo["host_ms"] + lo["extend_gpu_ms"], 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": m.dtype,
+            "data": "synthetic",
+            "config": {"workload": "program_queue",
+                       "queue": f"{pq.program.max() + 1} programs x {len(pq.seqs) // (pq.program.max() + 1)} "
+                                f"questions, interleaved; {len(pq.seqs[0])} tokens each",
+                       "pool_slots": pq.workload.pool_slots, "max_batch": pq.max_batch,
+                       "max_new_tokens": pq.max_new_tokens, "layers": m.layers,
+                       "step": "the whole queue served once, fresh cache",
+                       "time": "host calls + extend kernels (synthetic q/k/v fills excluded)"},
+            "policies": out,
+            "speedup_lspf_over_fcfs": round(val / out["fcfs"]["prompt_tokens_per_s"], 2),
+            "roofline": {"kernel": "extend_attention (lspf batches)", "bound": "tensor",
+                         "achieved": lo["extend_tflops"], "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(lo["extend_tflops"] / pk["bf16_tflops"], 4),
+                         "traffic": None, "peak_source": pk["source"]},
+            "prefill_tokens_skipped": {"skipped": prompt - lo["computed_tokens"],
+                                       "prompt_tokens": prompt},
+            "clocks": clk, "gpu_launches": launches}
+
+
 def bench_reference(args, rank, world):
     """The oracle timed on the host cores, same workload and metric, bounded sample per step."""
     if rank != 0:
@@ -658,8 +755,10 @@ def main():
     ap.add_argument("--workload", default="fork_mixed_step",
                     choices=["fork_mixed_step", "tiny_extend", "few_shot_extend",
                              "two_level_extend", "multi_turn_decode",
-                             "multi_turn_decode_unshared", "fork_extend_layer"],
-                    help="fork_mixed_step = the full step; the others replay one kernel")
+                             "multi_turn_decode_unshared", "fork_extend_layer",
+                             "program_queue"],
+                    help="fork_mixed_step = the full step; program_queue = the scheduler over a "
+                         "request queue; the others replay one kernel")
     ap.add_argument("--kv-chunk", type=int, default=0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -683,6 +782,8 @@ def main():
         __graft_entry__.build()
         if args.workload == "fork_mixed_step":
             out = bench_ours(args, rank, world, local)
+        elif args.workload == "program_queue":
+            out = bench_queue(args, rank, world, local)
         else:
             out = bench_replay(args, rank, world, local)
     if rank == 0 and out is not None:

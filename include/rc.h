@@ -148,6 +148,33 @@ int rc_radix_insert_batch(rc_radix* tree, const int32_t* tokens, const int64_t* 
                           const rc_node* unlock_nodes, int32_t keep_locked, rc_node* end_nodes,
                           int64_t* out_freed);
 
+/* Cache-aware batch formation (paper digest Sec. 3 "cache-aware scheduling": order the waiting
+ * requests longest shared prefix first rather than first come first served; its Theorem 3.1
+ * says that order is the radix tree's depth-first order, which computes every edge once when
+ * the cache holds the longest request; App. A.2 pseudocode: match every waiting request, sort
+ * by match length, admit into the batch while memory allows, evicting as needed). Reads the
+ * tree and the pool; changes nothing (no split, no stamp, no lock).
+ *
+ * Waiting sequence w is tokens[indptr[w] : indptr[w+1]] (host arrays, w in queue order); its
+ * match is the longest cached prefix of its first match_len[w] tokens (match_len NULL = the
+ * whole sequence), written to out_match[w]. out_order[0:B] = the waiting sequences in
+ * scheduling order: RC_SCHED_LSPF by descending match, ties in queue order; RC_SCHED_FCFS in
+ * queue order. Admission walks that order and stops at the first sequence that does not fit:
+ *   - at most max_batch sequences;
+ *   - at most max_new_tokens computed tokens, sum of (length - match) (max_new_tokens < 0: no
+ *     limit);
+ *   - room: free slots + cached tokens in nodes with reference count 0 - reserve_slots must cover
+ *     the computed tokens plus the unreferenced cached tokens that the admitted matches would
+ *     lock (each cached token counted once).
+ * *out_admitted = the admitted count; the batch is out_order[0 : *out_admitted]. Matching the
+ * admitted sequences in that order (rc_radix_match_batch with the same match_len) and evicting
+ * the shortfall then always succeeds. RC_ERR_INVALID on a NULL or inconsistent argument. */
+enum { RC_SCHED_LSPF = 0, RC_SCHED_FCFS = 1 };
+int rc_schedule_batch(const rc_radix* tree, const int32_t* tokens, const int64_t* indptr,
+                      int32_t B, const int32_t* match_len, int32_t policy, int32_t max_batch,
+                      int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
+                      int32_t* out_match, int32_t* out_admitted);
+
 /* ---------------------------------------------------------------------------------------- */
 /* Device entry points                                                                       */
 /* ---------------------------------------------------------------------------------------- */

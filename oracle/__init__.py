@@ -238,6 +238,74 @@ def merge(o_parts, lse_parts):
     return out, float(lse.value)
 
 
+def peek_match(children, seq):
+    """Longest cached prefix of `seq` by walking the tree from the root, changing nothing.
+
+    `children` maps (parent id, first token of the edge) to a dumped node. Returns the matched
+    length and the path as [(node id, tokens of its edge matched)], root excluded.
+    """
+    cur, pos, path = 0, 0, []
+    while pos < len(seq):
+        c = children.get((cur, int(seq[pos])))
+        if c is None:
+            break
+        key = c["key"]
+        k = 0
+        while k < len(key) and pos + k < len(seq) and key[k] == seq[pos + k]:
+            k += 1
+        path.append((c["id"], k))
+        pos += k
+        if k < len(key):
+            break
+        cur = c["id"]
+    return pos, path
+
+
+def schedule_batch(tree: Tree, seqs, match_lens=None, fcfs: bool = False,
+                   max_batch: int = 1 << 30, max_new_tokens: int = -1, reserve: int = 0):
+    """Cache-aware batch formation, longest shared prefix first (paper digest Sec. 3
+    "cache-aware scheduling" and App. A.2: match every waiting request, sort by match length,
+    admit into the batch while memory allows); `fcfs` keeps queue order instead, the
+    first-come-first-served order the digest contrasts it with.
+
+    Readings: ties keep queue order; admission stops at the first request that does not fit;
+    a request fits while the batch holds at most `max_batch` requests and `max_new_tokens`
+    computed tokens (len - match; negative = no limit), and while free slots plus the cached
+    tokens of unreferenced nodes, less `reserve`, cover the computed tokens plus the set of
+    unreferenced cached tokens the admitted matches lock. Returns (order, match, admitted).
+    """
+    nodes = tree.nodes()
+    children = {(n["parent"], int(n["key"][0])): n for n in nodes}
+    ref = {n["id"]: n["ref"] for n in nodes}
+    match, paths = [], []
+    for w, s in enumerate(seqs):
+        s = _i32(s)
+        lim = len(s) if match_lens is None else int(match_lens[w])
+        m, path = peek_match(children, s[:lim])
+        match.append(m)
+        paths.append(path)
+    order = list(range(len(seqs)))
+    if not fcfs:
+        order.sort(key=lambda w: -match[w])     # stable: ties in queue order
+    room = (tree.pool.available() + sum(len(n["key"]) for n in nodes if n["ref"] == 0)
+            - reserve)
+    locked = set()     # (node id, offset in its edge) of unreferenced cached tokens locked
+    computed = admitted = 0
+    for w in order:
+        if admitted == max_batch:
+            break
+        fresh = len(seqs[w]) - match[w]
+        if max_new_tokens >= 0 and computed + fresh > max_new_tokens:
+            break
+        mine = {(nid, j) for nid, k in paths[w] if ref[nid] == 0 for j in range(k)}
+        if computed + fresh + len(locked | mine) > room:
+            break
+        locked |= mine
+        computed += fresh
+        admitted += 1
+    return order, match, admitted
+
+
 @dataclass
 class BatchResult:
     prefix_len: list = field(default_factory=list)   # matched (reused) tokens per request

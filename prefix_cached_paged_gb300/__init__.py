@@ -16,13 +16,14 @@ import ctypes
 import numpy as np
 
 from ._lib import (RC_DTYPE_BF16, RC_DTYPE_F32, RC_ERR_CUDA, RC_ERR_DEVICE, RC_ERR_INSUFFICIENT,
-                   RC_ERR_INVALID, RC_ERR_OOM, RC_OK, RcDecodeArgs, RcError, RcExtendArgs,
-                   RcSlotWriteArgs, RcStats, check, lib)
+                   RC_ERR_INVALID, RC_ERR_OOM, RC_OK, RC_SCHED_FCFS, RC_SCHED_LSPF, RcDecodeArgs,
+                   RcError, RcExtendArgs, RcSlotWriteArgs, RcStats, check, lib)
 
 __all__ = [
     "Pool", "RadixTree", "RcError", "slot_table_write", "extend_attention", "decode_attention",
     "decode_workspace_bytes", "decode_attention_noalloc", "device_status", "launch_count", "RC_OK", "RC_ERR_INVALID",
-    "RC_ERR_OOM", "RC_ERR_INSUFFICIENT", "RC_ERR_CUDA", "RC_ERR_DEVICE",
+    "RC_ERR_OOM", "RC_ERR_INSUFFICIENT", "RC_ERR_CUDA", "RC_ERR_DEVICE", "RC_SCHED_LSPF",
+    "RC_SCHED_FCFS",
 ]
 
 
@@ -139,6 +140,26 @@ class RadixTree:
                                          rows.shape[1], _p(pl), _p(nodes)),
               "rc_radix_match_batch")
         return pl, nodes
+
+    def schedule_batch(self, tokens: np.ndarray, indptr: np.ndarray, match_len=None,
+                       policy: int = 0, max_batch: int = 1 << 30, max_new_tokens: int = -1,
+                       reserve_slots: int = 0):
+        """Batch formation over W waiting sequences (the tree is not changed); policy
+        RC_SCHED_LSPF (longest shared prefix first) or RC_SCHED_FCFS (queue order). Returns
+        (order int32[W], match int32[W], admitted): the batch is order[:admitted]."""
+        W = len(indptr) - 1
+        order = np.empty(W, dtype=np.int32)
+        match = np.empty(W, dtype=np.int32)
+        adm = ctypes.c_int32()
+        ml = None if match_len is None else _i32(match_len)
+        tok = _i32(tokens)
+        ip = np.ascontiguousarray(indptr, np.int64)
+        check(lib().rc_schedule_batch(self.h, _p(tok), _p(ip), W,
+                                      None if ml is None else _p(ml), int(policy),
+                                      int(max_batch), int(max_new_tokens), int(reserve_slots),
+                                      _p(order), _p(match), ctypes.byref(adm)),
+              "rc_schedule_batch")
+        return order, match, int(adm.value)
 
     def insert_batch(self, tokens, indptr, rows, prefix_len, unlock_nodes, keep_locked=False):
         """Insert B sequences with their slot rows, free duplicates, optionally lock the ends,

@@ -14,6 +14,8 @@ RC_ERR_CUDA = -4
 RC_ERR_DEVICE = -5
 RC_DTYPE_BF16 = 0
 RC_DTYPE_F32 = 1
+RC_SCHED_LSPF = 0
+RC_SCHED_FCFS = 1
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -42,6 +44,8 @@ SIGNATURES = {
     "rc_radix_dump": (_I64, [_P, _P, _I64]),
     "rc_radix_match_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P, _P]),
     "rc_radix_insert_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
+    "rc_schedule_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I64, _I64, _P, _P,
+                                         _P]),
     "rc_slot_table_write": (ctypes.c_int, [_P, _P]),
     "rc_extend_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "rc_extend_attention": (ctypes.c_int, [_P, _P]),

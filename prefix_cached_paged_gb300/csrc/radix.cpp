@@ -58,6 +58,7 @@ struct rc_radix {
   int64_t clock = 0;
   int64_t next_id = 1;
   int64_t cached_tokens = 0;
+  int64_t evictable_tokens = 0;  // tokens in nodes with reference count 0 (root excluded)
   int64_t splits = 0, evicted_nodes = 0, evicted_tokens = 0;
   int64_t matched_tokens = 0, match_queries = 0;
 
@@ -179,6 +180,24 @@ struct rc_radix {
     *out_end = cur;
     return pos;
   }
+  // Longest cached prefix of tokens[0:n] without changing the tree (no split, no stamp).
+  // When `visit` is given it is called with (node index, matched tokens of its edge) for every
+  // node on the matched path, root excluded, from the root down.
+  template <class Visit>
+  int64_t peek(const int32_t* tok, int64_t n, Visit&& visit) const {
+    int32_t cur = 0;
+    int64_t pos = 0;
+    while (pos < n) {
+      const int32_t c = find_child(cur, tok[pos]);
+      if (c < 0) break;
+      const size_t k = common(c, tok, pos, n);
+      visit(c, (int64_t)k);
+      pos += (int64_t)k;
+      if (k < nodes[(size_t)c].key.size()) break;
+      cur = c;
+    }
+    return pos;
+  }
   int64_t insert(const int32_t* tok, const int32_t* slots, int64_t n, int32_t* out_end) {
     int32_t cur = 0;
     int64_t pos = 0;
@@ -194,6 +213,7 @@ struct rc_radix {
         nodes[(size_t)cur].nchildren += 1;
         if (cur != 0) lru_refresh(cur);
         cached_tokens += n - pos;
+        evictable_tokens += n - pos;
         cur = leaf;
         break;
       }
@@ -210,7 +230,10 @@ struct rc_radix {
   int lock(int32_t i) {
     for (int32_t x = i; x != 0; x = nodes[(size_t)x].parent) {
       Node& n = nodes[(size_t)x];
-      if (++n.ref == 1) lru_out(x);
+      if (++n.ref == 1) {
+        lru_out(x);
+        evictable_tokens -= (int64_t)n.key.size();
+      }
     }
     return RC_OK;
   }
@@ -221,7 +244,10 @@ struct rc_radix {
                     (long long)nodes[(size_t)x].id);
     for (int32_t x = i; x != 0; x = nodes[(size_t)x].parent) {
       Node& n = nodes[(size_t)x];
-      if (--n.ref == 0) lru_refresh(x);
+      if (--n.ref == 0) {
+        evictable_tokens += (int64_t)n.key.size();
+        lru_refresh(x);
+      }
     }
     return RC_OK;
   }
@@ -239,6 +265,7 @@ struct rc_radix {
       lru_out(i);
       freed += (int64_t)n.slots.size();
       cached_tokens -= (int64_t)n.slots.size();
+      evictable_tokens -= (int64_t)n.slots.size();
       evicted_tokens += (int64_t)n.slots.size();
       evicted_nodes++;
       const int32_t par = n.parent;
@@ -427,6 +454,67 @@ int rc_radix_insert_batch(rc_radix* t, const int32_t* tokens, const int64_t* ind
     }
   }
   if (out_freed) *out_freed = freed;
+  return RC_OK;
+}
+
+int rc_schedule_batch(const rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                      const int32_t* match_len, int32_t policy, int32_t max_batch,
+                      int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
+                      int32_t* out_match, int32_t* out_admitted) {
+  RC_CHECK_ARG(t && out_admitted && B >= 0 && max_batch >= 0 && reserve_slots >= 0 &&
+                   (policy == RC_SCHED_LSPF || policy == RC_SCHED_FCFS) &&
+                   (B == 0 || (tokens && indptr && out_order && out_match)),
+               "rc_schedule_batch: bad argument");
+  for (int32_t w = 0; w < B; ++w) {
+    const int64_t len = indptr[w + 1] - indptr[w];
+    const int64_t n = match_len ? (int64_t)match_len[w] : len;
+    RC_CHECK_ARG(indptr[w] >= 0 && len >= 0 && n >= 0 && n <= len,
+                 "rc_schedule_batch: sequence %d: length %lld, match %lld", w, (long long)len,
+                 (long long)n);
+  }
+  auto seq = [&](int32_t w) { return tokens + indptr[w]; };
+  auto lim = [&](int32_t w) {
+    return match_len ? (int64_t)match_len[w] : indptr[w + 1] - indptr[w];
+  };
+  for (int32_t w = 0; w < B; ++w)
+    out_match[w] = (int32_t)t->peek(seq(w), lim(w), [](int32_t, int64_t) {});
+  for (int32_t w = 0; w < B; ++w) out_order[w] = w;
+  if (policy == RC_SCHED_LSPF)
+    std::stable_sort(out_order, out_order + B,
+                     [&](int32_t a, int32_t b) { return out_match[a] > out_match[b]; });
+  // Room: free slots plus every cached token in an unreferenced node (all of them can be
+  // evicted, leaves first), minus the reserve. An admitted sequence takes its computed tokens
+  // and locks its match, which takes the unreferenced cached tokens on that path out of the
+  // evictable room (each counted once across the batch).
+  int64_t free_slots = 0;
+  rc_kv_pool_available(t->pool, &free_slots);
+  const int64_t room = free_slots + t->evictable_tokens - reserve_slots;
+  std::unordered_map<int32_t, int64_t> held;  // node index -> protected prefix of its edge
+  std::vector<std::pair<int32_t, int64_t>> ups;
+  int64_t used = 0, computed = 0;
+  int32_t admitted = 0;
+  for (int32_t i = 0; i < B && admitted < max_batch; ++i) {
+    const int32_t w = out_order[i];
+    const int64_t fresh = indptr[w + 1] - indptr[w] - out_match[w];
+    if (max_new_tokens >= 0 && computed + fresh > max_new_tokens) break;
+    int64_t locked = 0;
+    ups.clear();
+    t->peek(seq(w), lim(w), [&](int32_t c, int64_t k) {
+      if (t->nodes[(size_t)c].ref != 0) return;
+      auto it = held.find(c);
+      const int64_t have = it == held.end() ? 0 : it->second;
+      if (k > have) {
+        locked += k - have;
+        ups.emplace_back(c, k);
+      }
+    });
+    if (used + fresh + locked > room) break;
+    used += fresh + locked;
+    computed += fresh;
+    for (const auto& u : ups) held[u.first] = u.second;
+    ++admitted;
+  }
+  *out_admitted = admitted;
   return RC_OK;
 }
 

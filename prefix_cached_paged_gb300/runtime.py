@@ -4,6 +4,8 @@
 Sec. 2.3: traverse, reuse, compute, insert; LRU eviction when the pool runs short; paper digest
 App. A.2 batch formation):
 
+  schedule: pick the next batch from a waiting queue, longest cached prefix first, as much as
+          the pool can take (rc_schedule_batch; paper digest Sec. 3 cache-aware scheduling);
   plan:   match every sequence (all but its last token; all of it for a cache fill) and lock the
           matched node (rc_radix_match_batch); if fewer slots are free than the batch needs,
           evict LRU leaves for the shortfall (rc_radix_evict_lru); allocate the unmatched
@@ -20,7 +22,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import RC_OK, Pool, RadixTree, RcError
+from . import RC_OK, RC_SCHED_LSPF, Pool, RadixTree, RcError
 
 
 @dataclass
@@ -92,6 +94,25 @@ class HostCache:
         plan.out_loc = new[: qo[-1]]
         plan.extra = new[qo[-1]:]
         return plan
+
+    def schedule(self, waiting, max_batch: int = 1 << 30, max_new_tokens: int = -1,
+                 reserve: int = 0, policy: int = RC_SCHED_LSPF):
+        """Batch formation (rc_schedule_batch; longest shared prefix first by default) over the
+        waiting sequences, matched like `plan` matches them (all but the last token). Returns
+        the queue positions of the admitted batch, in the order to plan them."""
+        t0 = time.perf_counter()
+        try:
+            seqs = [np.asarray(s, dtype=np.int32) for s in waiting]
+            lengths = np.array([len(s) for s in seqs], dtype=np.int64)
+            indptr = np.zeros(len(seqs) + 1, dtype=np.int64)
+            np.cumsum(lengths, out=indptr[1:])
+            tokens = np.concatenate(seqs) if seqs else np.zeros(0, np.int32)
+            order, _, admitted = self.tree.schedule_batch(
+                tokens, indptr, np.maximum(lengths - 1, 0).astype(np.int32), policy, max_batch,
+                max_new_tokens, reserve)
+            return order[:admitted].tolist()
+        finally:
+            self.host_seconds += time.perf_counter() - t0
 
     def finish(self, plan: Plan, keep_locked: bool = False):
         """Insert, free duplicates, unlock. Returns (end nodes, duplicates freed)."""

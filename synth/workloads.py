@@ -279,6 +279,45 @@ def fork_mixed_step(seed: int = 0, layers: int = 32, pool_slots: int = 300_000,
     return ForkMixed(w, programs, dec, n_forks, suffix_len, seed)
 
 
+@dataclass
+class ProgramQueue:
+    """A waiting queue of extend requests (full sequences, queue order) for batch formation."""
+    workload: Workload
+    seqs: list
+    program: np.ndarray          # program index of each request
+    max_batch: int
+    max_new_tokens: int
+
+
+def program_queue(seed: int = 0, n_programs: int = 24, prefix_len: int = 2000,
+                  n_questions: int = 8, question_len: int = 50, pool_slots: int = 20_000,
+                  max_batch: int = 32, max_new_tokens: int = 16_384) -> ProgramQueue:
+    """Few-shot programs (32 x 128 MHA bf16, 1 layer): each of `n_programs` programs has its own
+    `prefix_len`-token prefix and `n_questions` questions of `question_len` tokens. Requests
+    arrive interleaved, question-major (program 0..n-1 asking question 0, then question 1, ...),
+    into a pool that holds fewer prefixes than there are programs. Per batch at most `max_batch`
+    requests and `max_new_tokens` computed tokens."""
+    m = Model(1, 32, 32, 128, "bf16", seed)
+    taken = set()
+    prefixes = [_first_distinct(seed, tokens(seed, 5000 + p, prefix_len), taken, 6000 + p)
+                for p in range(n_programs)]
+    questions = []
+    for p in range(n_programs):
+        qt = set()
+        questions.append([_first_distinct(seed, tokens(seed, 7000 + p * n_questions + q,
+                                                       question_len),
+                                          qt, 50_000 + p * n_questions + q)
+                          for q in range(n_questions)])
+    seqs, prog = [], []
+    for q in range(n_questions):
+        for p in range(n_programs):
+            seqs.append(np.concatenate([prefixes[p], questions[p][q]]))
+            prog.append(p)
+    w = Workload("program_queue", m, pool_slots, permutation(seed, pool_slots),
+                 max_ctx=_round16(prefix_len + question_len))
+    return ProgramQueue(w, seqs, np.array(prog, np.int32), max_batch, max_new_tokens)
+
+
 CONFIGS = {
     "tiny_extend": tiny_extend,
     "few_shot_extend": few_shot_extend,

@@ -402,3 +402,41 @@ def test_extend_stacking_contract_breach_is_reported():
     torch.cuda.synchronize()
     assert rc.device_status() != 0
     eng.extend_end(b)
+
+
+@pytest.mark.parametrize("policy", ["lspf", "fcfs"])
+def test_program_queue_served_by_the_scheduler(policy):
+    """The program queue (small) served batch by batch: rc_schedule_batch picks each batch, the
+    extend kernel computes it over slots that eviction keeps recycling; every batch's sampled
+    outputs match the oracle, its slot rows and scattered K/V are exact."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    from synth import device as sdev
+    pq = W.program_queue(n_programs=6, prefix_len=200, n_questions=4, question_len=20,
+                         pool_slots=700, max_batch=8, max_new_tokens=1200)
+    w = pq.workload
+    eng = H.make_engine(w, max_reqs=pq.max_batch + 8)
+    pol = rc.RC_SCHED_LSPF if policy == "lspf" else rc.RC_SCHED_FCFS
+    waiting = list(range(len(pq.seqs)))
+    rng = np.random.default_rng(3)
+    batches = evicted = 0
+    while waiting:
+        idx = eng.host.schedule([pq.seqs[i] for i in waiting], pq.max_batch, pq.max_new_tokens,
+                                policy=pol)
+        assert idx
+        seqs = [pq.seqs[waiting[i]] for i in idx]
+        b = eng.extend_begin(seqs)
+        evicted += int(b.plan.evicted)
+        h = H.new_token_hashes(w.model, seqs, b.plan.prefix_len)
+        q, k, v = H.dense_qkv(w.model, sdev.hashes_to_device(h), 0, b.num_tokens)
+        o = torch.empty_like(q)
+        eng.extend_layer(b, 0, q, k, v, o)
+        _check_extend(w, b, {0: (o, None)}, seqs, _sample_units(rng, len(seqs), 1, 32, 6))
+        _check_slot_rows(eng, b)
+        _check_scatter(eng, w, seqs, b, sample=rng.choice(b.num_tokens, 32, replace=False))
+        eng.extend_end(b)
+        for i in sorted(idx, reverse=True):
+            waiting.pop(i)
+        batches += 1
+    assert evicted > 0 and batches > 2
+    _status_clear()

@@ -100,6 +100,129 @@ def test_random_ops_match_oracle_bit_exact(seed):
     assert op_.alloc(n).tolist() == pp.alloc(n).tolist()
 
 
+def _waiting_list(rnd, cached, alpha):
+    """Waiting sequences: extensions of cached sequences (cut at random points) and fresh ones."""
+    out = []
+    for _ in range(rnd.randint(0, 12)):
+        if cached and rnd.random() < 0.7:
+            base = rnd.choice(cached)
+            base = base[:rnd.randint(0, len(base))]
+        else:
+            base = []
+        out.append(base + [rnd.randrange(alpha) for _ in range(rnd.randint(0, 8))])
+    return out
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_schedule_batch_matches_oracle_bit_exact(seed):
+    """rc_schedule_batch against the oracle's scheduler on random tree states (locks, partial
+    edges, a short pool), both policies: same order, matches and admitted count, and the tree
+    unchanged."""
+    rnd = random.Random(5000 + seed)
+    alpha = rnd.choice([2, 3, 6])
+    N = 200
+    order = np.array(rnd.sample(range(N), N), dtype=np.int32)
+    op_ = oracle.Pool(N, order)
+    ot = oracle.Tree(op_)
+    pp = rc.Pool(N, order)
+    pt = rc.RadixTree(pp)
+    locked, cached = [], []
+    compared = admitted_some = 0
+    for step in range(120):
+        r = rnd.random()
+        toks = [rnd.randrange(alpha) for _ in range(rnd.randint(1, 14))]
+        if r < 0.25 and cached:
+            toks = rnd.choice(cached)[:rnd.randint(0, 14)]
+            _, _, id1 = ot.match(toks)
+            _, _, h2 = pt.match_prefix(toks)
+            if rnd.random() < 0.6:
+                ot.lock(id1)
+                pt.lock(h2)
+                locked.append((id1, h2))
+        elif r < 0.6:
+            a1 = op_.alloc(len(toks))
+            if a1 is None:
+                continue
+            a2 = pp.alloc(len(toks))
+            e1, _ = ot.insert(toks, a1)
+            e2, _ = pt.insert(toks, a2)
+            op_.free(a1[:e1])
+            pp.free(a2[:e2])
+            cached.append(toks)
+        elif r < 0.7 and locked:
+            i1, h2 = locked.pop(rnd.randrange(len(locked)))
+            ot.unlock(i1)
+            pt.unlock(h2)
+        elif r < 0.8:
+            want = rnd.randint(0, 30)
+            ot.evict(want)
+            pt.evict_lru(want)
+        else:
+            waiting = _waiting_list(rnd, cached, alpha)
+            mlen = None
+            if waiting and rnd.random() < 0.5:
+                mlen = [max(len(w) - 1, 0) for w in waiting]
+            kw = dict(max_batch=rnd.choice([0, 1, 3, 1 << 30]),
+                      max_new_tokens=rnd.choice([-1, 0, 5, 20]),
+                      reserve=rnd.choice([0, 0, 10, 150]))
+            fcfs = rnd.random() < 0.3
+            o1, m1, a1 = oracle.schedule_batch(ot, waiting, mlen, fcfs, **kw)
+            lens = np.array([len(w) for w in waiting], dtype=np.int64)
+            indptr = np.zeros(len(waiting) + 1, dtype=np.int64)
+            np.cumsum(lens, out=indptr[1:])
+            flat = (np.concatenate([np.array(w, np.int32) for w in waiting]) if waiting
+                    else np.zeros(0, np.int32))
+            o2, m2, a2 = pt.schedule_batch(flat, indptr, mlen,
+                                           rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF,
+                                           kw["max_batch"], kw["max_new_tokens"], kw["reserve"])
+            assert (list(o1), list(m1), a1) == (o2.tolist(), m2.tolist(), a2)
+            compared += 1
+            admitted_some += a2 > 0
+        np.testing.assert_array_equal(ot.dump(), pt.dump())
+    assert compared >= 10 and admitted_some > 0
+
+
+def test_schedule_admission_is_feasible_and_tight():
+    """Planning the admitted batch through the engine's host path never runs out of slots;
+    when admission stopped for room, adding the next request does."""
+    rnd = random.Random(99)
+    stops = 0
+    for trial in range(40):
+        N = rnd.choice([60, 120, 250])
+        hc = runtime.HostCache(N, 64)
+        hc2 = runtime.HostCache(N, 64)
+        cached = []
+        for _ in range(rnd.randint(1, 10)):
+            s = [rnd.randrange(4) for _ in range(rnd.randint(2, 30))]
+            for h in (hc, hc2):
+                try:
+                    h.finish(h.plan([s], match_all=True))
+                except rc.RcError:
+                    break
+            else:
+                cached.append(s)
+        waiting = [w for w in _waiting_list(rnd, cached, 4) if w]
+        if not waiting:
+            continue
+        lens = np.array([len(w) for w in waiting], dtype=np.int64)
+        indptr = np.zeros(len(waiting) + 1, dtype=np.int64)
+        np.cumsum(lens, out=indptr[1:])
+        flat = np.concatenate([np.array(w, np.int32) for w in waiting])
+        mlen = np.maximum(lens - 1, 0).astype(np.int32)
+        policy = rc.RC_SCHED_FCFS if trial % 3 == 0 else rc.RC_SCHED_LSPF
+        order, match, adm = hc.tree.schedule_batch(flat, indptr, mlen, policy)
+        batch = [waiting[w] for w in order[:adm]]
+        if batch:
+            p = hc.plan(batch)
+            assert p.prefix_len.tolist() == [match[w] for w in order[:adm]]
+            hc.finish(p)
+        if adm < len(waiting):
+            stops += 1
+            with pytest.raises(rc.RcError):
+                hc2.plan([waiting[w] for w in order[:adm + 1]])
+    assert stops > 0
+
+
 def test_stale_handles_and_unlock_underflow():
     pool = rc.Pool(20)
     t = rc.RadixTree(pool)
@@ -279,3 +402,62 @@ def test_stacking_policy_on_the_measured_workloads():
     assert not stacking_pays([1500] * 5, [200] * 5, 1500, 1)
     v = np.random.default_rng(0).integers(1, 99, 64)
     assert not stacking_pays(1000 + v, (100 - v) + 20, 1000, 8)
+
+
+def _serve_queue_product(pq, policy):
+    """Serve the whole queue batch by batch through the product's host path."""
+    w = pq.workload
+    hc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order)
+    waiting = list(range(len(pq.seqs)))
+    steps = []
+    while waiting:
+        idx = hc.schedule([pq.seqs[i] for i in waiting], pq.max_batch, pq.max_new_tokens,
+                          policy=policy)
+        assert idx, "no progress"
+        ids = [waiting[i] for i in idx]
+        p = hc.plan([pq.seqs[i] for i in ids])
+        steps.append((ids, p.prefix_len.tolist(), int(p.evicted)))
+        hc.finish(p)
+        for i in sorted(idx, reverse=True):
+            waiting.pop(i)
+    return steps
+
+
+def _serve_queue_oracle(pq, fcfs):
+    w = pq.workload
+    sim = oracle.CacheSim(w.pool_slots, w.pool_order)
+    waiting = list(range(len(pq.seqs)))
+    steps = []
+    while waiting:
+        seqs = [pq.seqs[i] for i in waiting]
+        order, _, adm = oracle.schedule_batch(sim.tree, seqs, [len(s) - 1 for s in seqs], fcfs,
+                                              pq.max_batch, pq.max_new_tokens)
+        assert adm > 0, "no progress"
+        ids = [waiting[i] for i in order[:adm]]
+        batch = [pq.seqs[i] for i in ids]
+        res = sim.extend_prepare(batch)
+        steps.append((ids, list(res.prefix_len), int(res.evicted)))
+        sim.extend_finish(batch, res)
+        for i in sorted(order[:adm], reverse=True):
+            waiting.pop(i)
+    return steps
+
+
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_program_queue_schedules_match_oracle(size):
+    """The program queue served under both policies: the same batches, matches and evictions
+    as the oracle's loop, and longest-shared-prefix-first computes far fewer tokens."""
+    if size == "small":
+        pq = W.program_queue(n_programs=6, prefix_len=200, n_questions=4, question_len=20,
+                             pool_slots=700, max_batch=8, max_new_tokens=1200)
+    else:
+        pq = W.program_queue()
+    computed = {}
+    for policy, fcfs in ((rc.RC_SCHED_LSPF, False), (rc.RC_SCHED_FCFS, True)):
+        a = _serve_queue_product(pq, policy)
+        b = _serve_queue_oracle(pq, fcfs)
+        assert a == b
+        served = sorted(i for ids, _, _ in a for i in ids)
+        assert served == list(range(len(pq.seqs)))
+        computed[fcfs] = sum(len(pq.seqs[i]) - p for ids, pl, _ in a for i, p in zip(ids, pl))
+    assert computed[False] < 0.5 * computed[True]
