@@ -291,13 +291,15 @@ class ProgramQueue:
 
 def program_queue(seed: int = 0, n_programs: int = 24, prefix_len: int = 2000,
                   n_questions: int = 8, question_len: int = 50, pool_slots: int = 20_000,
-                  max_batch: int = 32, max_new_tokens: int = 16_384) -> ProgramQueue:
+                  max_batch: int = 32, max_new_tokens: int = 16_384, layers: int = 1,
+                  shared: bool = True) -> ProgramQueue:
     """Few-shot programs (32 x 128 MHA bf16, 1 layer): each of `n_programs` programs has its own
     `prefix_len`-token prefix and `n_questions` questions of `question_len` tokens. Requests
     arrive interleaved, question-major (program 0..n-1 asking question 0, then question 1, ...),
     into a pool that holds fewer prefixes than there are programs. Per batch at most `max_batch`
-    requests and `max_new_tokens` computed tokens."""
-    m = Model(1, 32, 32, 128, "bf16", seed)
+    requests and `max_new_tokens` computed tokens. `shared=False` is the no-reuse twin: the same
+    lengths and order, but every request has a prefix of its own."""
+    m = Model(layers, 32, 32, 128, "bf16", seed)
     taken = set()
     prefixes = [_first_distinct(seed, tokens(seed, 5000 + p, prefix_len), taken, 6000 + p)
                 for p in range(n_programs)]
@@ -311,7 +313,11 @@ def program_queue(seed: int = 0, n_programs: int = 24, prefix_len: int = 2000,
     seqs, prog = [], []
     for q in range(n_questions):
         for p in range(n_programs):
-            seqs.append(np.concatenate([prefixes[p], questions[p][q]]))
+            pre = prefixes[p]
+            if not shared:
+                pre = _first_distinct(seed, tokens(seed, 90_000 + len(seqs), prefix_len), taken,
+                                      190_000 + len(seqs))
+            seqs.append(np.concatenate([pre, questions[p][q]]))
             prog.append(p)
     w = Workload("program_queue", m, pool_slots, permutation(seed, pool_slots),
                  max_ctx=_round16(prefix_len + question_len))
