@@ -120,6 +120,10 @@ typedef struct rc_stats {
   int64_t evicted_tokens;
   int64_t matched_tokens;    /* sum of match lengths (prefill tokens skipped) */
   int64_t match_queries;     /* sum of query lengths given to match */
+  int64_t host_tokens;       /* tokens held in the host tier */
+  int64_t spilled_tokens;    /* evicted device tokens moved to the host tier */
+  int64_t loaded_tokens;     /* host-tier tokens moved back to the device */
+  int64_t dropped_tokens;    /* tokens that left a tree with a host tier altogether */
 } rc_stats;
 int rc_radix_stats(const rc_radix* tree, rc_stats* out);
 
@@ -147,6 +151,45 @@ int rc_radix_insert_batch(rc_radix* tree, const int32_t* tokens, const int64_t* 
                           const int32_t* rows, int64_t row_stride, const int32_t* prefix_len,
                           const rc_node* unlock_nodes, int32_t keep_locked, rc_node* end_nodes,
                           int64_t* out_freed);
+
+/* Host tier (SGLang blog Sec. 6.1 HiCache: GPU memory holds the hottest KV, host memory the next
+ * tier). With a host pool attached, rc_radix_evict_lru moves each least-recently-used device
+ * leaf to host slots instead of freeing it: the node keeps its place in the tree and becomes
+ * host-resident. Device-resident nodes always form the part of the tree that contains the root
+ * (a device leaf = device-resident, unreferenced, no device-resident child). To make room in the
+ * host pool, unreferenced host nodes without children are dropped, least recently used first
+ * (smallest (stamp, node id)); a victim the host tier cannot take even then is freed. Host slots
+ * index the caller's host KV planes exactly as device slots index the device planes.
+ *
+ * The tree records the copies this implies and the caller performs them before any later device
+ * work writes a recycled slot: spills (device slot -> host slot) first, then loads (host slot ->
+ * device slot), in one stream. rc_radix_pending_copies counts them; rc_radix_drain_copies hands
+ * them out (buffers sized by the counts) and forgets them. Eviction is refused (RC_ERR_INVALID)
+ * while loads are pending.
+ *
+ * The single-sequence match, rc_radix_match_batch and rc_schedule_batch see device-resident
+ * tokens only (a walk stops at the first host-resident node). rc_radix_match_batch_tiered
+ * continues through host-resident nodes: prefix_len[b] = the device-resident part (its slots in
+ * rows), host_len[b] = the host-resident tokens after it; the lock covers both. After making
+ * room for sum(host_len) device slots, rc_radix_load_batch moves those nodes back to the device
+ * (device slots from the pool in request and token order; the host slots return to the host
+ * pool when the copies are drained), writes their slots to rows[b, prefix_len[b]:...] and adds
+ * host_len[b] to prefix_len[b]. RC_ERR_OOM if fewer device slots are free than sum(host_len).
+ * An insert through host-resident tokens gives them the caller's slots (the node returns to the
+ * device) and counts only the leading device-resident tokens as already present.
+ * rc_radix_tiers writes (node id, 1 if host-resident) per node in the dump's order. */
+int rc_radix_attach_host_tier(rc_radix* tree, rc_pool* host_pool);
+int rc_radix_match_batch_tiered(rc_radix* tree, const int32_t* tokens, const int64_t* indptr,
+                                int32_t B, const int32_t* match_len, int32_t* rows,
+                                int64_t row_stride, int32_t* prefix_len, rc_node* nodes,
+                                int32_t* host_len);
+int rc_radix_load_batch(rc_radix* tree, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                        int32_t* rows, int64_t row_stride, int32_t* prefix_len,
+                        const int32_t* host_len);
+int rc_radix_pending_copies(const rc_radix* tree, int64_t* n_spill, int64_t* n_load);
+int rc_radix_drain_copies(rc_radix* tree, int32_t* spill_dev, int32_t* spill_host,
+                          int32_t* load_host, int32_t* load_dev);
+int64_t rc_radix_tiers(const rc_radix* tree, int64_t* buf, int64_t cap);
 
 /* Cache-aware batch formation (paper digest Sec. 3 "cache-aware scheduling": order the waiting
  * requests longest shared prefix first rather than first come first served; its Theorem 3.1

@@ -74,6 +74,14 @@ def lib():
         L.or_attention_units.argtypes = [_I64, _P, _P, _P, _P, _P, _I64, _I64, _I64,
                                          ctypes.c_double, _P, _I64]
         L.or_merge.argtypes = [_P, _P, _I64, _I64, _P, _P]
+        L.or_attach_host.argtypes = [_P, _P]
+        L.or_match_tiered.argtypes = [_P, _P, _I64, _P, _P, _P, _P]
+        L.or_load.restype = ctypes.c_int
+        L.or_load.argtypes = [_P, _P, _I64, _P]
+        L.or_pending.argtypes = [_P, _P, _P]
+        L.or_drain.argtypes = [_P, _P, _P, _P, _P]
+        L.or_tiers.restype = _I64
+        L.or_tiers.argtypes = [_P, _P, _I64]
         _lib = L
     return _lib
 
@@ -152,6 +160,48 @@ class Tree:
         if rc != 0:
             raise KeyError((node, rc))
 
+    def attach_host(self, host_pool: Pool) -> None:
+        """Evicted device leaves move to the host tier's slots instead of being freed."""
+        self.host_pool = host_pool
+        lib().or_attach_host(self.h, host_pool.h)
+
+    def match_tiered(self, tokens):
+        """Match through both tiers: (device-resident length, host-resident length after it,
+        device slots, node id)."""
+        t = _i32(tokens)
+        slots = np.empty(len(t), dtype=np.int32)
+        dev, host, node = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        lib().or_match_tiered(self.h, _ptr(t), len(t), _ptr(slots), ctypes.byref(dev),
+                              ctypes.byref(host), ctypes.byref(node))
+        return int(dev.value), int(host.value), slots[: dev.value].copy(), int(node.value)
+
+    def load(self, tokens):
+        """Move the host-resident nodes on the path of `tokens` to the device; returns the
+        path's slots, or None if the device pool is short."""
+        t = _i32(tokens)
+        row = np.empty(len(t), dtype=np.int32)
+        if lib().or_load(self.h, _ptr(t), len(t), _ptr(row)) != 0:
+            return None
+        return row
+
+    def drain(self):
+        """Owed copies since the last drain: (spill_dev, spill_host, load_host, load_dev)."""
+        ns, nl = ctypes.c_int64(), ctypes.c_int64()
+        lib().or_pending(self.h, ctypes.byref(ns), ctypes.byref(nl))
+        out = [np.empty(ns.value, np.int32), np.empty(ns.value, np.int32),
+               np.empty(nl.value, np.int32), np.empty(nl.value, np.int32)]
+        lib().or_drain(self.h, *(_ptr(a) for a in out))
+        return tuple(out)
+
+    def tiers(self) -> np.ndarray:
+        cap = 1 << 16
+        while True:
+            buf = np.empty(cap, dtype=np.int64)
+            n = lib().or_tiers(self.h, _ptr(buf), cap)
+            if n >= 0:
+                return buf[:n].copy()
+            cap = -n
+
     def evict(self, n: int):
         """Evict LRU unreferenced leaves until >= n tokens are freed. Returns (ok, freed, ids)."""
         freed = ctypes.c_int64()
@@ -184,10 +234,11 @@ class Tree:
         return out
 
     def stats(self) -> dict:
-        s = np.zeros(6, dtype=np.int64)
+        s = np.zeros(10, dtype=np.int64)
         lib().or_stats(self.h, _ptr(s))
         keys = ["splits", "evicted_nodes", "evicted_tokens", "nodes", "cached_tokens",
-                "protected_tokens"]
+                "protected_tokens", "host_tokens", "spilled_tokens", "loaded_tokens",
+                "dropped_tokens"]
         return {k: int(v) for k, v in zip(keys, s)}
 
 
@@ -316,6 +367,8 @@ class BatchResult:
     existing: list = field(default_factory=list)     # insert: leading tokens already present
     freed_dups: int = 0                              # duplicate slots returned after insert
     extra_slots: np.ndarray = None                   # slots allocated for decode tokens
+    host_len: list = field(default_factory=list)     # host-tier tokens loaded per request
+    copies: tuple = None                             # (spill_dev, spill_host, load_host, load_dev)
 
 
 class OutOfSlots(RuntimeError):
@@ -333,9 +386,15 @@ class CacheSim:
     inserted, and unlock the matched node.
     """
 
-    def __init__(self, num_slots: int, order=None):
+    def __init__(self, num_slots: int, order=None, host_slots: int = 0, host_order=None):
         self.pool = Pool(num_slots, order)
         self.tree = Tree(self.pool)
+        self.host_pool = None
+        if host_slots:
+            # host tier (SGLang blog Sec. 6.1): evicted leaves move to host slots; a later match
+            # that reaches them loads them back instead of recomputing
+            self.host_pool = Pool(host_slots, host_order)
+            self.tree.attach_host(self.host_pool)
 
     def _make_room(self, need: int, res: BatchResult):
         avail = self.pool.available()
@@ -353,13 +412,26 @@ class CacheSim:
         for s in seqs:
             s = _i32(s)
             lim = len(s) if match_all else len(s) - 1
-            n, slots, node = self.tree.match(s[:max(lim, 0)])
+            if self.host_pool is None:
+                n, slots, node = self.tree.match(s[:max(lim, 0)])
+                h = 0
+            else:
+                n, h, slots, node = self.tree.match_tiered(s[:max(lim, 0)])
             self.tree.lock(node)
             res.prefix_len.append(n)
+            res.host_len.append(h)
             res.rows.append(slots)
             res.nodes.append(node)
+        # device slots for the computed suffixes and for the host-tier tokens to load back
         need = sum(len(s) - p for s, p in zip(seqs, res.prefix_len)) + extra
         self._make_room(need, res)
+        for i, s in enumerate(seqs):
+            if res.host_len[i]:
+                p = res.prefix_len[i] + res.host_len[i]
+                row = self.tree.load(_i32(s)[:p])
+                assert row is not None
+                res.rows[i] = row
+                res.prefix_len[i] = p
         for i, s in enumerate(seqs):
             new = self.pool.alloc(len(s) - res.prefix_len[i])
             assert new is not None
@@ -367,6 +439,8 @@ class CacheSim:
         if extra:
             res.extra_slots = self.pool.alloc(extra)
             assert res.extra_slots is not None
+        if self.host_pool is not None:
+            res.copies = self.tree.drain()
         return res
 
     def extend_finish(self, seqs, res: BatchResult, keep_locked: bool = False) -> list:
@@ -403,4 +477,6 @@ class CacheSim:
             res.nodes.append(node)
         self._make_room(len(contexts), res)
         res.extra_slots = self.pool.alloc(len(contexts))
+        if self.host_pool is not None:
+            res.copies = self.tree.drain()
         return res

@@ -57,6 +57,11 @@ struct Node {
   std::map<int32_t, Node*> children;  // keyed by the first token of the child's edge
   int64_t ref = 0;
   int64_t stamp = 0;
+  bool host = false;  // KV held in host-tier slots
+};
+
+struct Copy {
+  int32_t src, dst;
 };
 
 struct Tree {
@@ -66,6 +71,9 @@ struct Tree {
   int64_t next_id = 1;  // the root has id 0
   std::map<int64_t, Node*> by_id;
   int64_t splits = 0, evicted_nodes = 0, evicted_tokens = 0;
+  Pool* host = nullptr;                     // host tier, or none
+  std::vector<Copy> spills, loads;          // owed copies; a spill with dst -1 is cancelled
+  int64_t host_tokens = 0, spilled = 0, loaded = 0, dropped = 0;
 };
 
 Node* new_node(Tree* t) {
@@ -84,6 +92,7 @@ Node* split(Tree* t, Node* child, size_t k) {
   up->slots.assign(child->slots.begin(), child->slots.begin() + k);
   up->ref = child->ref;
   up->stamp = child->stamp;
+  up->host = child->host;
   child->key.erase(child->key.begin(), child->key.begin() + k);
   child->slots.erase(child->slots.begin(), child->slots.begin() + k);
   child->parent = up;
@@ -97,6 +106,25 @@ void touch_path(Tree* t, Node* last) {
   std::vector<Node*> path;
   for (Node* n = last; n != t->root; n = n->parent) path.push_back(n);
   for (auto it = path.rbegin(); it != path.rend(); ++it) (*it)->stamp = ++t->clock;
+}
+
+// Cancel the owed spill copies that write into any of these host slots.
+void cancel_spills_into(Tree* t, const std::vector<int32_t>& host_slots) {
+  for (Copy& c : t->spills)
+    for (int32_t h : host_slots)
+      if (c.dst == h) c.dst = -1;
+}
+
+bool has_device_child(const Node* x) {
+  for (auto& kv : x->children)
+    if (!kv.second->host) return true;
+  return false;
+}
+
+void remove_leaf(Tree* t, Node* x) {
+  x->parent->children.erase(x->key[0]);
+  t->by_id.erase(x->id);
+  delete x;
 }
 
 void free_node(Tree* t, Node* n) {
@@ -157,7 +185,7 @@ void or_match(void* tv, const int32_t* tok, int64_t n, int32_t* out_slots, int64
   int64_t pos = 0;
   while (pos < n) {
     auto it = cur->children.find(tok[pos]);
-    if (it == cur->children.end()) break;
+    if (it == cur->children.end() || it->second->host) break;
     Node* child = it->second;
     size_t k = 0;
     while (k < child->key.size() && pos + (int64_t)k < n && child->key[k] == tok[pos + k]) ++k;
@@ -179,7 +207,7 @@ void or_insert(void* tv, const int32_t* tok, const int32_t* slots, int64_t n, in
                int64_t* out_node) {
   Tree* t = (Tree*)tv;
   Node* cur = t->root;
-  int64_t pos = 0;
+  int64_t pos = 0, existing = -1;
   while (pos < n) {
     auto it = cur->children.find(tok[pos]);
     if (it == cur->children.end()) {
@@ -189,19 +217,31 @@ void or_insert(void* tv, const int32_t* tok, const int32_t* slots, int64_t n, in
       leaf->slots.assign(slots + pos, slots + n);
       cur->children[tok[pos]] = leaf;
       cur = leaf;
+      if (existing < 0) existing = pos;
+      pos = n;
       break;
     }
     Node* child = it->second;
     size_t k = 0;
     while (k < child->key.size() && pos + (int64_t)k < n && child->key[k] == tok[pos + k]) ++k;
     if (k < child->key.size()) child = split(t, child, k);
+    if (child->host) {
+      // tokens held in the host tier take the caller's slots; the host copy is released
+      if (existing < 0) existing = pos;
+      or_pool_free(t->host, child->slots.data(), (int64_t)child->slots.size());
+      cancel_spills_into(t, child->slots);
+      child->slots.assign(slots + pos, slots + pos + k);
+      child->host = false;
+      t->host_tokens -= (int64_t)k;
+    }
     pos += (int64_t)k;
     cur = child;
   }
   touch_path(t, cur);
   *out_node = cur->id;
-  // the walk stopped either at n (all present) or where the new leaf starts
-  *out_existing = pos;
+  // present = the leading device-resident tokens: the walk stopped at n (all present), at the
+  // first host-resident node, or where the new leaf starts
+  *out_existing = existing >= 0 ? existing : pos;
 }
 
 int or_lock(void* tv, int64_t node_id) {
@@ -227,28 +267,161 @@ int or_evict(void* tv, int64_t n, int64_t* out_freed, int64_t* out_ids, int64_t 
              int64_t* out_nids) {
   Tree* t = (Tree*)tv;
   int64_t freed = 0, nids = 0;
+  if (t->host && !t->loads.empty()) return -2;   // loads owed: drain first
   while (freed < n) {
+    // the least recently used device leaf: device-resident, unreferenced, no device child
     Node* best = nullptr;
     for (auto& kv : t->by_id) {
       Node* x = kv.second;
-      if (x == t->root || x->ref != 0 || !x->children.empty()) continue;
+      if (x == t->root || x->host || x->ref != 0 || has_device_child(x)) continue;
       if (!best || x->stamp < best->stamp || (x->stamp == best->stamp && x->id < best->id))
         best = x;
     }
     if (!best) break;
-    or_pool_free(t->pool, best->slots.data(), (int64_t)best->slots.size());
-    freed += (int64_t)best->slots.size();
+    const int64_t len = (int64_t)best->slots.size();
+    or_pool_free(t->pool, best->slots.data(), len);
+    freed += len;
     if (out_ids && nids < cap) out_ids[nids] = best->id;
     nids++;
-    best->parent->children.erase(best->key[0]);
-    t->by_id.erase(best->id);
     t->evicted_nodes++;
-    t->evicted_tokens += (int64_t)best->slots.size();
-    delete best;
+    t->evicted_tokens += len;
+    if (t->host) {
+      // drop the least recently used host leaves until the host tier can take it
+      while ((int64_t)t->host->free_list.size() < len) {
+        Node* h = nullptr;
+        for (auto& kv : t->by_id) {
+          Node* x = kv.second;
+          if (x == t->root || !x->host || x->ref != 0 || !x->children.empty()) continue;
+          if (!h || x->stamp < h->stamp || (x->stamp == h->stamp && x->id < h->id)) h = x;
+        }
+        if (!h) break;
+        or_pool_free(t->host, h->slots.data(), (int64_t)h->slots.size());
+        cancel_spills_into(t, h->slots);
+        t->host_tokens -= (int64_t)h->slots.size();
+        t->dropped += (int64_t)h->slots.size();
+        remove_leaf(t, h);
+      }
+      if ((int64_t)t->host->free_list.size() >= len) {
+        std::vector<int32_t> hs((size_t)len);
+        or_pool_alloc(t->host, len, hs.data());
+        for (int64_t k = 0; k < len; ++k) t->spills.push_back({best->slots[k], hs[k]});
+        best->slots = hs;
+        best->host = true;
+        t->host_tokens += len;
+        t->spilled += len;
+        continue;
+      }
+      t->dropped += len;   // not even an emptied host tier takes it; it has no child left
+    }
+    remove_leaf(t, best);
   }
   *out_freed = freed;
   if (out_nids) *out_nids = nids;
   return freed >= n ? 0 : -1;
+}
+
+// ----- host tier -----
+void or_attach_host(void* tv, void* host_pool) { ((Tree*)tv)->host = (Pool*)host_pool; }
+
+// Match through both tiers: *out_dev = device-resident tokens matched (their slots written),
+// *out_host = host-resident tokens matched after them; splits where the match ends, stamps the
+// path. *out_node = the node where it ends.
+void or_match_tiered(void* tv, const int32_t* tok, int64_t n, int32_t* out_slots,
+                     int64_t* out_dev, int64_t* out_host, int64_t* out_node) {
+  Tree* t = (Tree*)tv;
+  Node* cur = t->root;
+  int64_t pos = 0, dev = 0;
+  while (pos < n) {
+    auto it = cur->children.find(tok[pos]);
+    if (it == cur->children.end()) break;
+    Node* child = it->second;
+    size_t k = 0;
+    while (k < child->key.size() && pos + (int64_t)k < n && child->key[k] == tok[pos + k]) ++k;
+    const bool ends_inside = k < child->key.size();
+    if (ends_inside) child = split(t, child, k);
+    if (!child->host) {
+      for (size_t i = 0; i < k; ++i) out_slots[pos + i] = child->slots[i];
+      dev = pos + (int64_t)k;
+    }
+    pos += (int64_t)k;
+    cur = child;
+    if (ends_inside) break;
+  }
+  touch_path(t, cur);
+  *out_dev = dev;
+  *out_host = pos - dev;
+  *out_node = cur->id;
+}
+
+// Move the host-resident nodes on the path of tok[0:n] back to the device: fresh device slots
+// per node (token order), a load copy per token; the host slots are released at the drain.
+// Writes the path's slots to row[0:n]. Returns 0, or -1 if the device pool is short.
+int or_load(void* tv, const int32_t* tok, int64_t n, int32_t* row) {
+  Tree* t = (Tree*)tv;
+  Node* cur = t->root;
+  int64_t pos = 0;
+  while (pos < n) {
+    Node* child = cur->children.at(tok[pos]);
+    const int64_t len = (int64_t)child->key.size();
+    if (child->host) {
+      std::vector<int32_t> ds((size_t)len);
+      if (or_pool_alloc(t->pool, len, ds.data()) != 0) return -1;
+      for (int64_t k = 0; k < len; ++k) t->loads.push_back({child->slots[k], ds[k]});
+      child->slots = ds;
+      child->host = false;
+      t->host_tokens -= len;
+      t->loaded += len;
+    }
+    for (int64_t k = 0; k < len; ++k) row[pos + k] = child->slots[k];
+    pos += len;
+    cur = child;
+  }
+  return 0;
+}
+
+void or_pending(void* tv, int64_t* n_spill, int64_t* n_load) {
+  Tree* t = (Tree*)tv;
+  int64_t ns = 0;
+  for (const Copy& c : t->spills) ns += c.dst >= 0;
+  *n_spill = ns;
+  *n_load = (int64_t)t->loads.size();
+}
+
+void or_drain(void* tv, int32_t* sd, int32_t* sh, int32_t* lh, int32_t* ld) {
+  Tree* t = (Tree*)tv;
+  int64_t w = 0;
+  for (const Copy& c : t->spills)
+    if (c.dst >= 0) {
+      sd[w] = c.src;
+      sh[w] = c.dst;
+      ++w;
+    }
+  for (size_t i = 0; i < t->loads.size(); ++i) {
+    lh[i] = t->loads[i].src;
+    ld[i] = t->loads[i].dst;
+    or_pool_free(t->host, &t->loads[i].src, 1);
+  }
+  t->spills.clear();
+  t->loads.clear();
+}
+
+// (id, 1 if host-resident) per node, in the dump's order.
+int64_t or_tiers(void* tv, int64_t* buf, int64_t cap) {
+  Tree* t = (Tree*)tv;
+  std::vector<int64_t> out;
+  std::vector<Node*> stack;
+  for (auto it = t->root->children.rbegin(); it != t->root->children.rend(); ++it)
+    stack.push_back(it->second);
+  while (!stack.empty()) {
+    Node* x = stack.back();
+    stack.pop_back();
+    out.push_back(x->id);
+    out.push_back(x->host ? 1 : 0);
+    for (auto it = x->children.rbegin(); it != x->children.rend(); ++it) stack.push_back(it->second);
+  }
+  if ((int64_t)out.size() > cap) return -(int64_t)out.size();
+  std::memcpy(buf, out.data(), out.size() * sizeof(int64_t));
+  return (int64_t)out.size();
 }
 
 // Canonical dump: depth-first, children in ascending first-token order. Per node (root excluded):
@@ -278,13 +451,15 @@ int64_t or_dump(void* tv, int64_t* buf, int64_t cap) {
 }
 
 // counters: [splits, evicted_nodes, evicted_tokens, node_count (excl. root), cached_tokens,
-//            protected_tokens (ref > 0)]
+//            protected_tokens (ref > 0), host_tokens, spilled, loaded, dropped]; cached and
+//            protected count device-resident nodes only
 void or_stats(void* tv, int64_t* out) {
   Tree* t = (Tree*)tv;
   int64_t nodes = 0, cached = 0, prot = 0;
   for (auto& kv : t->by_id) {
     if (kv.second == t->root) continue;
     nodes++;
+    if (kv.second->host) continue;
     cached += (int64_t)kv.second->key.size();
     if (kv.second->ref > 0) prot += (int64_t)kv.second->key.size();
   }
@@ -294,6 +469,10 @@ void or_stats(void* tv, int64_t* out) {
   out[3] = nodes;
   out[4] = cached;
   out[5] = prot;
+  out[6] = t->host_tokens;
+  out[7] = t->spilled;
+  out[8] = t->loaded;
+  out[9] = t->dropped;
 }
 
 // ----- attention -----

@@ -141,6 +141,57 @@ class RadixTree:
               "rc_radix_match_batch")
         return pl, nodes
 
+    def attach_host_tier(self, host_pool: "Pool") -> None:
+        """Evicted device leaves move to host_pool's slots instead of being freed."""
+        check(lib().rc_radix_attach_host_tier(self.h, host_pool.h), "rc_radix_attach_host_tier")
+        self.host_pool = host_pool
+
+    def match_batch_tiered(self, tokens, indptr, match_len, rows):
+        """Match + lock B sequences through both tiers. Returns (prefix_len int32[B] = the
+        device-resident part, nodes uint64[B], host_len int32[B])."""
+        B = len(indptr) - 1
+        pl = np.empty(B, dtype=np.int32)
+        nodes = np.empty(B, dtype=np.uint64)
+        hl = np.empty(B, dtype=np.int32)
+        ml = None if match_len is None else _i32(match_len)
+        check(lib().rc_radix_match_batch_tiered(self.h, _p(tokens), _p(indptr), B,
+                                                None if ml is None else _p(ml), _p(rows),
+                                                rows.shape[1], _p(pl), _p(nodes), _p(hl)),
+              "rc_radix_match_batch_tiered")
+        return pl, nodes, hl
+
+    def load_batch(self, tokens, indptr, rows, prefix_len, host_len) -> None:
+        """Move the matched host-resident tokens back to the device; prefix_len (int32, in
+        place) grows by host_len and rows receive the new device slots."""
+        assert prefix_len.dtype == np.int32 and prefix_len.flags.c_contiguous
+        hl = _i32(host_len)
+        check(lib().rc_radix_load_batch(self.h, _p(tokens), _p(indptr), len(indptr) - 1,
+                                        _p(rows), rows.shape[1], _p(prefix_len), _p(hl)),
+              "rc_radix_load_batch")
+
+    def drain_copies(self):
+        """The copies owed since the last drain: (spill_dev, spill_host, load_host, load_dev),
+        spills to run before loads."""
+        ns, nl = ctypes.c_int64(), ctypes.c_int64()
+        check(lib().rc_radix_pending_copies(self.h, ctypes.byref(ns), ctypes.byref(nl)),
+              "rc_radix_pending_copies")
+        sd = np.empty(ns.value, np.int32)
+        sh = np.empty(ns.value, np.int32)
+        lh = np.empty(nl.value, np.int32)
+        ld = np.empty(nl.value, np.int32)
+        check(lib().rc_radix_drain_copies(self.h, _p(sd), _p(sh), _p(lh), _p(ld)),
+              "rc_radix_drain_copies")
+        return sd, sh, lh, ld
+
+    def tiers(self) -> np.ndarray:
+        """(node id, 1 if host-resident) per node, in the dump's order."""
+        n = lib().rc_radix_tiers(self.h, None, 0)
+        need = -n if n < 0 else n
+        buf = np.empty(max(need, 1), dtype=np.int64)
+        w = lib().rc_radix_tiers(self.h, _p(buf), need)
+        assert w >= 0
+        return buf[:w]
+
     def schedule_batch(self, tokens: np.ndarray, indptr: np.ndarray, match_len=None,
                        policy: int = 0, max_batch: int = 1 << 30, max_new_tokens: int = -1,
                        reserve_slots: int = 0):

@@ -44,6 +44,12 @@ SIGNATURES = {
     "rc_radix_dump": (_I64, [_P, _P, _I64]),
     "rc_radix_match_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P, _P]),
     "rc_radix_insert_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I64, _P, _P, _I32, _P, _P]),
+    "rc_radix_match_batch_tiered": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I64, _P, _P, _P]),
+    "rc_radix_attach_host_tier": (ctypes.c_int, [_P, _P]),
+    "rc_radix_load_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I64, _P, _P]),
+    "rc_radix_pending_copies": (ctypes.c_int, [_P, _P, _P]),
+    "rc_radix_drain_copies": (ctypes.c_int, [_P, _P, _P, _P, _P]),
+    "rc_radix_tiers": (_I64, [_P, _P, _I64]),
     "rc_schedule_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I64, _I64, _P, _P,
                                          _P]),
     "rc_slot_table_write": (ctypes.c_int, [_P, _P]),
@@ -59,7 +65,9 @@ SIGNATURES = {
 class RcStats(ctypes.Structure):
     _fields_ = [(n, _I64) for n in ("nodes", "cached_tokens", "evictable_tokens",
                                     "protected_tokens", "splits", "evicted_nodes",
-                                    "evicted_tokens", "matched_tokens", "match_queries")]
+                                    "evicted_tokens", "matched_tokens", "match_queries",
+                                    "host_tokens", "spilled_tokens", "loaded_tokens",
+                                    "dropped_tokens")]
 
 
 class RcSlotWriteArgs(ctypes.Structure):

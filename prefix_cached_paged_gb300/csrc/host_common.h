@@ -21,3 +21,8 @@ void count_launches(uint64_t n);
   do {                                              \
     if (!(cond)) return ::rc::fail(RC_ERR_INVALID, __VA_ARGS__); \
   } while (0)
+
+#define RC_CHECK(cond, code, ...)                     \
+  do {                                                \
+    if (!(cond)) return ::rc::fail((code), __VA_ARGS__); \
+  } while (0)

@@ -16,4 +16,5 @@ struct rc_pool {
 namespace rc {
 int pool_take(rc_pool* p, int64_t n, int32_t* out);
 int pool_give(rc_pool* p, const int32_t* slots, int64_t n);
+inline int64_t pool_free_count(const rc_pool* p) { return p->count; }
 }  // namespace rc

@@ -33,8 +33,12 @@ struct Node {
   int32_t parent = -1;
   uint32_t gen = 0;
   bool live = false;
-  bool in_lru = false;
+  bool in_lru = false;    // in the device eviction set
+  bool in_hlru = false;   // in the host eviction set
+  bool host = false;      // KV held in host-tier slots (a tree with a host tier only)
   int32_t nchildren = 0;
+  int32_t ndev = 0;       // device-resident children
+  int64_t pending = -1;   // first pending spill copy of this node (-1: none)
   int64_t id = 0;
   int64_t stamp = 0;
   int64_t ref = 0;
@@ -50,10 +54,16 @@ inline uint64_t child_key(int32_t parent, int32_t tok) {
 
 struct rc_radix {
   rc_pool* pool = nullptr;
+  rc_pool* host_pool = nullptr;  // host tier (NULL: evicted leaves are freed)
   std::vector<Node> nodes;
   std::vector<int32_t> free_idx;
   std::unordered_map<uint64_t, int32_t> child;
-  std::set<std::tuple<int64_t, int64_t, int32_t>> lru;  // (stamp, id, index)
+  std::set<std::tuple<int64_t, int64_t, int32_t>> lru;   // device leaves: (stamp, id, index)
+  std::set<std::tuple<int64_t, int64_t, int32_t>> hlru;  // host leaves
+  // copies the caller owes the pool contents: spills (device slot -> host slot, dst -1 =
+  // cancelled) before loads (host slot -> device slot), drained by rc_radix_drain_copies
+  std::vector<int32_t> spill_src, spill_dst, load_src, load_dst;
+  std::vector<int32_t> spill_node;  // node index of each spill copy
   std::vector<int32_t> path_buf;
   int64_t clock = 0;
   int64_t next_id = 1;
@@ -61,6 +71,7 @@ struct rc_radix {
   int64_t evictable_tokens = 0;  // tokens in nodes with reference count 0 (root excluded)
   int64_t splits = 0, evicted_nodes = 0, evicted_tokens = 0;
   int64_t matched_tokens = 0, match_queries = 0;
+  int64_t host_tokens = 0, spilled_tokens = 0, loaded_tokens = 0, dropped_tokens = 0;
 
   rc_node handle(int32_t idx) const {
     return ((uint64_t)nodes[(size_t)idx].gen << 32) | (uint32_t)idx;
@@ -74,9 +85,15 @@ struct rc_radix {
     if (!n.live || n.gen != gen) return -1;
     return (int32_t)idx;
   }
+  // device leaf: device-resident, unreferenced, no device-resident child
   bool evictable(int32_t i) const {
     const Node& n = nodes[(size_t)i];
-    return i != 0 && n.live && n.ref == 0 && n.nchildren == 0;
+    return i != 0 && n.live && !n.host && n.ref == 0 && n.ndev == 0;
+  }
+  // host leaf: host-resident, unreferenced, no child at all
+  bool host_evictable(int32_t i) const {
+    const Node& n = nodes[(size_t)i];
+    return i != 0 && n.live && n.host && n.ref == 0 && n.nchildren == 0;
   }
   void lru_out(int32_t i) {
     Node& n = nodes[(size_t)i];
@@ -84,15 +101,27 @@ struct rc_radix {
       lru.erase(std::make_tuple(n.stamp, n.id, i));
       n.in_lru = false;
     }
+    if (n.in_hlru) {
+      hlru.erase(std::make_tuple(n.stamp, n.id, i));
+      n.in_hlru = false;
+    }
   }
   void lru_refresh(int32_t i) {
     Node& n = nodes[(size_t)i];
-    const bool want = evictable(i);
-    if (want && !n.in_lru) {
-      lru.emplace(n.stamp, n.id, i);
-      n.in_lru = true;
-    } else if (!want && n.in_lru) {
-      lru_out(i);
+    const bool want = evictable(i), hwant = host_evictable(i);
+    if (want != n.in_lru) {
+      if (want)
+        lru.emplace(n.stamp, n.id, i);
+      else
+        lru.erase(std::make_tuple(n.stamp, n.id, i));
+      n.in_lru = want;
+    }
+    if (hwant != n.in_hlru) {
+      if (hwant)
+        hlru.emplace(n.stamp, n.id, i);
+      else
+        hlru.erase(std::make_tuple(n.stamp, n.id, i));
+      n.in_hlru = hwant;
     }
   }
   int32_t new_node() {
@@ -108,7 +137,11 @@ struct rc_radix {
     n.gen += 1;
     n.live = true;
     n.in_lru = false;
+    n.in_hlru = false;
+    n.host = false;
     n.nchildren = 0;
+    n.ndev = 0;
+    n.pending = -1;
     n.ref = 0;
     n.stamp = 0;
     n.parent = -1;
@@ -131,21 +164,81 @@ struct rc_radix {
     up.slots.assign(lo.slots.begin(), lo.slots.begin() + (std::ptrdiff_t)k);
     up.ref = lo.ref;
     up.stamp = lo.stamp;
+    up.host = lo.host;
     up.nchildren = 1;
+    up.ndev = lo.host ? 0 : 1;
     lo.key.erase(lo.key.begin(), lo.key.begin() + (std::ptrdiff_t)k);
     lo.slots.erase(lo.slots.begin(), lo.slots.begin() + (std::ptrdiff_t)k);
     lo.parent = u;
+    if (lo.pending >= 0) {  // its pending spill copies are in token order: the first k go up
+      up.pending = lo.pending;
+      for (size_t j = 0; j < k; ++j) spill_node[(size_t)up.pending + j] = u;
+      lo.pending += (int64_t)k;
+    }
     child[child_key(up.parent, up.key[0])] = u;
     child[child_key(u, lo.key[0])] = c;
     splits++;
     return u;
+  }
+  // ---------------------------------------------------------------- host tier
+  void cancel_pending(int32_t i) {
+    Node& n = nodes[(size_t)i];
+    if (n.pending < 0) return;
+    for (size_t j = 0; j < n.key.size(); ++j) spill_dst[(size_t)n.pending + j] = -1;
+    n.pending = -1;
+  }
+  // Unlink a childless node (either tier) and recycle its arena entry; slots are the caller's.
+  void unlink(int32_t i) {
+    Node& n = nodes[(size_t)i];
+    lru_out(i);
+    const int32_t par = n.parent;
+    child.erase(child_key(par, n.key[0]));
+    Node& p = nodes[(size_t)par];
+    p.nchildren -= 1;
+    if (!n.host) p.ndev -= 1;
+    n.live = false;
+    n.key.clear();
+    n.key.shrink_to_fit();
+    n.slots.clear();
+    n.slots.shrink_to_fit();
+    free_idx.push_back(i);
+    if (par != 0) lru_refresh(par);
+  }
+  // Drop the least recently used host leaf.
+  void drop_host_leaf() {
+    const int32_t i = std::get<2>(*hlru.begin());
+    Node& n = nodes[(size_t)i];
+    const int64_t len = (int64_t)n.slots.size();
+    cancel_pending(i);
+    rc::pool_give(host_pool, n.slots.data(), len);
+    host_tokens -= len;
+    dropped_tokens += len;
+    unlink(i);
+  }
+  // Host-resident node i becomes device-resident with device slots dev[0:len]; its host slots
+  // are released now (release_now) or after the pending copies are drained (a load reads them).
+  void to_device(int32_t i, const int32_t* dev, bool release_now) {
+    Node& n = nodes[(size_t)i];
+    const size_t len = n.key.size();
+    if (release_now) {
+      cancel_pending(i);
+      rc::pool_give(host_pool, n.slots.data(), (int64_t)len);
+    }
+    n.slots.assign(dev, dev + len);
+    n.host = false;
+    host_tokens -= (int64_t)len;
+    cached_tokens += (int64_t)len;
+    if (n.ref == 0) evictable_tokens += (int64_t)len;
+    nodes[(size_t)n.parent].ndev += 1;
+    lru_refresh(i);
+    if (n.parent != 0) lru_refresh(n.parent);
   }
   void touch_path(int32_t end) {
     path_buf.clear();
     for (int32_t x = end; x != 0; x = nodes[(size_t)x].parent) path_buf.push_back(x);
     for (auto it = path_buf.rbegin(); it != path_buf.rend(); ++it) {
       const int32_t x = *it;
-      const bool was = nodes[(size_t)x].in_lru;
+      const bool was = nodes[(size_t)x].in_lru || nodes[(size_t)x].in_hlru;
       if (was) lru_out(x);
       nodes[(size_t)x].stamp = ++clock;
       if (was) lru_refresh(x);
@@ -159,12 +252,25 @@ struct rc_radix {
     while (k < lim && nd.key[k] == tok[pos + (int64_t)k]) ++k;
     return k;
   }
-  int64_t match(const int32_t* tok, int64_t n, int32_t* out_slots, int32_t* out_end) {
+  // Longest device-resident cached prefix (with host_len: continue through host-resident nodes,
+  // whose tokens are counted in *host_len and whose slots are not written).
+  int64_t match(const int32_t* tok, int64_t n, int32_t* out_slots, int32_t* out_end,
+                int64_t* host_len = nullptr) {
     int32_t cur = 0;
-    int64_t pos = 0;
-    while (pos < n) {
-      int32_t c = find_child(cur, tok[pos]);
+    int64_t pos = 0, hpos = 0;
+    while (pos + hpos < n) {
+      int32_t c = find_child(cur, tok[pos + hpos]);
       if (c < 0) break;
+      if (nodes[(size_t)c].host) {
+        if (!host_len) break;
+        const size_t k = common(c, tok, pos + hpos, n);
+        const bool inside = k < nodes[(size_t)c].key.size();
+        if (inside) c = split(c, k);
+        hpos += (int64_t)k;
+        cur = c;
+        if (inside) break;
+        continue;
+      }
       const size_t k = common(c, tok, pos, n);
       const bool inside = k < nodes[(size_t)c].key.size();
       if (inside) c = split(c, k);
@@ -175,7 +281,8 @@ struct rc_radix {
       if (inside) break;
     }
     touch_path(cur);
-    matched_tokens += pos;
+    if (host_len) *host_len = hpos;
+    matched_tokens += pos + hpos;
     match_queries += n;
     *out_end = cur;
     return pos;
@@ -189,7 +296,7 @@ struct rc_radix {
     int64_t pos = 0;
     while (pos < n) {
       const int32_t c = find_child(cur, tok[pos]);
-      if (c < 0) break;
+      if (c < 0 || nodes[(size_t)c].host) break;
       const size_t k = common(c, tok, pos, n);
       visit(c, (int64_t)k);
       pos += (int64_t)k;
@@ -198,9 +305,13 @@ struct rc_radix {
     }
     return pos;
   }
+  // Insert tokens[0:n] with slots[0:n]. Device-resident tokens already present keep their
+  // slots; tokens held by host-resident nodes take the caller's slots (the node returns to the
+  // device, its host slots are freed). Returns the length of the leading device-resident part
+  // that was already present.
   int64_t insert(const int32_t* tok, const int32_t* slots, int64_t n, int32_t* out_end) {
     int32_t cur = 0;
-    int64_t pos = 0;
+    int64_t pos = 0, existing = -1;
     while (pos < n) {
       int32_t c = find_child(cur, tok[pos]);
       if (c < 0) {
@@ -211,28 +322,35 @@ struct rc_radix {
         lf.slots.assign(slots + pos, slots + n);
         child[child_key(cur, tok[pos])] = leaf;
         nodes[(size_t)cur].nchildren += 1;
+        nodes[(size_t)cur].ndev += 1;
         if (cur != 0) lru_refresh(cur);
         cached_tokens += n - pos;
         evictable_tokens += n - pos;
+        if (existing < 0) existing = pos;
         cur = leaf;
+        pos = n;
         break;
       }
       const size_t k = common(c, tok, pos, n);
       if (k < nodes[(size_t)c].key.size()) c = split(c, k);
+      if (nodes[(size_t)c].host) {
+        if (existing < 0) existing = pos;
+        to_device(c, slots + pos, true);
+      }
       pos += (int64_t)k;
       cur = c;
     }
     touch_path(cur);
     if (cur != 0) lru_refresh(cur);
     *out_end = cur;
-    return pos;
+    return existing < 0 ? pos : existing;
   }
   int lock(int32_t i) {
     for (int32_t x = i; x != 0; x = nodes[(size_t)x].parent) {
       Node& n = nodes[(size_t)x];
       if (++n.ref == 1) {
         lru_out(x);
-        evictable_tokens -= (int64_t)n.key.size();
+        if (!n.host) evictable_tokens -= (int64_t)n.key.size();
       }
     }
     return RC_OK;
@@ -245,7 +363,7 @@ struct rc_radix {
     for (int32_t x = i; x != 0; x = nodes[(size_t)x].parent) {
       Node& n = nodes[(size_t)x];
       if (--n.ref == 0) {
-        evictable_tokens += (int64_t)n.key.size();
+        if (!n.host) evictable_tokens += (int64_t)n.key.size();
         lru_refresh(x);
       }
     }
@@ -253,31 +371,51 @@ struct rc_radix {
   }
   int evict(int64_t want, int64_t* freed_out) {
     int64_t freed = 0;
+    if (host_pool && !load_src.empty()) {
+      *freed_out = 0;
+      return fail(RC_ERR_INVALID,
+                  "radix_evict_lru: host-tier loads are pending; drain the copies first");
+    }
     while (freed < want && !lru.empty()) {
       const int32_t i = std::get<2>(*lru.begin());
-      Node& n = nodes[(size_t)i];
-      const int rc = rc::pool_give(pool, n.slots.data(), (int64_t)n.slots.size());
+      const int64_t len = (int64_t)nodes[(size_t)i].slots.size();
+      const int rc = rc::pool_give(pool, nodes[(size_t)i].slots.data(), len);
       if (rc != RC_OK) {
         *freed_out = freed;
         return fail(RC_ERR_INVALID, "radix_evict_lru: node %lld holds slots the pool rejects",
-                    (long long)n.id);
+                    (long long)nodes[(size_t)i].id);
       }
-      lru_out(i);
-      freed += (int64_t)n.slots.size();
-      cached_tokens -= (int64_t)n.slots.size();
-      evictable_tokens -= (int64_t)n.slots.size();
-      evicted_tokens += (int64_t)n.slots.size();
+      freed += len;
+      cached_tokens -= len;
+      evictable_tokens -= len;
+      evicted_tokens += len;
+      if (host_pool) {
+        // make room in the host tier, least recently used host leaves first
+        while (rc::pool_free_count(host_pool) < len && !hlru.empty()) drop_host_leaf();
+        if (rc::pool_free_count(host_pool) >= len) {
+          // spill: the node keeps its place in the tree, its KV moves to host slots
+          Node& n = nodes[(size_t)i];
+          lru_out(i);
+          const size_t at = spill_src.size();
+          spill_src.insert(spill_src.end(), n.slots.begin(), n.slots.end());
+          spill_dst.resize(at + (size_t)len);
+          rc::pool_take(host_pool, len, spill_dst.data() + at);
+          spill_node.insert(spill_node.end(), (size_t)len, i);
+          n.slots.assign(spill_dst.begin() + (std::ptrdiff_t)at, spill_dst.end());
+          n.pending = (int64_t)at;
+          n.host = true;
+          host_tokens += len;
+          spilled_tokens += len;
+          evicted_nodes++;
+          nodes[(size_t)n.parent].ndev -= 1;
+          lru_refresh(i);
+          if (n.parent != 0) lru_refresh(n.parent);
+          continue;
+        }
+        dropped_tokens += len;  // the host tier cannot take it: freed (it has no child left)
+      }
       evicted_nodes++;
-      const int32_t par = n.parent;
-      child.erase(child_key(par, n.key[0]));
-      n.live = false;
-      n.key.clear();
-      n.key.shrink_to_fit();
-      n.slots.clear();
-      n.slots.shrink_to_fit();
-      free_idx.push_back(i);
-      nodes[(size_t)par].nchildren -= 1;
-      if (par != 0) lru_refresh(par);
+      unlink(i);
     }
     *freed_out = freed;
     if (freed < want)
@@ -348,11 +486,17 @@ int rc_radix_stats(const rc_radix* t, rc_stats* s) {
     const Node& n = t->nodes[i];
     if (!n.live) continue;
     s->nodes++;
-    if (n.ref > 0)
+    if (n.host)
+      continue;
+    else if (n.ref > 0)
       s->protected_tokens += (int64_t)n.key.size();
     else
       s->evictable_tokens += (int64_t)n.key.size();
   }
+  s->host_tokens = t->host_tokens;
+  s->spilled_tokens = t->spilled_tokens;
+  s->loaded_tokens = t->loaded_tokens;
+  s->dropped_tokens = t->dropped_tokens;
   s->cached_tokens = t->cached_tokens;
   s->splits = t->splits;
   s->evicted_nodes = t->evicted_nodes;
@@ -395,28 +539,172 @@ int64_t rc_radix_dump(const rc_radix* t, int64_t* buf, int64_t cap) {
   return w;
 }
 
-int rc_radix_match_batch(rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
-                         const int32_t* match_len, int32_t* rows, int64_t row_stride,
-                         int32_t* prefix_len, rc_node* nodes) {
+static int match_batch_impl(rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                            const int32_t* match_len, int32_t* rows, int64_t row_stride,
+                            int32_t* prefix_len, rc_node* nodes, int32_t* host_len,
+                            const char* name) {
   RC_CHECK_ARG(t && B >= 0 && (B == 0 || (tokens && indptr && rows && prefix_len && nodes)),
-               "rc_radix_match_batch: bad argument");
+               "%s: bad argument", name);
   for (int32_t b = 0; b < B; ++b) {
     const int64_t len = indptr[b + 1] - indptr[b];
     const int64_t n = match_len ? (int64_t)match_len[b] : len;
     RC_CHECK_ARG(len >= 0 && n >= 0 && n <= len && len <= row_stride,
-                 "rc_radix_match_batch: request %d: length %lld, match %lld, row %lld", b,
-                 (long long)len, (long long)n, (long long)row_stride);
+                 "%s: request %d: length %lld, match %lld, row %lld", name, b, (long long)len,
+                 (long long)n, (long long)row_stride);
   }
   for (int32_t b = 0; b < B; ++b) {
     const int64_t len = indptr[b + 1] - indptr[b];
     const int64_t n = match_len ? (int64_t)match_len[b] : len;
     int32_t end;
-    const int64_t p = t->match(tokens + indptr[b], n, rows + (int64_t)b * row_stride, &end);
+    int64_t h = 0;
+    const int64_t p = t->match(tokens + indptr[b], n, rows + (int64_t)b * row_stride, &end,
+                               host_len ? &h : nullptr);
     t->lock(end);
     prefix_len[b] = (int32_t)p;
     nodes[b] = t->handle(end);
+    if (host_len) host_len[b] = (int32_t)h;
   }
   return RC_OK;
+}
+
+int rc_radix_match_batch(rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                         const int32_t* match_len, int32_t* rows, int64_t row_stride,
+                         int32_t* prefix_len, rc_node* nodes) {
+  return match_batch_impl(t, tokens, indptr, B, match_len, rows, row_stride, prefix_len, nodes,
+                          nullptr, "rc_radix_match_batch");
+}
+
+int rc_radix_match_batch_tiered(rc_radix* t, const int32_t* tokens, const int64_t* indptr,
+                                int32_t B, const int32_t* match_len, int32_t* rows,
+                                int64_t row_stride, int32_t* prefix_len, rc_node* nodes,
+                                int32_t* host_len) {
+  RC_CHECK_ARG(host_len != nullptr, "rc_radix_match_batch_tiered: host_len is NULL");
+  return match_batch_impl(t, tokens, indptr, B, match_len, rows, row_stride, prefix_len, nodes,
+                          host_len, "rc_radix_match_batch_tiered");
+}
+
+int rc_radix_attach_host_tier(rc_radix* t, rc_pool* host_pool) {
+  RC_CHECK_ARG(t && host_pool && host_pool != t->pool, "rc_radix_attach_host_tier: bad argument");
+  RC_CHECK_ARG(t->host_pool == nullptr, "rc_radix_attach_host_tier: a host tier is attached");
+  t->host_pool = host_pool;
+  return RC_OK;
+}
+
+int rc_radix_load_batch(rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                        int32_t* rows, int64_t row_stride, int32_t* prefix_len,
+                        const int32_t* host_len) {
+  RC_CHECK_ARG(t && t->host_pool && B >= 0 &&
+                   (B == 0 || (tokens && indptr && rows && prefix_len && host_len)),
+               "rc_radix_load_batch: bad argument (or no host tier)");
+  int64_t need = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t len = indptr[b + 1] - indptr[b];
+    RC_CHECK_ARG(prefix_len[b] >= 0 && host_len[b] >= 0 &&
+                     (int64_t)prefix_len[b] + host_len[b] <= len && len <= row_stride,
+                 "rc_radix_load_batch: request %d: bad lengths", b);
+    need += host_len[b];
+  }
+  int64_t avail = rc::pool_free_count(t->pool);
+  RC_CHECK(avail >= need, RC_ERR_OOM,
+           "rc_radix_load_batch: %lld device slots free, up to %lld needed", (long long)avail,
+           (long long)need);
+  std::vector<int32_t> dev;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t* tok = tokens + indptr[b];
+    int32_t* row = rows + (int64_t)b * row_stride;
+    const int64_t end = (int64_t)prefix_len[b] + host_len[b];
+    int32_t cur = 0;
+    int64_t pos = 0;
+    while (pos < end) {
+      const int32_t c = t->find_child(cur, tok[pos]);
+      RC_CHECK(c >= 0, RC_ERR_INVALID, "rc_radix_load_batch: request %d: path gone at %lld", b,
+               (long long)pos);
+      Node& n = t->nodes[(size_t)c];
+      const int64_t len = (int64_t)n.key.size();
+      RC_CHECK(pos + len <= end && t->common(c, tok, pos, end) == (size_t)len, RC_ERR_INVALID,
+               "rc_radix_load_batch: request %d: the matched path changed", b);
+      if (n.host) {
+        RC_CHECK(n.ref > 0, RC_ERR_INVALID,
+                 "rc_radix_load_batch: request %d: host node not locked by its match", b);
+        dev.resize((size_t)len);
+        rc::pool_take(t->pool, len, dev.data());
+        t->load_src.insert(t->load_src.end(), n.slots.begin(), n.slots.end());
+        t->load_dst.insert(t->load_dst.end(), dev.begin(), dev.end());
+        t->loaded_tokens += len;
+        n.pending = -1;  // pending spill copies stay valid: they run before the loads
+        t->to_device(c, dev.data(), false);
+      }
+      if (pos >= prefix_len[b])
+        std::copy(t->nodes[(size_t)c].slots.begin(), t->nodes[(size_t)c].slots.end(), row + pos);
+      pos += len;
+      cur = c;
+    }
+    prefix_len[b] = (int32_t)end;
+  }
+  return RC_OK;
+}
+
+int rc_radix_pending_copies(const rc_radix* t, int64_t* n_spill, int64_t* n_load) {
+  RC_CHECK_ARG(t && n_spill && n_load, "rc_radix_pending_copies: NULL argument");
+  int64_t ns = 0;
+  for (int32_t d : t->spill_dst) ns += d >= 0;
+  *n_spill = ns;
+  *n_load = (int64_t)t->load_src.size();
+  return RC_OK;
+}
+
+int rc_radix_drain_copies(rc_radix* t, int32_t* spill_dev, int32_t* spill_host, int32_t* load_host,
+                          int32_t* load_dev) {
+  RC_CHECK_ARG(t, "rc_radix_drain_copies: tree is NULL");
+  int64_t ns = 0;
+  for (size_t j = 0; j < t->spill_src.size(); ++j) {
+    if (t->spill_dst[j] < 0) continue;
+    RC_CHECK_ARG(spill_dev && spill_host, "rc_radix_drain_copies: NULL spill buffers");
+    spill_dev[ns] = t->spill_src[j];
+    spill_host[ns] = t->spill_dst[j];
+    ++ns;
+  }
+  if (!t->load_src.empty()) {
+    RC_CHECK_ARG(load_host && load_dev, "rc_radix_drain_copies: NULL load buffers");
+    std::copy(t->load_src.begin(), t->load_src.end(), load_host);
+    std::copy(t->load_dst.begin(), t->load_dst.end(), load_dev);
+    // the loads' host slots were held until their copies were handed out
+    const int rc = rc::pool_give(t->host_pool, t->load_src.data(), (int64_t)t->load_src.size());
+    if (rc != RC_OK) return rc;
+  }
+  for (auto& n : t->nodes) n.pending = -1;
+  t->spill_src.clear();
+  t->spill_dst.clear();
+  t->spill_node.clear();
+  t->load_src.clear();
+  t->load_dst.clear();
+  return RC_OK;
+}
+
+int64_t rc_radix_tiers(const rc_radix* t, int64_t* buf, int64_t cap) {
+  if (!t) return 0;
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> kids(t->nodes.size());
+  int64_t need = 0;
+  for (size_t i = 1; i < t->nodes.size(); ++i) {
+    const Node& n = t->nodes[i];
+    if (!n.live) continue;
+    kids[(size_t)n.parent].emplace_back(n.key[0], (int32_t)i);
+    need += 2;
+  }
+  if (need > cap || !buf) return -need;
+  for (auto& k : kids) std::sort(k.begin(), k.end());
+  int64_t w = 0;
+  std::vector<int32_t> stack;
+  for (auto it = kids[0].rbegin(); it != kids[0].rend(); ++it) stack.push_back(it->second);
+  while (!stack.empty()) {
+    const int32_t i = stack.back();
+    stack.pop_back();
+    buf[w++] = t->nodes[(size_t)i].id;
+    buf[w++] = t->nodes[(size_t)i].host ? 1 : 0;
+    for (auto it = kids[(size_t)i].rbegin(); it != kids[(size_t)i].rend(); ++it)
+      stack.push_back(it->second);
+  }
+  return w;
 }
 
 int rc_radix_insert_batch(rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,

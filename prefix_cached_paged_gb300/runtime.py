@@ -38,6 +38,9 @@ class Plan:
     extra: np.ndarray         # int32 [extra], slots allocated after the batch's own
     evict_request: int = 0
     evicted: int = 0
+    host_len: np.ndarray = None   # int32 [B], tokens loaded back from the host tier
+    copies: tuple = None          # host-tier copies owed: (spill_dev, spill_host, load_host,
+                                  # load_dev), spills before loads
 
     @property
     def num_tokens(self) -> int:
@@ -45,10 +48,15 @@ class Plan:
 
 
 class HostCache:
-    def __init__(self, num_slots: int, row_stride: int, initial_order=None):
+    def __init__(self, num_slots: int, row_stride: int, initial_order=None, host_slots: int = 0,
+                 host_order=None):
         self.pool = Pool(num_slots, initial_order)
         self.tree = RadixTree(self.pool)
         self.row_stride = int(row_stride)
+        self.host_pool = None
+        if host_slots:
+            self.host_pool = Pool(host_slots, host_order)
+            self.tree.attach_host_tier(self.host_pool)
 
     def _make_room(self, need: int, plan: Plan, nodes) -> None:
         avail = self.pool.available()
@@ -79,8 +87,18 @@ class HostCache:
         tokens = np.concatenate(seqs) if B else np.zeros(0, np.int32)
         match_len = lengths if match_all else np.maximum(lengths - 1, 0)
         rows = np.zeros((B, self.row_stride), dtype=np.int32)
-        prefix_len, nodes = self.tree.match_batch(tokens, indptr, match_len.astype(np.int32),
-                                                  rows)
+        host_len = None
+        pre = Plan(*(np.zeros(0),) * 9)     # eviction done before a load, if any
+        if self.host_pool is None:
+            prefix_len, nodes = self.tree.match_batch(tokens, indptr,
+                                                      match_len.astype(np.int32), rows)
+        else:
+            prefix_len, nodes, host_len = self.tree.match_batch_tiered(
+                tokens, indptr, match_len.astype(np.int32), rows)
+            if host_len.any():
+                # device room for the suffixes and the host-tier tokens, then load those back
+                self._make_room(int((lengths - prefix_len).sum()) + int(extra), pre, nodes)
+                self.tree.load_batch(tokens, indptr, rows, prefix_len, host_len)
         S = lengths - prefix_len
         qo = np.zeros(B + 1, dtype=np.int32)
         np.cumsum(S, out=qo[1:])
@@ -88,11 +106,16 @@ class HostCache:
                     np.zeros(0, np.int32), np.zeros(0, np.int32))
         need = int(qo[-1]) + int(extra)
         self._make_room(need, plan, nodes)
+        if pre.evict_request:
+            plan.evict_request, plan.evicted = pre.evict_request, pre.evicted
         new = self.pool.alloc(need)
         for b in range(B):
             rows[b, prefix_len[b]:lengths[b]] = new[qo[b]:qo[b + 1]]
         plan.out_loc = new[: qo[-1]]
         plan.extra = new[qo[-1]:]
+        if self.host_pool is not None:
+            plan.host_len = host_len
+            plan.copies = self.tree.drain_copies()
         return plan
 
     def schedule(self, waiting, max_batch: int = 1 << 30, max_new_tokens: int = -1,
@@ -129,6 +152,8 @@ class HostCache:
         self._make_room(n, p, [])
         out = self.pool.alloc(n)
         self.last_alloc_evicted = p.evicted
+        self.last_alloc_copies = (self.tree.drain_copies() if self.host_pool is not None
+                                  else None)
         return out
 
 

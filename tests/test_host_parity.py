@@ -461,3 +461,99 @@ def test_program_queue_schedules_match_oracle(size):
         assert served == list(range(len(pq.seqs)))
         computed[fcfs] = sum(len(pq.seqs[i]) - p for ids, pl, _ in a for i, p in zip(ids, pl))
     assert computed[False] < 0.5 * computed[True]
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_host_tier_random_ops_match_oracle_bit_exact(seed):
+    """A tree with a host tier against the oracle's: random matches (device-only and through
+    both tiers, with loads), inserts, locks, evictions that spill and drop, and drains; the
+    same dumps, tiers, pool contents, owed copies and counters after every step."""
+    rnd = random.Random(9000 + seed)
+    alpha = rnd.choice([2, 3, 5])
+    N, NH = rnd.choice([(120, 60), (200, 150), (80, 400), (100, 25)])
+    order = np.array(rnd.sample(range(N), N), dtype=np.int32)
+    horder = np.array(rnd.sample(range(NH), NH), dtype=np.int32)
+    op_, oh = oracle.Pool(N, order), oracle.Pool(NH, horder)
+    ot = oracle.Tree(op_)
+    ot.attach_host(oh)
+    pp, ph = rc.Pool(N, order), rc.Pool(NH, horder)
+    pt = rc.RadixTree(pp)
+    pt.attach_host_tier(ph)
+    locked, cached = [], []
+    seen = {"spill": 0, "load": 0, "drop": 0, "refused": 0}
+    for step in range(160):
+        r = rnd.random()
+        toks = [rnd.randrange(alpha) for _ in range(rnd.randint(1, 14))]
+        if cached and rnd.random() < 0.5:
+            toks = rnd.choice(cached)[:rnd.randint(1, 14)] + toks[:rnd.randint(0, 3)]
+        if r < 0.2:
+            n1, s1, id1 = ot.match(toks)
+            n2, s2, h2 = pt.match_prefix(toks)
+            assert (n1, s1.tolist()) == (n2, s2.tolist())
+            if rnd.random() < 0.4:
+                ot.lock(id1)
+                pt.lock(h2)
+                locked.append((id1, h2))
+        elif r < 0.4:
+            # through both tiers, then load the host part if the device pool has room
+            d1, h1, s1, id1 = ot.match_tiered(toks)
+            ot.lock(id1)
+            t = np.array(toks, np.int32)
+            ip = np.array([0, len(t)], np.int64)
+            rows = np.zeros((1, 32), np.int32)
+            pl, nodes, hl = pt.match_batch_tiered(t, ip, None, rows)
+            assert (d1, h1, s1.tolist()) == (int(pl[0]), int(hl[0]), rows[0, :d1].tolist())
+            locked.append((id1, int(nodes[0])))
+            if h1 and op_.available() >= h1:
+                row1 = ot.load(t[:d1 + h1])
+                pt.load_batch(t, ip, rows, pl, hl)
+                assert row1.tolist() == rows[0, :d1 + h1].tolist() and pl[0] == d1 + h1
+                seen["load"] += 1
+        elif r < 0.6:
+            a1 = op_.alloc(len(toks))
+            if a1 is None:
+                continue
+            a2 = pp.alloc(len(toks))
+            assert a1.tolist() == a2.tolist()
+            e1, _ = ot.insert(toks, a1)
+            e2, _ = pt.insert(toks, a2)
+            assert e1 == e2
+            op_.free(a1[:e1])
+            pp.free(a2[:e2])
+            cached.append(toks)
+        elif r < 0.7 and locked:
+            i1, h2 = locked.pop(rnd.randrange(len(locked)))
+            ot.unlock(i1)
+            pt.unlock(h2)
+        elif r < 0.84:
+            want = rnd.randint(0, 40)
+            ok1, f1, _ = ot.evict(want)
+            try:
+                st, f2 = pt.evict_lru(want)
+            except rc.RcError as e:      # loads still owed: both refuse and change nothing
+                assert e.code == rc.RC_ERR_INVALID and not ok1 and f1 == 0
+                seen["refused"] += 1
+                continue
+            assert f1 == f2 and ok1 == (st == rc.RC_OK)
+        else:
+            c1 = ot.drain()
+            c2 = pt.drain_copies()
+            for a, b in zip(c1, c2):
+                assert a.tolist() == b.tolist()
+            seen["spill"] += len(c1[0])
+        np.testing.assert_array_equal(ot.dump(), pt.dump())
+        np.testing.assert_array_equal(ot.tiers(), pt.tiers())
+        assert (op_.available(), oh.available()) == (pp.available(), ph.available())
+        s1, s2 = ot.stats(), pt.stats()
+        for k in ("evicted_nodes", "evicted_tokens", "nodes", "cached_tokens",
+                  "protected_tokens", "host_tokens", "spilled_tokens", "loaded_tokens",
+                  "dropped_tokens"):
+            assert s1[k] == s2[k], k
+        seen["drop"] = s2["dropped_tokens"]
+    c1, c2 = ot.drain(), pt.drain_copies()
+    for a, b in zip(c1, c2):
+        assert a.tolist() == b.tolist()
+    # both free lists agree in order
+    assert op_.alloc(op_.available()).tolist() == pp.alloc(pp.available()).tolist()
+    assert oh.alloc(oh.available()).tolist() == ph.alloc(ph.available()).tolist()
+    assert pt.stats()["spilled_tokens"] > 0
