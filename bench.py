@@ -620,13 +620,13 @@ def bench_replay(args, rank, world, local):
             "clocks": clk, "gpu_launches": rc.launch_count() - launches0}
 
 
-def _queue_batches(pq, policy):
+def _queue_batches(pq, policy, host_slots=0):
     """The batches the scheduler forms over the queue (host only; the engine's host cache makes
-    the same decisions): [(request ids, matched lengths)]."""
-    import prefix_cached_paged_gb300 as rc
+    the same decisions): [(request ids, matched lengths incl. tokens loaded from the host
+    tier, tokens loaded)]."""
     from prefix_cached_paged_gb300.runtime import HostCache
     w = pq.workload
-    hc = HostCache(w.pool_slots, w.max_ctx, w.pool_order)
+    hc = HostCache(w.pool_slots, w.max_ctx, w.pool_order, host_slots=host_slots)
     waiting = list(range(len(pq.seqs)))
     out = []
     while waiting:
@@ -636,42 +636,45 @@ def _queue_batches(pq, policy):
             raise RuntimeError("program queue: no request fits the pool")
         ids = [waiting[i] for i in idx]
         p = hc.plan([pq.seqs[i] for i in ids])
-        out.append((ids, p.prefix_len.copy()))
+        out.append((ids, p.prefix_len.copy(),
+                    0 if p.host_len is None else int(p.host_len.sum())))
         hc.finish(p)
         for i in sorted(idx, reverse=True):
             waiting.pop(i)
     return out
 
 
-def _serve_queue(pq, policy, batches, inputs, overlap):
+def _serve_queue(pq, policy, batches, inputs, overlap, host_slots=0, host_planes=None):
     """Serve the queue once through a fresh engine. overlap=False synchronises after every
     batch's kernels (host and GPU take turns); overlap=True never waits: the host schedules,
     plans and inserts batch k+1 while batch k's kernels run (stream order keeps the slots and
-    slot-table rows that the host recycles safe). Returns host ms, tree ms, kernel ms, wall ms."""
+    slot-table rows that the host recycles safe). Returns host ms, tree ms, kernel ms (extend),
+    wall ms, and the device time of the batches' begin work (slot table, host-tier copies)."""
     import torch
     from tests import harness as H
     m = pq.workload.model
-    eng = H.make_engine(pq.workload, max_reqs=pq.max_batch + 8)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in batches]
+    eng = H.make_engine(pq.workload, max_reqs=pq.max_batch + 8, host_tier_slots=host_slots,
+                        host_planes=host_planes)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in batches]
     waiting = list(range(len(pq.seqs)))
     host_s = 0.0
     torch.cuda.synchronize()
     tree0 = eng.host.host_seconds
     t_start = time.perf_counter()
-    for k, (ids_ref, _) in enumerate(batches):
+    for k, (ids_ref, _, _) in enumerate(batches):
         t0 = time.perf_counter()
         idx = eng.host.schedule([pq.seqs[i] for i in waiting], pq.max_batch, pq.max_new_tokens,
                                 policy=policy)
         ids = [waiting[i] for i in idx]
         assert ids == ids_ref
+        evs[k][0].record()
         b = eng.extend_begin([pq.seqs[i] for i in ids])
         host_s += time.perf_counter() - t0
         q, kk, v, o = inputs[k]
-        evs[k][0].record()
+        evs[k][1].record()
         for layer in range(m.layers):
             eng.extend_layer(b, layer, q, kk, v, o)
-        evs[k][1].record()
+        evs[k][2].record()
         if not overlap:
             torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -681,8 +684,9 @@ def _serve_queue(pq, policy, batches, inputs, overlap):
         host_s += time.perf_counter() - t0
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_start
-    gpu_ms = sum(a.elapsed_time(b) for a, b in evs)
-    return host_s * 1e3, (eng.host.host_seconds - tree0) * 1e3, gpu_ms, wall * 1e3
+    gpu_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    begin_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    return host_s * 1e3, (eng.host.host_seconds - tree0) * 1e3, gpu_ms, wall * 1e3, begin_ms
 
 
 def bench_queue(args, rank, world, local):
@@ -693,7 +697,10 @@ def bench_queue(args, rank, world, local):
         taking turns (synchronised after every batch);
       lspf overlapped: the host runs ahead of the GPU (no synchronisation until the end);
       no_reuse overlapped: the same lengths with every prefix distinct, the tree's overhead
-        when nothing is reused.
+        when nothing is reused;
+      fcfs_pool8k / fcfs_pool8k_host_tier: first-come-first-served behind an 8000-slot device
+        pool (four prefixes), without and with a 50000-slot host tier in pinned host memory.
+    Then the host tier's copy kernel alone: 16384 tokens x all layers spilled and loaded back.
     Timed: wall clock of the pass, the host calls (perf_counter; the tree and pool part
     separately) and each batch's kernels (CUDA events). The synthetic q / k / v of every batch
     are generated before the timed passes; every layer reads layer 0's values."""
@@ -704,21 +711,30 @@ def bench_queue(args, rank, world, local):
     from tests import harness as H
 
     L = args.layers
-    cases = [("lspf", dict(), rc.RC_SCHED_LSPF, False),
-             ("fcfs", dict(), rc.RC_SCHED_FCFS, False),
-             ("lspf_overlapped", dict(), rc.RC_SCHED_LSPF, True),
-             ("no_reuse_overlapped", dict(shared=False), rc.RC_SCHED_LSPF, True)]
+    HOST = 50_000
+    cases = [("lspf", dict(), rc.RC_SCHED_LSPF, False, 0),
+             ("fcfs", dict(), rc.RC_SCHED_FCFS, False, 0),
+             ("lspf_overlapped", dict(), rc.RC_SCHED_LSPF, True, 0),
+             ("no_reuse_overlapped", dict(shared=False), rc.RC_SCHED_LSPF, True, 0),
+             ("fcfs_pool8k", dict(pool_slots=8_000), rc.RC_SCHED_FCFS, False, 0),
+             ("fcfs_pool8k_host_tier", dict(pool_slots=8_000), rc.RC_SCHED_FCFS, False, HOST)]
     out = {}
     launches = 0
+    m0 = W.program_queue(layers=L).workload.model
+    dt = H.torch_dtype(m0.dtype)
+    hshape = (L, HOST, m0.n_kv_heads, m0.head_dim)
+    planes = (torch.empty(hshape, dtype=dt, pin_memory=True),
+              torch.empty(hshape, dtype=dt, pin_memory=True))
     clocks = ClockSampler(local)
     clocks.start()
-    for name, kw, policy, overlap in cases:
+    for name, kw, policy, overlap, host_slots in cases:
         pq = W.program_queue(layers=L, **kw)
         m = pq.workload.model
         prompt = int(sum(len(s) for s in pq.seqs))
-        batches = _queue_batches(pq, policy)
+        batches = _queue_batches(pq, policy, host_slots)
         inputs, flops, computed = [], 0.0, 0
-        for ids, pl in batches:
+        loaded = sum(x[2] for x in batches)
+        for ids, pl, _ in batches:
             seqs = [pq.seqs[i] for i in ids]
             h = H.new_token_hashes(m, seqs, pl)
             q, kk, v = H.dense_qkv(m, sdev.hashes_to_device(h), 0, len(h))
@@ -730,15 +746,18 @@ def bench_queue(args, rank, world, local):
         runs = []
         for rep in range(args.warmup + args.steps):
             l0 = rc.launch_count()
-            r = _serve_queue(pq, policy, batches, inputs, overlap)
+            r = _serve_queue(pq, policy, batches, inputs, overlap, host_slots,
+                             planes if host_slots else None)
             assert rc.device_status() == 0
             if rep >= args.warmup:
                 runs.append(r)
                 launches += rc.launch_count() - l0
-        host_ms, tree_ms, gpu_ms, wall_ms = (float(np.median([r[i] for r in runs]))
-                                             for i in range(4))
+        host_ms, tree_ms, gpu_ms, wall_ms, begin_ms = (float(np.median([r[i] for r in runs]))
+                                                       for i in range(5))
         out[name] = {"batches": len(batches), "computed_tokens": computed,
                      "hit_rate": round(1 - computed / prompt, 4),
+                     "pool_slots": pq.workload.pool_slots, "host_tier_slots": host_slots,
+                     "loaded_tokens": loaded, "begin_gpu_ms": round(begin_ms, 2),
                      "wall_ms": round(wall_ms, 2), "host_ms": round(host_ms, 2),
                      "tree_ms": round(tree_ms, 2), "kernel_ms": round(gpu_ms, 2),
                      "tree_frac_of_wall": round(tree_ms / wall_ms, 4),
@@ -747,6 +766,53 @@ def bench_queue(args, rank, world, local):
                      "prompt_tokens_per_s": round(prompt / (wall_ms * 1e-3), 1)}
         del inputs
         torch.cuda.empty_cache()
+    # the host tier's copy kernel alone: spill 16384 tokens' rows of every layer to pinned host
+    # memory, then load them back to other device slots
+    n = 16_384
+    dk = torch.empty((L, 20_000, m0.n_kv_heads, m0.head_dim), dtype=dt, device="cuda")
+    dv = torch.empty_like(dk)
+    g = np.random.default_rng(0)
+    src = torch.from_numpy(g.choice(20_000, n, replace=False).astype(np.int32)).cuda()
+    dst = torch.from_numpy(g.choice(20_000, n, replace=False).astype(np.int32)).cuda()
+    hsl = torch.from_numpy(g.choice(HOST, n, replace=False).astype(np.int32)).cuda()
+    nbytes = 2 * n * L * m0.n_kv_heads * m0.head_dim * dk.element_size()
+    tier = {}
+    for direction, args_ in (("spill_device_to_host", (dk, dv, src, planes[0], planes[1], hsl)),
+                             ("load_host_to_device", (planes[0], planes[1], hsl, dk, dv, dst))):
+        for _ in range(args.warmup):
+            rc.kv_copy(*args_)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            rc.kv_copy(*args_)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        tier[direction] = {"gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                           "ms": round(ms, 3), "bytes": nbytes}
+    # the link's own copy rate: one contiguous pinned <-> device copy of the same size
+    # (cudaMemcpyAsync through torch), the roofline of the row copies above
+    flat_h = planes[0].view(-1)[: nbytes // 2 // dk.element_size()]
+    flat_d = dk.view(-1)[: flat_h.numel()]
+    for direction, (dst_, src_) in (("spill_device_to_host", (flat_h, flat_d)),
+                                    ("load_host_to_device", (flat_d, flat_h))):
+        for _ in range(args.warmup):
+            dst_.copy_(src_, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            dst_.copy_(src_, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        link = flat_h.numel() * flat_h.element_size() / (ms * 1e-3) / 1e9
+        tier[direction]["link_memcpy_gb_per_s"] = round(link, 1)
+        tier[direction]["frac_of_link"] = round(tier[direction]["gb_per_s"] / link, 4)
+    assert rc.device_status() == 0
+    out["host_tier_copy"] = tier
+    del dk, dv, planes
     clk = clocks.stop()
     pk = peaks()
     best = out["lspf_overlapped"]

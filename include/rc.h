@@ -238,6 +238,29 @@ typedef struct rc_slot_write_args {
 } rc_slot_write_args;
 int rc_slot_table_write(const rc_slot_write_args* args, void* stream);
 
+/* KV row copies between two pools (the host tier's spills and loads; SGLang blog Sec. 6.1):
+ * for i < n and every layer, the K row and the V row of slot src_slots[i] in the source planes
+ * are copied to slot dst_slots[i] in the destination planes. Planes are [layers][num_slots][row]
+ * with row = row_bytes (Hkv x d x element size, a multiple of 16), 16-byte aligned, in device
+ * memory or in pinned host memory that the GPU can address (on Grace-Blackwell the kernel reads
+ * and writes it directly). src_slots / dst_slots are device int32 arrays. Destination slots
+ * must be distinct; rows are copied in no particular order. A slot outside its pool sets the
+ * device status word (rc_device_status) and that row is skipped. Asynchronous on `stream`. */
+typedef struct rc_kv_copy_args {
+  int64_t n;
+  int32_t layers;
+  int64_t row_bytes;
+  const int32_t* src_slots;
+  const int32_t* dst_slots;
+  const void* src_k;
+  const void* src_v;
+  int64_t src_num_slots;
+  void* dst_k;
+  void* dst_v;
+  int64_t dst_num_slots;
+} rc_kv_copy_args;
+int rc_kv_copy(const rc_kv_copy_args* args, void* stream);
+
 /* Extend attention (SGLang blog Sec. 2.3 "compute only the unmatched tokens"; paper digest
  * App. A.1). For request b with matched prefix P = prefix_len[b] and S = qo_indptr[b+1] -
  * qo_indptr[b] new tokens at positions P .. P+S-1, each new token's query attends to the P

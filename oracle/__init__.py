@@ -319,13 +319,19 @@ def schedule_batch(tree: Tree, seqs, match_lens=None, fcfs: bool = False,
     admit into the batch while memory allows); `fcfs` keeps queue order instead, the
     first-come-first-served order the digest contrasts it with.
 
-    Readings: ties keep queue order; admission stops at the first request that does not fit;
+    Readings: with a host tier, matches and room count device-resident tokens only; ties keep
+    queue order; admission stops at the first request that does not fit;
     a request fits while the batch holds at most `max_batch` requests and `max_new_tokens`
     computed tokens (len - match; negative = no limit), and while free slots plus the cached
     tokens of unreferenced nodes, less `reserve`, cover the computed tokens plus the set of
     unreferenced cached tokens the admitted matches lock. Returns (order, match, admitted).
     """
     nodes = tree.nodes()
+    if getattr(tree, "host_pool", None) is not None:
+        # with a host tier, scheduling sees the device-resident part of the tree only
+        t = tree.tiers()
+        host = {int(i) for i, h in zip(t[0::2], t[1::2]) if h}
+        nodes = [n for n in nodes if n["id"] not in host]
     children = {(n["parent"], int(n["key"][0])): n for n in nodes}
     ref = {n["id"]: n["ref"] for n in nodes}
     match, paths = [], []

@@ -17,7 +17,7 @@ import numpy as np
 
 from ._lib import (RC_DTYPE_BF16, RC_DTYPE_F32, RC_ERR_CUDA, RC_ERR_DEVICE, RC_ERR_INSUFFICIENT,
                    RC_ERR_INVALID, RC_ERR_OOM, RC_OK, RC_SCHED_FCFS, RC_SCHED_LSPF, RcDecodeArgs,
-                   RcError, RcExtendArgs, RcSlotWriteArgs, RcStats, check, lib)
+                   RcError, RcExtendArgs, RcKvCopyArgs, RcSlotWriteArgs, RcStats, check, lib)
 
 __all__ = [
     "Pool", "RadixTree", "RcError", "slot_table_write", "extend_attention", "decode_attention",
@@ -260,6 +260,29 @@ def slot_table_write(req_to_token, seg_row, seg_col, seg_indptr, values, stream=
                         seg_indptr=seg_indptr.data_ptr(), values=values.data_ptr(),
                         req_to_token=req_to_token.data_ptr())
     check(lib().rc_slot_table_write(ctypes.byref(a), _stream(stream)), "rc_slot_table_write")
+
+
+def kv_copy(src_k, src_v, src_slots, dst_k, dst_v, dst_slots, stream=None):
+    """For every i and layer: K and V rows of src_slots[i] -> dst_slots[i]. Planes are
+    [layers, num_slots, Hkv, d] tensors on the device or in pinned host memory (the host tier);
+    slot arrays are device int32."""
+    for t in (src_k, src_v, dst_k, dst_v):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("kv_copy: planes must be device tensors or pinned host tensors")
+        if not t.is_contiguous():
+            raise ValueError("kv_copy: planes must be contiguous")
+    if src_k.shape[0] != dst_k.shape[0] or src_k.shape[2:] != dst_k.shape[2:] or \
+            src_k.dtype != dst_k.dtype or src_k.shape != src_v.shape or dst_k.shape != dst_v.shape:
+        raise ValueError("kv_copy: plane shapes or dtypes differ")
+    if src_slots.numel() != dst_slots.numel():
+        raise ValueError("kv_copy: slot arrays differ in length")
+    row = src_k.shape[2] * src_k.shape[3] * src_k.element_size()
+    a = RcKvCopyArgs(n=src_slots.numel(), layers=src_k.shape[0], row_bytes=row,
+                     src_slots=src_slots.data_ptr(), dst_slots=dst_slots.data_ptr(),
+                     src_k=src_k.data_ptr(), src_v=src_v.data_ptr(),
+                     src_num_slots=src_k.shape[1], dst_k=dst_k.data_ptr(),
+                     dst_v=dst_v.data_ptr(), dst_num_slots=dst_k.shape[1])
+    check(lib().rc_kv_copy(ctypes.byref(a), _stream(stream)), "rc_kv_copy")
 
 
 def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_to_token,

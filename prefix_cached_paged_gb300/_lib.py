@@ -53,6 +53,7 @@ SIGNATURES = {
     "rc_schedule_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I64, _I64, _P, _P,
                                          _P]),
     "rc_slot_table_write": (ctypes.c_int, [_P, _P]),
+    "rc_kv_copy": (ctypes.c_int, [_P, _P]),
     "rc_extend_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
     "rc_extend_attention": (ctypes.c_int, [_P, _P]),
     "rc_decode_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),
@@ -68,6 +69,12 @@ class RcStats(ctypes.Structure):
                                     "evicted_tokens", "matched_tokens", "match_queries",
                                     "host_tokens", "spilled_tokens", "loaded_tokens",
                                     "dropped_tokens")]
+
+
+class RcKvCopyArgs(ctypes.Structure):
+    _fields_ = [("n", _I64), ("layers", _I32), ("row_bytes", _I64), ("src_slots", _P),
+                ("dst_slots", _P), ("src_k", _P), ("src_v", _P), ("src_num_slots", _I64),
+                ("dst_k", _P), ("dst_v", _P), ("dst_num_slots", _I64)]
 
 
 class RcSlotWriteArgs(ctypes.Structure):

@@ -22,7 +22,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
-               extend_workspace_bytes, prefix_stacking_groups, shared_context_groups,
+               extend_workspace_bytes, kv_copy, prefix_stacking_groups, shared_context_groups,
                stacking_pays)
 from .runtime import DeviceKV, HostCache, Plan
 
@@ -65,13 +65,26 @@ STACK_MIN_SHARED = 256
 class Engine:
     def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
                  max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True,
-                 stack_extend=True):
+                 stack_extend=True, host_tier_slots=0, host_planes=None):
         self.layers = layers
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
         self.sm_scale = 1.0 / float(np.sqrt(head_dim))
-        self.host = HostCache(num_slots, max_ctx, initial_order)
+        self.host = HostCache(num_slots, max_ctx, initial_order, host_slots=host_tier_slots)
         self.dev = DeviceKV(layers, num_slots, n_kv_heads, head_dim, dtype, max_reqs, max_ctx,
                             device)
+        self.host_k = self.host_v = None
+        if host_tier_slots:
+            # the host tier's KV planes: pinned host memory the kernels address directly
+            # (host_planes: a caller's (k, v) pair of that shape, reused across engines)
+            torch = self.dev.torch
+            shape = (layers, host_tier_slots, n_kv_heads, head_dim)
+            if host_planes is not None:
+                self.host_k, self.host_v = host_planes
+                if tuple(self.host_k.shape) != shape or not self.host_k.is_pinned():
+                    raise ValueError(f"host_planes must be pinned tensors of shape {shape}")
+            else:
+                self.host_k = torch.empty(shape, dtype=dtype, pin_memory=True)
+                self.host_v = torch.empty(shape, dtype=dtype, pin_memory=True)
         self.max_ctx = max_ctx
         self.kv_chunk = kv_chunk
         # decode reads a context prefix that several requests share once for all of them
@@ -82,6 +95,20 @@ class Engine:
         self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
+
+    def _tier_copies(self, copies):
+        """Perform the host tier's owed copies on the stream: spills (device -> host) before
+        loads (host -> device), both before any later kernel that writes a recycled slot."""
+        if copies is None:
+            return
+        sd, sh, lh, ld = copies
+        if len(sd) == 0 and len(lh) == 0:
+            return
+        d_sd, d_sh, d_lh, d_ld = self.dev.upload_i32([sd, sh, lh, ld])
+        if len(sd):
+            kv_copy(self.dev.k, self.dev.v, d_sd, self.host_k, self.host_v, d_sh)
+        if len(lh):
+            kv_copy(self.host_k, self.host_v, d_lh, self.dev.k, self.dev.v, d_ld)
 
     # ---------------------------------------------------------------- rows
     def _take_rows(self, n):
@@ -95,6 +122,7 @@ class Engine:
     # ---------------------------------------------------------------- extend
     def extend_begin(self, seqs, extra: int = 0, match_all: bool = False) -> ExtendBatch:
         plan = self.host.plan(seqs, extra=extra, match_all=match_all)
+        self._tier_copies(plan.copies)
         B = len(seqs)
         row_ids = self._take_rows(B)
         self.dev.write_rows(row_ids, plan.rows, plan.lengths)
@@ -143,6 +171,7 @@ class Engine:
         """Requests enter decoding: each context must be cached; it is matched and locked, its
         slots written to a fresh slot-table row. The first decode_step allocates the new tokens."""
         plan = self.host.plan(contexts, match_all=True)
+        self._tier_copies(plan.copies)
         if plan.num_tokens:
             self.host.pool.free(plan.out_loc)
             for n in plan.nodes:
@@ -170,6 +199,7 @@ class Engine:
         B = len(batch.row_ids)
         if new_slots is None:
             new_slots = self.host.alloc(B)
+            self._tier_copies(self.host.last_alloc_copies)
         cols = batch.seq_len.astype(np.int64)
         rows = np.zeros((B, self.max_ctx), dtype=np.int32)
         rows[np.arange(B), cols] = new_slots

@@ -9,6 +9,7 @@ seeded sample of units in the launch configuration the benchmark uses.
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from synth import workloads as W
 from tests import harness as H
@@ -439,4 +440,104 @@ def test_program_queue_served_by_the_scheduler(policy):
             waiting.pop(i)
         batches += 1
     assert evicted > 0 and batches > 2
+    _status_clear()
+
+
+@pytest.mark.parametrize("dtype,Hkv,d,layers", [("bf16", 4, 128, 3), ("f32", 2, 64, 2)])
+def test_kv_copy_round_trip_through_pinned_host(dtype, Hkv, d, layers):
+    """rc_kv_copy device -> pinned host -> device at scattered slots: every row bit-exact, rows
+    not named untouched; an out-of-range slot is reported, not written."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    dt = H.torch_dtype(dtype)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    N, NH, n = 3000, 2000, 777
+    dk = torch.randn((layers, N, Hkv, d), device="cuda", generator=g).to(dt)
+    dv = torch.randn((layers, N, Hkv, d), device="cuda", generator=g).to(dt)
+    hk = torch.zeros((layers, NH, Hkv, d), dtype=dt).pin_memory()
+    hv = torch.zeros((layers, NH, Hkv, d), dtype=dt).pin_memory()
+    rng = np.random.default_rng(2)
+    src = rng.choice(N, n, replace=False).astype(np.int32)
+    hst = rng.choice(NH, n, replace=False).astype(np.int32)
+    dst = rng.choice(N, n, replace=False).astype(np.int32)
+    S, Hs, D = (torch.from_numpy(a).cuda() for a in (src, hst, dst))
+    rc.kv_copy(dk, dv, S, hk, hv, Hs)
+    ek, ev = dk.clone(), dv.clone()
+    out_k = torch.zeros_like(dk)
+    out_v = torch.zeros_like(dv)
+    rc.kv_copy(hk, hv, Hs, out_k, out_v, D)
+    torch.cuda.synchronize()
+    assert torch.equal(hk[:, torch.from_numpy(hst).long()], ek[:, torch.from_numpy(src).long()].cpu())
+    assert torch.equal(out_k[:, D.long()], ek[:, S.long()])
+    assert torch.equal(out_v[:, D.long()], ev[:, S.long()])
+    untouched = np.setdiff1d(np.arange(N), dst)
+    assert int(out_k[:, torch.from_numpy(untouched).cuda().long()].abs().sum()) == 0
+    _status_clear()
+    bad = torch.tensor([0, N], dtype=torch.int32, device="cuda")
+    ok = torch.tensor([1, 2], dtype=torch.int32, device="cuda")
+    rc.kv_copy(dk, dv, bad, hk, hv, ok)
+    assert rc.device_status() == 1      # slot out of range, reported and skipped
+
+
+@pytest.mark.parametrize("policy", ["fcfs", "lspf"])
+def test_program_queue_with_host_tier(policy):
+    """The small program queue behind a 700-slot device pool and a host tier: each batch's
+    matches, loads and copies equal the oracle's; reloaded slots hold the generator's K/V bit for
+    bit; sampled outputs match the oracle."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    from synth import device as sdev
+    pq = W.program_queue(n_programs=6, prefix_len=200, n_questions=4, question_len=20,
+                         pool_slots=700, max_batch=8, max_new_tokens=1200, layers=2)
+    w = pq.workload
+    eng = H.make_engine(w, max_reqs=pq.max_batch + 8, host_tier_slots=2000)
+    sim = oracle.CacheSim(w.pool_slots, w.pool_order, host_slots=2000)
+    fcfs = policy == "fcfs"
+    waiting = list(range(len(pq.seqs)))
+    rng = np.random.default_rng(4)
+    loaded = 0
+    while waiting:
+        seqs_w = [pq.seqs[i] for i in waiting]
+        idx = eng.host.schedule(seqs_w, pq.max_batch, pq.max_new_tokens,
+                                policy=rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF)
+        order, _, adm = oracle.schedule_batch(sim.tree, seqs_w, [len(s) - 1 for s in seqs_w],
+                                              fcfs, pq.max_batch, pq.max_new_tokens)
+        assert idx == order[:adm]
+        seqs = [pq.seqs[waiting[i]] for i in idx]
+        res = sim.extend_prepare(seqs)
+        b = eng.extend_begin(seqs)
+        assert b.plan.prefix_len.tolist() == res.prefix_len
+        assert b.plan.host_len.tolist() == res.host_len
+        for x, y in zip(b.plan.copies, res.copies):
+            assert x.tolist() == y.tolist()
+        loaded += int(b.plan.host_len.sum())
+        h = H.new_token_hashes(w.model, seqs, b.plan.prefix_len)
+        hd = sdev.hashes_to_device(h)
+        outs = {}
+        for layer in range(w.model.layers):
+            q, k, v = H.dense_qkv(w.model, hd, layer, b.num_tokens)
+            o = torch.empty_like(q)
+            eng.extend_layer(b, layer, q, k, v, o)
+            outs[layer] = (o, None)
+        _check_extend(w, b, outs, seqs, _sample_units(rng, len(seqs), w.model.layers, 32, 6))
+        _check_slot_rows(eng, b)
+        # the slots just loaded back hold each token's own K/V in every layer
+        for i, s in enumerate(seqs):
+            hl = int(b.plan.host_len[i])
+            if hl:
+                p = int(b.plan.prefix_len[i])
+                slots = b.plan.rows[i, p - hl:p]
+                hs = synth.prefix_hashes(w.model.seed, s)[p - hl:p]
+                for layer in range(w.model.layers):
+                    got = eng.dev.k[layer][torch.from_numpy(slots).long().cuda()].cpu()
+                    want = synth.values_bits(hs, synth.TENSOR_K, layer, range(w.model.n_kv_heads),
+                                             w.model.head_dim, w.model.dtype)
+                    np.testing.assert_array_equal(
+                        got.view(torch.int16).numpy().view(np.uint16), want)
+        eng.extend_end(b)
+        sim.extend_finish(seqs, res)
+        for i in sorted(idx, reverse=True):
+            waiting.pop(i)
+    if fcfs:
+        assert loaded > 0
     _status_clear()

@@ -557,3 +557,65 @@ def test_host_tier_random_ops_match_oracle_bit_exact(seed):
     assert op_.alloc(op_.available()).tolist() == pp.alloc(pp.available()).tolist()
     assert oh.alloc(oh.available()).tolist() == ph.alloc(ph.available()).tolist()
     assert pt.stats()["spilled_tokens"] > 0
+
+
+def _serve_tiered(pq, fcfs, host_slots, product):
+    """Serve the queue with a host tier: per batch (ids, prefix_len, host_len, copies)."""
+    w = pq.workload
+    if product:
+        hc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order, host_slots=host_slots)
+    else:
+        sim = oracle.CacheSim(w.pool_slots, w.pool_order, host_slots=host_slots)
+    waiting = list(range(len(pq.seqs)))
+    steps = []
+    while waiting:
+        seqs = [pq.seqs[i] for i in waiting]
+        if product:
+            idx = hc.schedule(seqs, pq.max_batch, pq.max_new_tokens,
+                              policy=rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF)
+            p = hc.plan([pq.seqs[waiting[i]] for i in idx])
+            step = (p.prefix_len.tolist(), p.host_len.tolist(), [c.tolist() for c in p.copies])
+            hc.finish(p)
+        else:
+            order, _, adm = oracle.schedule_batch(sim.tree, seqs, [len(s) - 1 for s in seqs],
+                                                  fcfs, pq.max_batch, pq.max_new_tokens)
+            idx = order[:adm]
+            batch = [pq.seqs[waiting[i]] for i in idx]
+            res = sim.extend_prepare(batch)
+            step = (list(res.prefix_len), list(res.host_len), [c.tolist() for c in res.copies])
+            sim.extend_finish(batch, res)
+        assert idx, "no progress"
+        steps.append(([waiting[i] for i in idx],) + step)
+        for i in sorted(idx, reverse=True):
+            waiting.pop(i)
+    return steps
+
+
+@pytest.mark.parametrize("fcfs", [False, True])
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_program_queue_with_host_tier_matches_oracle(fcfs, size):
+    """The program queue with a host tier behind a small device pool: the same batches, matches,
+    loads and owed copies as the oracle's loop; the tier turns recomputation into loads."""
+    if size == "small":
+        kw = dict(n_programs=6, prefix_len=200, n_questions=4, question_len=20, pool_slots=700,
+                  max_batch=8, max_new_tokens=1200)
+        host = 2000
+    else:
+        kw = dict(pool_slots=8_000)
+        host = 60_000
+    pq = W.program_queue(**kw)
+    a = _serve_tiered(pq, fcfs, host, product=True)
+    b = _serve_tiered(pq, fcfs, host, product=False)
+    assert a == b
+    loaded = sum(sum(h) for _, _, h, _ in a)
+    computed = sum(len(pq.seqs[i]) - p for ids, pl, _, _ in a for i, p in zip(ids, pl))
+    without = sum(len(pq.seqs[i]) - p for ids, pl, _ in
+                  _serve_queue_product(pq, rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF)
+                  for i, p in zip(ids, pl))
+    if fcfs:
+        # interleaved arrival evicts every prefix before its next question: the tier loads
+        # them back instead of recomputing
+        assert loaded > 0 and computed < without
+    else:
+        # longest shared prefix first finishes a program before leaving it: little to reload
+        assert computed <= without
