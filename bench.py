@@ -555,7 +555,10 @@ def bench_replay(args, rank, world, local):
     else:
         w = W.CONFIGS[name]()
     m = w.model
-    eng = H.make_engine(w, max_reqs=300, kv_chunk=args.kv_chunk)
+    stack = {"auto": (True, 4), "off": (False, 4), "flat": (True, 1), "always": ("always", 4),
+             "always-flat": ("always", 1)}[args.stack]
+    eng = H.make_engine(w, max_reqs=300, kv_chunk=args.kv_chunk, stack_extend=stack[0],
+                        stack_levels=stack[1])
     for ph in w.phases[:-1]:
         if ph.kind == "cache":
             H.run_cache_phase(eng, m, ph.seqs, ph.keep_locked)
@@ -576,6 +579,8 @@ def bench_replay(args, rank, world, local):
         peak = pk["bf16_tflops"]
         kernel = "extend_attention"
         skipped = (int(Pl.sum()), int(b.plan.lengths.sum()))
+        stacking = ("none" if b.stack is None else
+                    {"groups_per_level": np.diff(b.stack[4]).tolist()})
     else:
         seqs = last.seqs
         db = eng.decode_begin([s[:-1] for s in seqs])
@@ -591,6 +596,7 @@ def bench_replay(args, rank, world, local):
         peak = pk["hbm_gbs"]
         kernel = "decode_attention (plan + split-K main + merge)"
         skipped = (0, int(db.seq_len.sum()))
+        stacking = None
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()
@@ -612,7 +618,8 @@ def bench_replay(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": m.dtype,
             "data": "synthetic",
             "config": {"workload": name, "mode": "kernel replay (same batch each step)",
-                       "l2": "not flushed between replays"},
+                       "l2": "not flushed between replays", "stack": args.stack,
+                       "stacking": stacking},
             "roofline": {"kernel": kernel, "bound": bound, "achieved": round(val, 2),
                          "peak": peak, "unit": unit, "frac": round(val / peak, 4),
                          "traffic": None, "peak_source": pk["source"]},
@@ -885,10 +892,15 @@ def main():
                     choices=["fork_mixed_step", "tiny_extend", "few_shot_extend",
                              "two_level_extend", "multi_turn_decode",
                              "multi_turn_decode_unshared", "fork_extend_layer",
-                             "program_queue"],
+                             "program_queue", "tree_extend"],
                     help="fork_mixed_step = the full step; program_queue = the scheduler over a "
                          "request queue; the others replay one kernel")
     ap.add_argument("--kv-chunk", type=int, default=0)
+    ap.add_argument("--stack", default="auto",
+                    choices=["auto", "off", "flat", "always", "always-flat"],
+                    help="extend prefix stacking in kernel replays: auto = the cost model over "
+                         "up to 4 tree levels, flat = the cost model on the shallowest level "
+                         "only, always = every group found")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

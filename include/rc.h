@@ -316,7 +316,21 @@ typedef struct rc_extend_args {
   const int32_t* group_shared;  /* [num_groups] */
   void* workspace;
   size_t workspace_bytes;
+  /* Optional cascade over the levels of the radix tree (num_levels <= 1: the single level
+   * above). Groups are listed level by level: level l holds groups [level_indptr[l],
+   * level_indptr[l+1]) (HOST int32 array of num_levels + 1 entries, level_indptr[0] = 0,
+   * level_indptr[num_levels] = num_groups, at most RC_MAX_STACK_LEVELS levels). Within a level
+   * the contract above holds. A group of level l > 0 lies inside one group of level l - 1 and
+   * group_start[g] (device int32 [num_groups]; NULL = all 0) is that parent's group_shared: its
+   * stacked pass covers keys [group_start[g], group_shared[g]) only and merges its result into
+   * the partial the levels above left (levels run in order). A request's per-request pass
+   * starts at the largest group_shared of the groups holding it. group_start[g] >= 0 and
+   * < group_shared[g], else reported through the status word. */
+  int32_t num_levels;
+  const int32_t* level_indptr;
+  const int32_t* group_start;
 } rc_extend_args;
+#define RC_MAX_STACK_LEVELS 4
 int rc_extend_workspace_bytes(const rc_extend_args* args, size_t* out_bytes);
 int rc_extend_attention(const rc_extend_args* args, void* stream);
 

@@ -292,12 +292,19 @@ def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_t
     Hkv = k_new.shape[1]
     g = {}
     if stack is not None:
-        ranges, shared, max_rows = stack
+        # (ranges, shared, max_rows) or, for a cascade over tree levels, (ranges, shared,
+        # max_rows, start, level_indptr) -- level_indptr a host int32 numpy array
+        ranges, shared, max_rows = stack[:3]
         g = dict(num_groups=int(shared.numel()), max_group_rows=int(max_rows),
                  group_range=ranges.data_ptr(), group_shared=shared.data_ptr(),
                  workspace=0 if workspace is None else workspace.data_ptr(),
                  workspace_bytes=0 if workspace is None else
                  workspace.numel() * workspace.element_size())
+        if len(stack) == 5:
+            start, level_indptr = stack[3], stack[4]
+            assert level_indptr.dtype == np.int32 and level_indptr.flags.c_contiguous
+            g.update(num_levels=len(level_indptr) - 1, level_indptr=level_indptr.ctypes.data,
+                     group_start=start.data_ptr())
     return RcExtendArgs(**g,
         dtype=_dtype_code(q), num_reqs=prefix_len.numel(), num_q_heads=Hq, num_kv_heads=Hkv,
         head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
@@ -396,22 +403,22 @@ def _extend_cost_us(P, S, key0, ppt, merge):
     return pairs * (per + _C_CTA_US + (_C_MERGE_US if merge else 0.0))
 
 
-def stacking_pays(prefix_len, new_len, shared: int, group: int) -> bool:
-    """Whether a stacked prefix pass over `shared` keys for these requests (one group of
-    consecutive requests) is estimated to save at least 10% of their extend time. It pays when
-    stacking fills query tiles that short suffixes leave mostly empty; with long suffixes or
-    many query heads per KV head the tiles are full already and the extra per-request pass
-    only adds CTAs."""
+def stacking_pays(prefix_len, new_len, shared: int, group: int, start: int = 0) -> bool:
+    """Whether a stacked prefix pass over keys [start, shared) for these requests (one group of
+    consecutive requests; start > 0: a deeper level whose parent covers the keys before it) is
+    estimated to save at least 10% of their extend time over those keys. It pays when stacking
+    fills query tiles that short suffixes leave mostly empty; with long suffixes or many query
+    heads per KV head the tiles are full already and the extra pass only adds CTAs."""
     ppt = max(128 // group, 1)
     P = [int(x) for x in prefix_len]
     S = [int(x) for x in new_len]
-    alone = sum(_extend_cost_us(p, s, 0, ppt, False) for p, s in zip(P, S))
+    alone = sum(_extend_cost_us(p, s, start, ppt, start > 0) for p, s in zip(P, S))
     U = sum(S)
     if U <= 0:
         return False
-    stacked_tiles = -(-shared // 128)
+    stacked_tiles = -(-(shared - start) // 128)
     first = -(-U // (2 * ppt)) * (stacked_tiles * (_T_TILE_US if U > ppt else _T_TILE_US / 2)
-                                 + _C_CTA_US)
+                                 + _C_CTA_US + (_C_MERGE_US if start > 0 else 0.0))
     second = sum(_extend_cost_us(p, s, shared, ppt, True) for p, s in zip(P, S))
     return first + second < 0.9 * alone
 
@@ -444,6 +451,43 @@ def prefix_stacking_groups(rows, prefix_len, new_len, min_shared: int):
             max_rows = max(max_rows, int(S[b:e].sum()))
         b = e
     return np.asarray(ranges, np.int32), np.asarray(shared, np.int32), max_rows
+
+
+MAX_STACK_LEVELS = 4   # RC_MAX_STACK_LEVELS
+
+
+def prefix_stacking_levels(rows, prefix_len, new_len, min_shared: int, pays=None,
+                           max_levels: int = MAX_STACK_LEVELS):
+    """Stacking groups over the levels of the tree (cascade): level 0 as prefix_stacking_groups;
+    inside each kept group of level l (shared length s), runs whose members agree over at least
+    s + min_shared positions form level l + 1, with key start s. pays(b0, b1, shared, start)
+    decides whether a candidate is kept (None: all); a group not kept is not searched further.
+    Returns (ranges [2 G], shared [G], start [G], level_indptr [L + 1], max_group_rows) as int32
+    numpy arrays (and an int), groups listed level by level; G = 0 when there is none."""
+    rows = np.asarray(rows)
+    P = np.asarray(prefix_len, dtype=np.int64)
+    S = np.asarray(new_len, dtype=np.int64)
+    parents = [(0, len(P), 0)]
+    ranges, shared, start, level_indptr, max_rows = [], [], [], [0], 0
+    for _ in range(max_levels):
+        found = []
+        for p0, p1, psh in parents:
+            r, sh, _ = prefix_stacking_groups(rows[p0:p1], P[p0:p1], S[p0:p1], psh + min_shared)
+            for g in range(len(sh)):
+                b0, b1 = p0 + int(r[2 * g]), p0 + int(r[2 * g + 1])
+                if pays is None or pays(b0, b1, int(sh[g]), psh):
+                    found.append((b0, b1, int(sh[g]), psh))
+        if not found:
+            break
+        for b0, b1, sh, st in found:
+            ranges += [b0, b1]
+            shared.append(sh)
+            start.append(st)
+            max_rows = max(max_rows, int(S[b0:b1].sum()))
+        level_indptr.append(len(shared))
+        parents = [(b0, b1, sh) for b0, b1, sh, _ in found]
+    return (np.asarray(ranges, np.int32), np.asarray(shared, np.int32),
+            np.asarray(start, np.int32), np.asarray(level_indptr, np.int32), max_rows)
 
 
 def shared_context_groups(rows, lengths, group_size: int, min_shared: int):

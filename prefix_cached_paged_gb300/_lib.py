@@ -92,7 +92,8 @@ class RcExtendArgs(ctypes.Structure):
                 ("req_idx", _P), ("req_to_token", _P), ("k_pool", _P), ("v_pool", _P),
                 ("o", _P), ("lse", _P), ("num_groups", _I32), ("max_group_rows", _I32),
                 ("group_range", _P), ("group_shared", _P), ("workspace", _P),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("num_levels", _I32),
+                ("level_indptr", _P), ("group_start", _P)]
 
 
 class RcDecodeArgs(ctypes.Structure):

@@ -47,6 +47,17 @@ extern "C" int rc_extend_attention(const rc_extend_args* a, void* stream) {
     RC_CHECK_ARG(a->workspace && ((uintptr_t)a->workspace & 15) == 0 && a->workspace_bytes >= need,
                  "rc_extend_attention: stacking needs a 16-byte aligned workspace of %zu bytes",
                  need);
+    RC_CHECK_ARG(a->num_levels >= 0 && a->num_levels <= RC_MAX_STACK_LEVELS,
+                 "rc_extend_attention: num_levels %d (at most %d)", a->num_levels,
+                 RC_MAX_STACK_LEVELS);
+    if (a->num_levels > 1) {
+      RC_CHECK_ARG(a->level_indptr && a->level_indptr[0] == 0 &&
+                       a->level_indptr[a->num_levels] == a->num_groups,
+                   "rc_extend_attention: level_indptr must run from 0 to num_groups");
+      for (int l = 0; l < a->num_levels; ++l)
+        RC_CHECK_ARG(a->level_indptr[l + 1] > a->level_indptr[l],
+                     "rc_extend_attention: level %d holds no group", l);
+    }
   }
   int* st = rc::device_status_ptr();
   if (!st) return rc::fail(RC_ERR_CUDA, "rc_extend_attention: no device status word");

@@ -94,11 +94,15 @@ struct TcParams {
   float scale2;      // sm_scale * log2(e)
   int pass;          // 0: one request per CTA z; 1: stacked prefix pass, one group per CTA z
   float* lse_part;   // [T, Hq] log2-sum-exp of the stacked pass's partial results
+  int group_lo;      // stacked pass: group of CTA z = group_lo + z (one launch per level)
+  int nlevels;       // levels of stacking groups (>= 1 when num_groups > 0)
+  int level_lo[RC_MAX_STACK_LEVELS + 1];   // groups of level l: [level_lo[l], level_lo[l+1])
 };
 
-// Shared length of the group holding request b (ranges ascending and disjoint), 0 if none.
-__device__ __forceinline__ int group_shared_of(const rc_extend_args& a, int b) {
-  int lo = 0, hi = a.num_groups - 1;
+// Shared length of the group of groups [g0, g1) holding request b (ranges ascending and
+// disjoint within a level), 0 if none.
+__device__ __forceinline__ int group_shared_of(const rc_extend_args& a, int b, int g0, int g1) {
+  int lo = g0, hi = g1 - 1;
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
     if (b < a.group_range[2 * mid]) hi = mid - 1;
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const bool stacked = kStack && p.pass == 1;
   int b, qo, S, P, row, kstart = 0;
   if (stacked) {
-    const int g = blockIdx.z;
+    const int g = p.group_lo + blockIdx.z;
     const int b0 = a.group_range[2 * g], b1 = a.group_range[2 * g + 1];
     if (b0 < 0 || b1 <= b0 || b1 > a.num_reqs) {
       if (threadIdx.x == 0 && blockIdx.x == 0 && hk == 0) set_status(p.status, kStatusPosRange);
@@ -303,8 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (a.prefix_len[bb] < P) set_status(p.status, kStatusPosRange);
     }
     if (S <= 0 || iA >= S) return;
+    // a deeper level covers only the keys after its parent's shared prefix
+    kstart = a.group_start ? a.group_start[g] : 0;
     if (P < 1 || P > a.prefix_len[b0] || P > a.max_ctx || row < 0 || row >= a.max_reqs ||
-        qo < 0 || (int64_t)qo + S > a.num_tokens) {
+        qo < 0 || (int64_t)qo + S > a.num_tokens || kstart < 0 || kstart >= P) {
       if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
       return;
     }
@@ -321,15 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       return;
     }
     if (kStack && a.num_groups > 0) {
-      kstart = group_shared_of(a, b);
+      for (int l = 0; l < p.nlevels; ++l)   // the deepest group holding b shares the most
+        kstart = max(kstart, group_shared_of(a, b, p.level_lo[l], p.level_lo[l + 1]));
       if (kstart < 0 || kstart > P) {
         if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
         kstart = 0;
       }
     }
   }
-  // rows merged with the stacked pass's partial result in the epilogue
-  const bool merge = kStack && !stacked && kstart > 0;
+  // rows merged in the epilogue with the partial result the stacked passes before left: the
+  // per-request pass after any group, a deeper level's stacked pass after its parent's
+  const bool merge = kStack && kstart > 0;
   const int iB = iA + p.ppt;
   const int nposA = min(p.ppt, S - iA);
   const int nposB = max(0, min(p.ppt, S - iB));
@@ -870,13 +878,24 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   p.scale2 = a->sm_scale * kLog2e;
   p.lse_part = (float*)a->workspace;
   int launches = 0;
+  p.group_lo = 0;
+  p.nlevels = a->num_levels > 1 ? a->num_levels : 1;
+  p.level_lo[0] = 0;
+  p.level_lo[1] = a->num_groups;
+  if (a->num_levels > 1)
+    for (int l = 0; l <= a->num_levels; ++l) p.level_lo[l] = a->level_indptr[l];
   if (a->num_groups > 0) {
-    // stacked prefix pass first: every group member's partial result is in place before the
-    // per-request pass merges it (same stream)
+    // stacked prefix passes first, level by level: every member's partial result over the keys
+    // above is in place before the next level (or the per-request pass) merges into it (same
+    // stream)
     p.pass = 1;
-    dim3 g1((a->max_group_rows + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_groups);
-    extend_tc_kernel<true><<<g1, kThreads, SmemLayout::ALLOC, s>>>(p);
-    ++launches;
+    for (int l = 0; l < p.nlevels; ++l) {
+      p.group_lo = p.level_lo[l];
+      dim3 g1((a->max_group_rows + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads,
+              p.level_lo[l + 1] - p.level_lo[l]);
+      extend_tc_kernel<true><<<g1, kThreads, SmemLayout::ALLOC, s>>>(p);
+      ++launches;
+    }
   }
   p.pass = 0;
   dim3 grid((a->max_q_len + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_reqs);

@@ -22,8 +22,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
-               extend_workspace_bytes, kv_copy, prefix_stacking_groups, shared_context_groups,
-               stacking_pays)
+               extend_workspace_bytes, kv_copy, prefix_stacking_levels, shared_context_groups,
+               stacking_pays, MAX_STACK_LEVELS)
 from .runtime import DeviceKV, HostCache, Plan
 
 
@@ -65,7 +65,8 @@ STACK_MIN_SHARED = 256
 class Engine:
     def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
                  max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True,
-                 stack_extend=True, host_tier_slots=0, host_planes=None):
+                 stack_extend=True, host_tier_slots=0, host_planes=None,
+                 stack_levels=MAX_STACK_LEVELS):
         self.layers = layers
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
         self.sm_scale = 1.0 / float(np.sqrt(head_dim))
@@ -92,6 +93,7 @@ class Engine:
         # extend stacks the new tokens of consecutive requests over a prefix they share, where
         # that is estimated to pay (True), for every group found ("always"), or never (False)
         self.stack_extend = stack_extend
+        self.stack_levels = stack_levels   # tree levels stacked (1: the shallowest group only)
         self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
@@ -132,21 +134,16 @@ class Engine:
         batch = ExtendBatch(plan, row_ids, qo, pl, ri, ol, int(S.max()) if B else 0,
                             int(plan.prefix_len.max()) if B else 0)
         if self.stack_extend and B > 1:
-            ranges, shared, max_rows = prefix_stacking_groups(plan.rows, plan.prefix_len, S,
-                                                              STACK_MIN_SHARED)
-            # keep the groups whose stacked pass is estimated to pay
+            # stacking groups over the levels of the tree, each kept where it is estimated to pay
             G = self.n_q_heads // self.n_kv_heads
-            keep = [g for g in range(len(shared))
-                    if self.stack_extend == "always" or stacking_pays(
-                        plan.prefix_len[ranges[2 * g]:ranges[2 * g + 1]],
-                        S[ranges[2 * g]:ranges[2 * g + 1]], int(shared[g]), G)]
-            ranges = ranges.reshape(-1, 2)[keep].reshape(-1)
-            shared = shared[keep]
-            max_rows = max([int(S[ranges[2 * g]:ranges[2 * g + 1]].sum())
-                            for g in range(len(shared))], default=0)
+            plen = plan.prefix_len
+            pays = None if self.stack_extend == "always" else (
+                lambda b0, b1, sh, st: stacking_pays(plen[b0:b1], S[b0:b1], sh, G, st))
+            ranges, shared, start, level_indptr, max_rows = prefix_stacking_levels(
+                plan.rows, plen, S, STACK_MIN_SHARED, pays, self.stack_levels)
             if len(shared):
-                r, sh = self.dev.upload_i32([ranges, shared])
-                batch.stack = (r, sh, max_rows)
+                r, sh, st = self.dev.upload_i32([ranges, shared, start])
+                batch.stack = (r, sh, max_rows, st, level_indptr)
                 need = extend_workspace_bytes(plan.num_tokens, self.n_q_heads)
                 if self._ext_ws is None or self._ext_ws.numel() < need:
                     self._ext_ws = self.dev.torch.empty(need, dtype=self.dev.torch.uint8,

@@ -279,6 +279,32 @@ def fork_mixed_step(seed: int = 0, layers: int = 32, pool_slots: int = 300_000,
     return ForkMixed(w, programs, dec, n_forks, suffix_len, seed)
 
 
+def tree_extend(seed: int = 0, root_len: int = 1024, n_branches: int = 16,
+                branch_len: int = 1024, per_branch: int = 4, new_len: int = 16,
+                pool_slots: int = 100_000) -> Workload:
+    """A two-level sharing tree (32 x 128 MHA bf16, 1 layer): a `root_len`-token system prompt
+    shared by every request, `n_branches` branches that add `branch_len` tokens of their own
+    (a document or conversation per branch), `per_branch` requests per branch adding
+    `new_len` new tokens each. The root and the branches are cached beforehand; the extend
+    batch lists the requests branch by branch."""
+    m = Model(1, 32, 32, 128, "bf16", seed)
+    root = tokens(seed, 8000, root_len)
+    taken = set()
+    cache, seqs = [root], []
+    for b in range(n_branches):
+        br = _first_distinct(seed, tokens(seed, 8100 + b, branch_len), taken, 8300 + b)
+        cache.append(np.concatenate([root, br]))
+        qt = set()
+        for k in range(per_branch):
+            own = _first_distinct(seed, tokens(seed, 8500 + per_branch * b + k, new_len), qt,
+                                  9500 + per_branch * b + k)
+            seqs.append(np.concatenate([root, br, own]))
+    w = Workload("tree_extend", m, pool_slots, permutation(seed, pool_slots),
+                 max_ctx=_round16(root_len + branch_len + new_len))
+    w.phases = [Phase("cache", cache), Phase("extend", seqs)]
+    return w
+
+
 @dataclass
 class ProgramQueue:
     """A waiting queue of extend requests (full sequences, queue order) for batch formation."""
@@ -330,4 +356,5 @@ CONFIGS = {
     "two_level_extend": two_level_extend,
     "multi_turn_decode": multi_turn_decode,
     "fork_mixed_step": fork_mixed_step,
+    "tree_extend": tree_extend,
 }

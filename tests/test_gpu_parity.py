@@ -541,3 +541,42 @@ def test_program_queue_with_host_tier(policy):
     if fcfs:
         assert loaded > 0
     _status_clear()
+
+
+def _tree_families(seed, root, branches, leaves, news):
+    """A three-level family: `root` tokens shared by all requests; `branches` branches add their
+    own cached tokens; each branch holds `leaves` leaf groups adding more; each leaf group has
+    one request per entry of `news` (its new tokens). Returns (cache seqs, extend seqs)."""
+    r = synth.tokens(seed, 900, root)
+    cache, ext = [r], []
+    for bi, bl in enumerate(branches):
+        b = np.concatenate([r, synth.tokens(seed, 910 + bi, bl)])
+        cache.append(b)
+        for li, ll in enumerate(leaves):
+            lf = np.concatenate([b, synth.tokens(seed, 950 + 10 * bi + li, ll)])
+            cache.append(lf)
+            for k, n in enumerate(news):
+                own = synth.tokens(seed, 2000 + 100 * bi + 10 * li + k, n)
+                ext.append(np.concatenate([lf, own]).astype(np.int32))
+    return cache, ext
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4)])
+def test_extend_prefix_stacking_cascade(Hq, Hkv):
+    """Stacking over three tree levels (root shared by all, branches, leaf groups): each deeper
+    level's stacked pass covers only its own keys and merges into the partial above; every unit
+    within tolerance of the oracle."""
+    m = W.Model(1, Hq, Hkv, 128, "bf16", 12)
+    cache, ext = _tree_families(12, 600, [300, 280], [260, 300], [1, 17, 40])
+    w = W.Workload("ext_cascade", m, 40_000, synth.permutation(12, 40_000), max_ctx=2048)
+    eng = H.make_engine(w, max_reqs=64, stack_extend="always")
+    for c in cache:
+        H.run_cache_phase(eng, m, [c])
+    b, outs = H.run_extend_phase(eng, m, ext, lse=True)
+    assert b.stack is not None
+    _, shared, _, start, level_indptr = b.stack
+    assert level_indptr.tolist() == [0, 1, 3, 7]          # 1 root, 2 branch, 4 leaf groups
+    assert start.cpu().tolist() == [0, 600, 600, 900, 900, 880, 880]
+    _status_clear()
+    units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
+    _check_extend(w, b, outs, ext, units)

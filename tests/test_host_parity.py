@@ -619,3 +619,41 @@ def test_program_queue_with_host_tier_matches_oracle(fcfs, size):
     else:
         # longest shared prefix first finishes a program before leaving it: little to reload
         assert computed <= without
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_prefix_stacking_levels_are_valid(seed):
+    """Nested stacking groups: within a level ranges ascend and are disjoint; each deeper group
+    lies inside a group of the level above and starts at that group's shared length; members
+    agree with the group's first over [0, shared), shared >= start + min_shared."""
+    rnd = random.Random(400 + seed)
+    B, width, min_shared = rnd.randint(2, 24), 120, 8
+    rows = np.zeros((B, width), np.int32)
+    base = [rnd.randrange(1000) for _ in range(width)]
+    for b in range(B):
+        # nested agreement: a random cut sequence along the sorted requests
+        cut = rnd.choice([10, 30, 60, 90, 119]) if b % rnd.randint(1, 4) else rnd.randint(0, 40)
+        rows[b] = base
+        rows[b, cut:] = [rnd.randrange(1000, 2000) for _ in range(width - cut)]
+    P = np.full(B, width, np.int64)
+    S = np.array([rnd.randint(0, 30) for _ in range(B)], np.int64)
+    ranges, shared, start, lvl, max_rows = rc.prefix_stacking_levels(rows, P, S, min_shared)
+    assert lvl[0] == 0 and lvl[-1] == len(shared) and np.all(np.diff(lvl) > 0)
+    spans = {}
+    for l in range(len(lvl) - 1):
+        prev_end = 0
+        for g in range(lvl[l], lvl[l + 1]):
+            b0, b1, sh, st = int(ranges[2 * g]), int(ranges[2 * g + 1]), int(shared[g]), int(start[g])
+            assert prev_end <= b0 < b1 and b1 - b0 >= 2
+            prev_end = b1
+            assert sh >= st + min_shared
+            for b in range(b0, b1):
+                assert np.array_equal(rows[b, :sh], rows[b0, :sh])
+            if l == 0:
+                assert st == 0
+            else:
+                parents = [(p0, p1, psh) for (p0, p1, psh) in spans[l - 1] if p0 <= b0 and b1 <= p1]
+                assert len(parents) == 1 and parents[0][2] == st
+            spans.setdefault(l, []).append((b0, b1, sh))
+    assert max_rows == max([int(S[int(ranges[2 * g]):int(ranges[2 * g + 1])].sum())
+                            for g in range(len(shared))], default=0)
