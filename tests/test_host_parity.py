@@ -657,3 +657,49 @@ def test_prefix_stacking_levels_are_valid(seed):
             spans.setdefault(l, []).append((b0, b1, sh))
     assert max_rows == max([int(S[int(ranges[2 * g]):int(ranges[2 * g + 1])].sum())
                             for g in range(len(shared))], default=0)
+
+
+def test_new_entry_points_reject_bad_arguments():
+    """Argument checks of the scheduler, the host tier and the KV copy (host side; nothing here
+    reaches a device)."""
+    import ctypes
+    from prefix_cached_paged_gb300._lib import RcKvCopyArgs
+    pool, hpool = rc.Pool(50), rc.Pool(20)
+    t = rc.RadixTree(pool)
+    # the scheduler: unknown policy, match longer than the sequence
+    tok = np.arange(6, dtype=np.int32)
+    ip = np.array([0, 6], np.int64)
+    with pytest.raises(rc.RcError) as e:
+        t.schedule_batch(tok, ip, None, policy=7)
+    assert e.value.code == rc.RC_ERR_INVALID
+    with pytest.raises(rc.RcError):
+        t.schedule_batch(tok, ip, np.array([7], np.int32))
+    # loads need a host tier; a tier is attached once and is not the device pool
+    rows = np.zeros((1, 8), np.int32)
+    with pytest.raises(rc.RcError):
+        t.load_batch(tok, ip, rows, np.zeros(1, np.int32), np.zeros(1, np.int32))
+    with pytest.raises(rc.RcError):
+        t.attach_host_tier(pool)
+    t.attach_host_tier(hpool)
+    with pytest.raises(rc.RcError):
+        t.attach_host_tier(rc.Pool(5))
+    # a load asks for more device slots than are free: RC_ERR_OOM, nothing moved
+    t.insert(list(range(6)), pool.alloc(6))
+    assert t.evict_lru(6) == (rc.RC_OK, 6)           # spilled to the host tier
+    assert t.drain_copies()[0].size == 6
+    pl, nodes, hl = t.match_batch_tiered(tok, ip, None, rows)
+    assert (int(pl[0]), int(hl[0])) == (0, 6)
+    pool.alloc(pool.available() - 3)
+    with pytest.raises(rc.RcError) as e:
+        t.load_batch(tok, ip, rows, pl, hl)
+    assert e.value.code == rc.RC_ERR_OOM and pl[0] == 0
+    # the KV copy: rows not a multiple of 16 bytes, NULL planes, misaligned planes
+    def kv(**kw):
+        a = dict(n=1, layers=1, row_bytes=256, src_slots=16, dst_slots=16, src_k=256, src_v=512,
+                 src_num_slots=4, dst_k=768, dst_v=1024, dst_num_slots=4)
+        a.update(kw)
+        return lib().rc_kv_copy(ctypes.byref(RcKvCopyArgs(**a)), None)
+    assert kv(row_bytes=100) == rc.RC_ERR_INVALID
+    assert kv(src_k=0) == rc.RC_ERR_INVALID
+    assert kv(dst_v=1032) == rc.RC_ERR_INVALID
+    assert kv(layers=0) == rc.RC_ERR_INVALID
