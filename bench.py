@@ -483,6 +483,8 @@ def bench_ours(args, rank, world, local):
                                    "hit_rate": round(skipped / max(prompt, 1), 4)},
         "evicted_tokens_per_step": int(np.mean([p.plan.evicted for p in plans])),
         "host_ms_per_step": round(1e3 * float(np.mean(host_t)), 3),
+        "layers_ms_median": round(float(np.median(
+            [e[0][0].elapsed_time(e[m.layers - 1][2]) for e in evs])), 3),
         "extend_ms_per_step": round(ext_ms / args.steps, 3),
         "decode_ms_per_step": round(dec_ms / args.steps, 3),
         "roofline": roof_dec if dom_is_decode else roof_ext,
@@ -526,7 +528,13 @@ def cpu_baseline(ctx, args, budget_s=None):
         oracle.attention_units(units, m.sm_scale, 1, 1, threads)
         dt += time.perf_counter() - t1
         reps += 1
+    # the same oracle on one core, two units
+    t1 = time.perf_counter()
+    oracle.attention_units(units[:2], m.sm_scale, 1, 1, 1)
+    one = time.perf_counter() - t1
+    one_flops = flops * 2 / n_units
     return {"value": round(flops * reps / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "single_core_value": round(one_flops / one / 1e12, 6),
             "kind": "oracle",
             "sample": f"{n_units} extend units (request x layer x head: 200 queries over 1700 "
                       f"keys, fp64) of the fork mixed step, x{reps} passes, {dt:.1f} s"}
