@@ -382,6 +382,11 @@ typedef struct rc_decode_args {
   const int32_t* group_indptr;   /* [num_groups + 1] */
   const int32_t* group_members;  /* [group_indptr[num_groups]] request indices */
   const int32_t* group_shared;   /* [num_groups] tokens of shared context */
+  /* 1: skip the plan (the job list in the workspace) and reuse the one the previous call on this
+   * workspace made -- the layers of one decode step share it. The caller guarantees that call had
+   * the same num_reqs, seq_len, req_idx contents, groups, kv_chunk and max_total_tokens, and that
+   * it completed without a status error. bf16 only; the fp32 path always plans. */
+  int32_t reuse_plan;
 } rc_decode_args;
 /* Workspace bytes rc_decode_attention needs for these arguments (device memory, 256-B aligned,
  * no initialisation needed). */

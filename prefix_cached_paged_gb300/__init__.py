@@ -372,12 +372,15 @@ def decode_workspace_bytes(q, k_new, req_to_token, k_pool, *, max_total_tokens, 
 
 def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
                      o, workspace, *, sm_scale, max_total_tokens, kv_chunk=0, lse=None,
-                     groups=None, stream=None):
+                     groups=None, stream=None, reuse_plan=False):
     """Split-K decode attention of one layer (see rc_decode_attention). workspace: a uint8 CUDA
     tensor of at least decode_workspace_bytes(...) bytes. groups: optional shared-context groups
-    (indptr, members, shared), int32 CUDA tensors, as built by shared_context_groups()."""
+    (indptr, members, shared), int32 CUDA tensors, as built by shared_context_groups().
+    reuse_plan: the previous call on this workspace had the same requests and sizes (the other
+    layers of a decode step) -- its job list is reused."""
     a = _decode_args(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k_pool, v_pool,
                      o, lse, sm_scale, max_total_tokens, kv_chunk, groups)
+    a.reuse_plan = 1 if reuse_plan else 0
     check(lib().rc_decode_attention(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "rc_decode_attention")

@@ -104,7 +104,7 @@ class RcDecodeArgs(ctypes.Structure):
                 ("out_loc", _P), ("seq_len", _P), ("req_idx", _P), ("req_to_token", _P),
                 ("k_pool", _P), ("v_pool", _P), ("o", _P), ("lse", _P),
                 ("num_groups", _I32), ("group_indptr", _P), ("group_members", _P),
-                ("group_shared", _P)]
+                ("group_shared", _P), ("reuse_plan", _I32)]
 
 
 _lib = None

@@ -22,6 +22,7 @@
 //     them.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "host_common.h"
@@ -35,7 +36,7 @@ constexpr int kWarps = 4;    // warps per CTA
 constexpr int kDefaultChunk = 512;
 
 struct Workspace {
-  int* njobs;     // [0]: jobs written, [1]: item counter
+  int* njobs;     // [0]: jobs written, [1]: item counter, [2]: warps finished (bf16 kernel)
   int* pbase;     // [B+1]: request b's partial states are slots pbase[b] + chunk
   int* group_of;  // [B]: shared-context group of each request, -1 for none
   int4* jobs;     // [max_jobs] (request, chunk, group of a stacked chunk or -1, 0)
@@ -51,7 +52,7 @@ Workspace carve(void* base, int B, int G, int D, int64_t max_jobs, int Hkv, size
   char* p = (char*)base;
   size_t off = 0;
   w.njobs = (int*)(p + off);
-  off += align256(2 * sizeof(int));
+  off += align256(3 * sizeof(int));
   w.pbase = (int*)(p + off);
   off += align256((size_t)(B + 1) * sizeof(int));
   w.group_of = (int*)(p + off);
@@ -169,6 +170,7 @@ __global__ void decode_plan_kernel(Params p) {
     p.w.pbase[B] = run_p;
     p.w.njobs[0] = (int)min((int64_t)run_j, p.w.max_jobs);
     p.w.njobs[1] = 0;
+    p.w.njobs[2] = 0;
   }
 }
 
@@ -519,6 +521,19 @@ __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
   return *(const uint32_t*)&v;
 }
 
+// A warp leaves the persistent loop: the last one of the grid resets the item counter, so a
+// later call that reuses the plan hands out the items again.
+__device__ __forceinline__ void retire_warp(const Params& p, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(&p.w.njobs[2], 1) == (int)gridDim.x * kWarps - 1) {
+      p.w.njobs[1] = 0;
+      p.w.njobs[2] = 0;
+    }
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
   using C = MmaCfg<D>;
@@ -723,6 +738,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
     }
     if (!ok) {
       asm volatile("cp.async.wait_all;" ::: "memory");   // no copy lands after the exit
+      retire_warp(p, lane);
       return;
     }
     // ---- epilogue: full denominators per head, then O^T columns -> output rows
@@ -816,6 +832,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_mma_kernel(Params p) {
     }
     __syncwarp();
   }
+  retire_warp(p, lane);
 }
 
 // ---------------------------------------------------------------- merge
@@ -909,12 +926,20 @@ int launch_t(const Params& p, cudaStream_t s) {
   });
   if (init_err != cudaSuccess)
     return fail(RC_ERR_CUDA, "rc_decode_attention: setup: %s", cudaGetErrorString(init_err));
-  decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+  // bf16 can reuse the plan of the previous call (the main kernel leaves the item counter reset)
+  constexpr bool kMma = std::is_same<T, __nv_bfloat16>::value;
+  int n = 0;
+  if (!(kMma && p.a.reuse_plan)) {
+    decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+    ++n;
+  }
   const int grid = std::max(1, num_sms * std::max(1, blocks_per_sm));
   kern<<<grid, kWarps * 32, C::SMEM, s>>>(p);
+  ++n;
   dim3 mg(p.a.num_reqs, p.a.num_q_heads);
   decode_merge_kernel<T, D, G><<<mg, D, 0, s>>>(p);
-  count_launches(3);
+  ++n;
+  count_launches(n);
   return check_launch("rc_decode_attention");
 }
 

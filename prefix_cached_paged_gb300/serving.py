@@ -56,6 +56,7 @@ class DecodeBatch:
     dev_out_loc: object = None
     groups: object = None   # device (indptr, members, shared) of shared-context groups, or None
     num_groups: int = 0
+    step_id: object = None  # identity of the current step's lengths (a fresh object per step)
 
 
 # shortest shared prefix worth a stacked pass: two key tiles
@@ -97,6 +98,7 @@ class Engine:
         self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
+        self._ws_plan = None   # (step id, workspace address, token bound) of the plan in _ws
 
     def _tier_copies(self, copies):
         """Perform the host tier's owed copies on the stream: spills (device -> host) before
@@ -203,6 +205,7 @@ class Engine:
         self.dev.write_rows(batch.row_ids, rows, cols + 1, cols=cols)
         batch.seq_len = batch.seq_len + 1
         batch.new_slots = np.asarray(new_slots, dtype=np.int32)
+        batch.step_id = object()   # the lengths changed: the next layer plans again
         batch.dev_seq_len, batch.dev_req_idx, batch.dev_out_loc = self.dev.upload_i32(
             [batch.seq_len, batch.row_ids, batch.new_slots])
         return batch
@@ -219,10 +222,17 @@ class Engine:
                      max_total_tokens=None):
         mt = int(batch.seq_len.sum()) if max_total_tokens is None else max_total_tokens
         ws = self.workspace(q, k_new, mt)
+        # every layer of a step has the same requests and lengths: the first plans, the others
+        # reuse its job list (same workspace, same bound)
+        key = (batch.step_id, ws.data_ptr(), mt)
+        reuse = batch.step_id is not None and self._ws_plan is not None and \
+            self._ws_plan[0] is key[0] and self._ws_plan[1:] == key[1:]
         decode_attention(q, k_new, v_new, batch.dev_out_loc, batch.dev_seq_len,
                          batch.dev_req_idx, self.dev.req_to_token, self.dev.k[layer],
                          self.dev.v[layer], o, ws, sm_scale=self.sm_scale, max_total_tokens=mt,
-                         kv_chunk=self.kv_chunk, lse=lse, groups=batch.groups)
+                         kv_chunk=self.kv_chunk, lse=lse, groups=batch.groups,
+                         reuse_plan=reuse)
+        self._ws_plan = key     # the workspace now holds this step's plan
 
     def decode_end(self, batch: DecodeBatch):
         for n in batch.nodes:

@@ -580,3 +580,43 @@ def test_extend_prefix_stacking_cascade(Hq, Hkv):
     _status_clear()
     units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
     _check_extend(w, b, outs, ext, units)
+
+
+@pytest.mark.parametrize("groups", [False, True])
+def test_decode_plan_reuse_across_layers(groups):
+    """The layers of a decode step reuse the first layer's plan (job list; the main kernel leaves
+    its item counter reset): every layer's output and LSE are bit-identical to a call that plans
+    afresh, and within tolerance of the oracle."""
+    import torch
+    import prefix_cached_paged_gb300 as rc
+    L = [70, 600, 1500, 1501, 2900, 3000, 513, 64]
+    m = W.Model(3, 16, 4, 128, "bf16", 6)
+    base = synth.tokens(6, 77, 2000)
+    seqs = [np.concatenate([base[:min(n, 1700)], synth.tokens(6, 80 + i, max(n - 1700, 0))])
+            .astype(np.int32)[:n] for i, n in enumerate(L)]
+    w = W.Workload("dec_reuse", m, 30_000, synth.permutation(6, 30_000), max_ctx=3008)
+    eng = H.make_engine(w, max_reqs=32, kv_chunk=256, share_decode=groups)
+    H.run_cache_phase(eng, m, [s[:-1] for s in seqs])
+    db, outs = H.run_decode(eng, m, seqs, lse=True)
+    assert (db.num_groups > 0) == groups
+    h = np.array([synth.prefix_hashes(m.seed, s)[-1] for s in seqs], dtype=np.uint64)
+    from synth import device as sdev
+    hd = sdev.hashes_to_device(h)
+    mt = int(db.seq_len.sum())
+    for layer in range(m.layers):
+        q, k, v = H.dense_qkv(m, hd, layer, len(seqs))
+        o = torch.empty_like(q)
+        lse = torch.empty((len(seqs), m.n_q_heads), dtype=torch.float32, device="cuda")
+        ws = torch.empty(rc.decode_workspace_bytes(q, k, eng.dev.req_to_token, eng.dev.k[0],
+                                                   max_total_tokens=mt, kv_chunk=256),
+                         dtype=torch.uint8, device="cuda")
+        rc.decode_attention(q, k, v, db.dev_out_loc, db.dev_seq_len, db.dev_req_idx,
+                            eng.dev.req_to_token, eng.dev.k[layer], eng.dev.v[layer], o, ws,
+                            sm_scale=eng.sm_scale, max_total_tokens=mt, kv_chunk=256, lse=lse,
+                            groups=db.groups)
+        assert torch.equal(o, outs[layer][0]), layer
+        assert torch.equal(lse, outs[layer][1]), layer
+    _check_decode(w, db, outs, seqs, [(i, l, hh) for i in range(len(L)) for l in range(3)
+                                      for hh in range(4)])
+    _status_clear()
+
