@@ -329,6 +329,17 @@ typedef struct rc_extend_args {
   int32_t num_levels;
   const int32_t* level_indptr;
   const int32_t* group_start;
+  /* Optional folding of short remainders into the stacked pass. group_fold[g] = 1 (device int32
+   * [num_groups], NULL = none) marks a group that no deeper group lies inside and whose every
+   * member b has at most 128 keys left after the shared prefix (prefix_len[b] - group_shared[g]
+   * + its new tokens <= 128): its stacked pass then also attends each member's rows to that
+   * remainder (one 128-key tile per member: its own cached tokens after the shared prefix, then
+   * its new tokens, causally), writes the final outputs and scatters the new K/V, and the
+   * per-request pass leaves its members alone. skip_request_pass = 1 (host flag) when every
+   * request is in a folded group: the per-request pass is not launched. A folded member whose
+   * remainder exceeds 128 keys is reported through the status word. */
+  const int32_t* group_fold;
+  int32_t skip_request_pass;
 } rc_extend_args;
 #define RC_MAX_STACK_LEVELS 4
 int rc_extend_workspace_bytes(const rc_extend_args* args, size_t* out_bytes);

@@ -300,11 +300,14 @@ def _extend_args(q, k_new, v_new, out_loc, qo_indptr, prefix_len, req_idx, req_t
                  workspace=0 if workspace is None else workspace.data_ptr(),
                  workspace_bytes=0 if workspace is None else
                  workspace.numel() * workspace.element_size())
-        if len(stack) == 5:
+        if len(stack) >= 5:
             start, level_indptr = stack[3], stack[4]
             assert level_indptr.dtype == np.int32 and level_indptr.flags.c_contiguous
             g.update(num_levels=len(level_indptr) - 1, level_indptr=level_indptr.ctypes.data,
                      group_start=start.data_ptr())
+        if len(stack) >= 7 and stack[5] is not None:
+            # (..., group_fold device int32 [G], every request folded)
+            g.update(group_fold=stack[5].data_ptr(), skip_request_pass=int(bool(stack[6])))
     return RcExtendArgs(**g,
         dtype=_dtype_code(q), num_reqs=prefix_len.numel(), num_q_heads=Hq, num_kv_heads=Hkv,
         head_dim=d, max_reqs=req_to_token.shape[0], max_ctx=req_to_token.shape[1], max_q_len=int(max_q_len),
@@ -457,6 +460,32 @@ def prefix_stacking_groups(rows, prefix_len, new_len, min_shared: int):
 
 
 MAX_STACK_LEVELS = 4   # RC_MAX_STACK_LEVELS
+
+
+FOLD_KEYS = 128   # a folded member's remainder fits one key tile
+
+
+def fold_groups(ranges, shared, level_indptr, prefix_len, new_len):
+    """Groups whose stacked pass can also take their members' remainders (rc_extend_args
+    group_fold): no deeper group lies inside, and every member's keys past the shared prefix
+    (its own cached tokens, then its new tokens) fit one 128-key tile. Returns (fold int32 [G],
+    every request of the batch folded)."""
+    P = np.asarray(prefix_len, dtype=np.int64)
+    S = np.asarray(new_len, dtype=np.int64)
+    G = len(shared)
+    fold = np.zeros(G, np.int32)
+    level = np.zeros(G, np.int64)
+    for l in range(len(level_indptr) - 1):
+        level[level_indptr[l]:level_indptr[l + 1]] = l
+    covered = np.zeros(len(P), bool)
+    for g in range(G):
+        b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
+        inner = any(level[h] > level[g] and b0 <= ranges[2 * h] and ranges[2 * h + 1] <= b1
+                    for h in range(G))
+        if not inner and np.all(P[b0:b1] - int(shared[g]) + S[b0:b1] <= FOLD_KEYS):
+            fold[g] = 1
+            covered[b0:b1] = True
+    return fold, bool(covered.all())
 
 
 def prefix_stacking_levels(rows, prefix_len, new_len, min_shared: int, pays=None,

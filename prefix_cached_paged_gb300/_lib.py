@@ -93,7 +93,8 @@ class RcExtendArgs(ctypes.Structure):
                 ("o", _P), ("lse", _P), ("num_groups", _I32), ("max_group_rows", _I32),
                 ("group_range", _P), ("group_shared", _P), ("workspace", _P),
                 ("workspace_bytes", ctypes.c_size_t), ("num_levels", _I32),
-                ("level_indptr", _P), ("group_start", _P)]
+                ("level_indptr", _P), ("group_start", _P), ("group_fold", _P),
+                ("skip_request_pass", _I32)]
 
 
 class RcDecodeArgs(ctypes.Structure):

@@ -99,17 +99,30 @@ struct TcParams {
   int level_lo[RC_MAX_STACK_LEVELS + 1];   // groups of level l: [level_lo[l], level_lo[l+1])
 };
 
-// Shared length of the group of groups [g0, g1) holding request b (ranges ascending and
-// disjoint within a level), 0 if none.
-__device__ __forceinline__ int group_shared_of(const rc_extend_args& a, int b, int g0, int g1) {
+// The group among groups [g0, g1) holding request b (ranges ascending and disjoint within a
+// level), -1 if none.
+__device__ __forceinline__ int group_index_of(const rc_extend_args& a, int b, int g0, int g1) {
   int lo = g0, hi = g1 - 1;
   while (lo <= hi) {
     const int mid = (lo + hi) >> 1;
     if (b < a.group_range[2 * mid]) hi = mid - 1;
     else if (b >= a.group_range[2 * mid + 1]) lo = mid + 1;
-    else return a.group_shared[mid];
+    else return mid;
   }
-  return 0;
+  return -1;
+}
+
+// The request among [b0, b1) whose new tokens hold stacked position pos (positions counted from
+// qo_indptr[b0] = qo): the last one starting at or before pos.
+__device__ __forceinline__ int request_of_pos(const rc_extend_args& a, int b0, int b1, int qo,
+                                              int pos) {
+  int lo = b0, hi = b1 - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.qo_indptr[mid] - qo <= pos) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -290,6 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // members, stacked in batch order, against keys [0, shared) only.
   const bool stacked = kStack && p.pass == 1;
   int b, qo, S, P, row, kstart = 0;
+  // folded stacked pass: the CTA also takes each of its members' remainders (one key tile per
+  // member, members r_first .. r_first + n_rem - 1 of the group [gb0, gb1)) and is final
+  bool fold = false;
+  int gb0 = 0, gb1 = 0, r_first = 0, n_rem = 0;
   if (stacked) {
     const int g = p.group_lo + blockIdx.z;
     const int b0 = a.group_range[2 * g], b1 = a.group_range[2 * g + 1];
@@ -302,13 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     S = a.qo_indptr[b1] - qo;
     P = a.group_shared[g];
     row = a.req_idx[b0];
+    fold = a.group_fold && a.group_fold[g];
+    gb0 = b0;
+    gb1 = b1;
     if (threadIdx.x == 0 && blockIdx.x == 0 && hk == 0) {
-      for (int bb = b0; bb < b1; ++bb)   // every member matched the shared prefix
+      for (int bb = b0; bb < b1; ++bb) {  // every member matched the shared prefix
         if (a.prefix_len[bb] < P) set_status(p.status, kStatusPosRange);
+        // a folded member's remainder fits one key tile
+        if (fold && a.prefix_len[bb] - P + (a.qo_indptr[bb + 1] - a.qo_indptr[bb]) > kN)
+          set_status(p.status, kStatusPosRange);
+      }
     }
     if (S <= 0 || iA >= S) return;
     // a deeper level covers only the keys after its parent's shared prefix
     kstart = a.group_start ? a.group_start[g] : 0;
+    if (fold) {
+      r_first = request_of_pos(a, b0, b1, qo, iA);
+      n_rem = request_of_pos(a, b0, b1, qo, min(iA + 2 * p.ppt, S) - 1) - r_first + 1;
+    }
     if (P < 1 || P > a.prefix_len[b0] || P > a.max_ctx || row < 0 || row >= a.max_reqs ||
         qo < 0 || (int64_t)qo + S > a.num_tokens || kstart < 0 || kstart >= P) {
       if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
@@ -327,8 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       return;
     }
     if (kStack && a.num_groups > 0) {
-      for (int l = 0; l < p.nlevels; ++l)   // the deepest group holding b shares the most
-        kstart = max(kstart, group_shared_of(a, b, p.level_lo[l], p.level_lo[l + 1]));
+      int deepest = -1;
+      for (int l = 0; l < p.nlevels; ++l) {   // the deepest group holding b shares the most
+        const int gi = group_index_of(a, b, p.level_lo[l], p.level_lo[l + 1]);
+        if (gi >= 0 && a.group_shared[gi] > kstart) {
+          kstart = a.group_shared[gi];
+          deepest = gi;
+        }
+      }
+      // a folded group's stacked pass computed its members completely
+      if (deepest >= 0 && a.group_fold && a.group_fold[deepest]) return;
       if (kstart < 0 || kstart > P) {
         if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
         kstart = 0;
@@ -344,8 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int n_pre = (P - kstart + kN - 1) / kN;     // prefix key tiles: keys [kstart, P)
   // key tiles of each query tile: the prefix, then (per-request pass) new-token keys up to its
   // last position
-  const int nA = n_pre + (stacked ? 0 : (iA + nposA + kN - 1) / kN);
-  const int nB = nposB > 0 ? n_pre + (stacked ? 0 : (iB + nposB + kN - 1) / kN) : 0;
+  const int nA = n_pre + (stacked ? n_rem : (iA + nposA + kN - 1) / kN);
+  const int nB = nposB > 0 ? n_pre + (stacked ? n_rem : (iB + nposB + kN - 1) / kN) : 0;
+  // the epilogue leaves a partial result (unfolded stacked pass) or the final one
+  const bool partial = stacked && !fold;
   const int ntiles = max(nA, nB);
   const int kend = nposB > 0 ? iB + nposB : iA + nposA;  // new-token keys loaded: [0, kend)
   // virtual tiles: pair mode (query tiles A and B, every key tile each) or split mode (query
@@ -422,14 +460,42 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t sbuf = (is_v ? sV : sK) + (uint32_t)(w * kRowsPerWarp * 128);
   // raw(j, q) only issues the slot load; rowptr() checks it when the tile is issued, so the
   // loads of tile j+1 stay in flight while tile j is being copied
+  // folded remainder tile j >= n_pre: member r_first + j - n_pre; its key k is its own cached
+  // token P + k while k < priv (= its prefix past the shared P), then its new token k - priv
+  auto fold_req = [&](int j) { return min(r_first + (j - n_pre), gb1 - 1); };
   auto raw = [&](int j, int q) -> int {
     if (j < n_pre) {
       const int key = kstart + j * kN + w * kRowsPerWarp + q * 32 + lane;
       return rt[key < P ? key : P - 1];
     }
+    if (fold) {
+      const int r = fold_req(j);
+      const int k = w * kRowsPerWarp + q * 32 + lane;
+      const int rr = a.req_idx[r];
+      if (k < a.prefix_len[r] - P && rr >= 0 && rr < a.max_reqs && P + k < a.max_ctx)
+        return a.req_to_token[(int64_t)rr * a.max_ctx + P + k];
+      return -1;   // a new token (or padding): resolved by rowptr
+    }
     return 0;
   };
   auto rowptr = [&](int j, int q, int rv) -> const __nv_bfloat16* {
+    if (fold && j >= n_pre) {
+      const int r = fold_req(j);
+      const int k = w * kRowsPerWarp + q * 32 + lane;
+      const int priv = a.prefix_len[r] - P;
+      if (k < priv) {
+        int sl = rv;
+        if (sl < 0 || (int64_t)sl >= a.num_slots) {
+          set_status(p.status, kStatusSlotRange);
+          sl = 0;
+        }
+        return pool + ((int64_t)sl * Hkv + hk) * kD;
+      }
+      // new token k - priv of member r (past its last: its last, masked anyway)
+      const int q0 = a.qo_indptr[r], nr = a.qo_indptr[r + 1] - q0;
+      const int tok = min(max(q0 + min(k - priv, nr - 1), 0), (int)a.num_tokens - 1);
+      return nsrc + ((int64_t)tok * Hkv + hk) * kD;
+    }
     if (j < n_pre) {
       int sl = rv;
       if (sl < 0 || (int64_t)sl >= a.num_slots) {
@@ -592,7 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const __nv_bfloat16* kn = (const __nv_bfloat16*)a.k_new;
     const __nv_bfloat16* vn = (const __nv_bfloat16*)a.v_new;
     constexpr int kU = 4;
-    const int total = stacked ? 0 : (nposA + nposB) * 16;   // the stacked pass writes no K/V
+    // an unfolded stacked pass writes no K/V (each member's own pass does)
+    const int total = partial ? 0 : (nposA + nposB) * 16;
     for (int base = (warp - kScatterWarp0) * 32 + lane; base < total; base += 32 * kScatterWarps * kU) {
       uint4 kv[kU], vv[kU];
       int64_t dst[kU];
@@ -632,6 +699,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const int iX = (X && !split) ? iB : iA;
     const int rows_used = ((X && !split) ? nposB : nposA) * G;
     const int ipos = min(iX + r / G, S - 1);          // this row's new-token index (clamped)
+    // folded stacked pass: the member this row belongs to and its index among that member's
+    // new tokens (the member's remainder tile is visible to it up to its own position)
+    int req_row = -1, i_row = 0;
+    if (fold) {
+      req_row = request_of_pos(a, gb0, gb1, qo, ipos);
+      i_row = ipos - (a.qo_indptr[req_row] - qo);
+    }
     const float sc2 = p.scale2;
     const uint64_t sc2x2 = f2pack(sc2, sc2);
     const uint32_t tS = tmem + X * 128 + lane_off;
@@ -645,8 +719,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       tc_fence_after();
       // keys [0, lim) of key tile kt are visible to this row (lim <= 0: none)
       const int kt = split ? 2 * j + X : j;
-      const int lim = kt < n_pre ? min(kN, P - kstart - kt * kN)
-                                 : min(kN, ipos - (kt - n_pre) * kN + 1);
+      int lim;
+      if (kt < n_pre) {
+        lim = min(kN, P - kstart - kt * kN);
+      } else if (fold) {
+        const int rk = min(r_first + (kt - n_pre), gb1 - 1);
+        lim = rk == req_row ? min(kN, a.prefix_len[rk] - P + i_row + 1) : 0;
+      } else {
+        lim = min(kN, ipos - (kt - n_pre) * kN + 1);
+      }
       float v[kN];
 #pragma unroll
       for (int c = 0; c < kN / 32; ++c) tmem_ld32(tS + c * 32, v + c * 32);
@@ -771,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           }
         }
         if (store) {
-          if (stacked) p.lse_part[rowidx] = lse2;
+          if (partial) p.lse_part[rowidx] = lse2;
           else if (a.lse) a.lse[rowidx] = lse2 * kLn2;
         }
       }
@@ -822,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           }
         }
         if (store && X == 0) {
-          if (stacked) p.lse_part[rowidx] = lse2;
+          if (partial) p.lse_part[rowidx] = lse2;
           else if (a.lse) a.lse[rowidx] = lse2 * kLn2;
         }
       }
@@ -899,11 +980,16 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   }
   p.pass = 0;
   dim3 grid((a->max_q_len + 2 * p.ppt - 1) / (2 * p.ppt), a->num_kv_heads, a->num_reqs);
-  if (a->num_groups > 0)
+  if (a->num_groups > 0 && a->skip_request_pass) {
+    // every request is in a folded group: the stacked passes computed everything
+  } else if (a->num_groups > 0) {
     extend_tc_kernel<true><<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
-  else
+    ++launches;
+  } else {
     extend_tc_kernel<false><<<grid, kThreads, SmemLayout::ALLOC, s>>>(p);
-  count_launches(launches + 1);
+    ++launches;
+  }
+  count_launches(launches);
   return check_launch("rc_extend_attention (tensor cores)");
 }
 

@@ -22,8 +22,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
-               extend_workspace_bytes, kv_copy, prefix_stacking_levels, shared_context_groups,
-               stacking_pays, MAX_STACK_LEVELS)
+               extend_workspace_bytes, fold_groups, kv_copy, prefix_stacking_levels,
+               shared_context_groups, stacking_pays, MAX_STACK_LEVELS)
 from .runtime import DeviceKV, HostCache, Plan
 
 
@@ -67,7 +67,7 @@ class Engine:
     def __init__(self, layers, n_q_heads, n_kv_heads, head_dim, dtype, num_slots, max_reqs,
                  max_ctx, initial_order=None, device="cuda", kv_chunk=0, share_decode=True,
                  stack_extend=True, host_tier_slots=0, host_planes=None,
-                 stack_levels=MAX_STACK_LEVELS):
+                 stack_levels=MAX_STACK_LEVELS, fold_extend=True):
         self.layers = layers
         self.n_q_heads, self.n_kv_heads, self.head_dim = n_q_heads, n_kv_heads, head_dim
         self.sm_scale = 1.0 / float(np.sqrt(head_dim))
@@ -95,6 +95,8 @@ class Engine:
         # that is estimated to pay (True), for every group found ("always"), or never (False)
         self.stack_extend = stack_extend
         self.stack_levels = stack_levels   # tree levels stacked (1: the shallowest group only)
+        # a stacked group whose members' remainders fit one key tile takes them in its own pass
+        self.fold_extend = fold_extend
         self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
         self._ws = None
@@ -144,8 +146,11 @@ class Engine:
             ranges, shared, start, level_indptr, max_rows = prefix_stacking_levels(
                 plan.rows, plen, S, STACK_MIN_SHARED, pays, self.stack_levels)
             if len(shared):
-                r, sh, st = self.dev.upload_i32([ranges, shared, start])
-                batch.stack = (r, sh, max_rows, st, level_indptr)
+                fold, all_folded = (fold_groups(ranges, shared, level_indptr, plen, S)
+                                    if self.fold_extend else (np.zeros(len(shared), np.int32),
+                                                              False))
+                r, sh, st, fo = self.dev.upload_i32([ranges, shared, start, fold])
+                batch.stack = (r, sh, max_rows, st, level_indptr, fo, all_folded)
                 need = extend_workspace_bytes(plan.num_tokens, self.n_q_heads)
                 if self._ext_ws is None or self._ext_ws.numel() < need:
                     self._ext_ws = self.dev.torch.empty(need, dtype=self.dev.torch.uint8,

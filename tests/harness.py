@@ -21,7 +21,7 @@ def torch_dtype(name):
 
 
 def make_engine(w, max_reqs=None, kv_chunk=0, share_decode=True, stack_extend=True,
-                host_tier_slots=0, host_planes=None, stack_levels=4):
+                host_tier_slots=0, host_planes=None, stack_levels=4, fold_extend=True):
     from prefix_cached_paged_gb300.serving import Engine
     m = w.model
     n_reqs = max_reqs or max(max((len(p.seqs) for p in w.phases), default=0) + 8, 64)
@@ -29,7 +29,7 @@ def make_engine(w, max_reqs=None, kv_chunk=0, share_decode=True, stack_extend=Tr
                   w.pool_slots, n_reqs, w.max_ctx, w.pool_order, kv_chunk=kv_chunk,
                   share_decode=share_decode, stack_extend=stack_extend,
                   host_tier_slots=host_tier_slots, host_planes=host_planes,
-                  stack_levels=stack_levels)
+                  stack_levels=stack_levels, fold_extend=fold_extend)
 
 
 def new_token_hashes(model, seqs, prefix_len):

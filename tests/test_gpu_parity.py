@@ -574,9 +574,12 @@ def test_extend_prefix_stacking_cascade(Hq, Hkv):
         H.run_cache_phase(eng, m, [c])
     b, outs = H.run_extend_phase(eng, m, ext, lse=True)
     assert b.stack is not None
-    _, shared, _, start, level_indptr = b.stack
+    shared, start, level_indptr, fold, all_folded = (b.stack[1], b.stack[3], b.stack[4],
+                                                     b.stack[5], b.stack[6])
     assert level_indptr.tolist() == [0, 1, 3, 7]          # 1 root, 2 branch, 4 leaf groups
     assert start.cpu().tolist() == [0, 600, 600, 900, 900, 880, 880]
+    # the leaf groups take their members' remainders; no per-request pass is left
+    assert fold.cpu().tolist() == [0, 0, 0, 1, 1, 1, 1] and all_folded
     _status_clear()
     units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
     _check_extend(w, b, outs, ext, units)
@@ -619,4 +622,33 @@ def test_decode_plan_reuse_across_layers(groups):
     _check_decode(w, db, outs, seqs, [(i, l, hh) for i in range(len(L)) for l in range(3)
                                       for hh in range(4)])
     _status_clear()
+
+
+_FOLD_SPEC = [(600, [(20, 30), (50, 60), (0, 128), (100, 1)]),   # private cached keys, a full tile
+              (300, [(0, 5)] * 7),                                # few-shot like
+              (900, [(10, 100), (0, 200)])]                       # too long to fold
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 2), (16, 8)])
+def test_extend_fold(Hq, Hkv):
+    """Folded stacked passes (each member's remainder -- its own cached tokens past the shared
+    prefix, then its new tokens -- in the group's pass, final outputs written there) next to an
+    unfolded group in the same batch: every unit within tolerance of the oracle, the new K/V
+    scattered bit-exactly, the same without stacking."""
+    m = W.Model(1, Hq, Hkv, 128, "bf16", 13)
+    cache, ext = _stack_families(13, _FOLD_SPEC)
+    w = W.Workload("ext_fold", m, 40_000, synth.permutation(13, 40_000), max_ctx=1216)
+    for fold in (True, False):
+        eng = H.make_engine(w, max_reqs=64, stack_extend="always", fold_extend=fold)
+        for c in cache:
+            H.run_cache_phase(eng, m, [c])
+        b, outs = H.run_extend_phase(eng, m, ext, lse=True)
+        assert b.stack is not None
+        assert b.stack[5].cpu().tolist() == ([1, 1, 0] if fold else [0, 0, 0])
+        assert not b.stack[6]
+        _status_clear()
+        units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
+        _check_extend(w, b, outs, ext, units)
+        _check_slot_rows(eng, b)
+        _check_scatter(eng, w, ext, b)
 
