@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // folded stacked pass: the CTA also takes each of its members' remainders (one key tile per
   // member, members r_first .. r_first + n_rem - 1 of the group [gb0, gb1)) and is final
   bool fold = false;
-  int gb0 = 0, gb1 = 0, r_first = 0, n_rem = 0;
+  int gb0 = 0, gb1 = 0, r_first = 0, n_rem = 0, n_rem_a = 0;
   if (stacked) {
     const int g = p.group_lo + blockIdx.z;
     const int b0 = a.group_range[2 * g], b1 = a.group_range[2 * g + 1];
@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     if (fold) {
       r_first = request_of_pos(a, b0, b1, qo, iA);
       n_rem = request_of_pos(a, b0, b1, qo, min(iA + 2 * p.ppt, S) - 1) - r_first + 1;
+      // query tile A needs the remainder tiles of its own members only, which come first
+      n_rem_a = request_of_pos(a, b0, b1, qo, min(iA + p.ppt, S) - 1) - r_first + 1;
     }
     if (P < 1 || P > a.prefix_len[b0] || P > a.max_ctx || row < 0 || row >= a.max_reqs ||
         qo < 0 || (int64_t)qo + S > a.num_tokens || kstart < 0 || kstart >= P) {
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int n_pre = (P - kstart + kN - 1) / kN;     // prefix key tiles: keys [kstart, P)
   // key tiles of each query tile: the prefix, then (per-request pass) new-token keys up to its
   // last position
-  const int nA = n_pre + (stacked ? n_rem : (iA + nposA + kN - 1) / kN);
+  const int nA = n_pre + (stacked ? n_rem_a : (iA + nposA + kN - 1) / kN);
   const int nB = nposB > 0 ? n_pre + (stacked ? n_rem : (iB + nposB + kN - 1) / kN) : 0;
   // the epilogue leaves a partial result (unfolded stacked pass) or the final one
   const bool partial = stacked && !fold;
