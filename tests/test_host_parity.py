@@ -703,3 +703,34 @@ def test_new_entry_points_reject_bad_arguments():
     assert kv(src_k=0) == rc.RC_ERR_INVALID
     assert kv(dst_v=1032) == rc.RC_ERR_INVALID
     assert kv(layers=0) == rc.RC_ERR_INVALID
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fold_groups_follow_their_rule(seed):
+    """fold_groups marks exactly the groups that no deeper group lies inside and whose every
+    member's remainder (cached tokens past the shared prefix + new tokens) fits one key tile;
+    all_folded is whether every request is in such a group."""
+    rnd = random.Random(600 + seed)
+    B, width = rnd.randint(2, 20), 400
+    rows = np.zeros((B, width), np.int32)
+    base = [rnd.randrange(1000) for _ in range(width)]
+    for b in range(B):
+        cut = rnd.choice([50, 120, 260, 300, 399]) if b % rnd.randint(1, 3) else rnd.randint(0, 60)
+        rows[b] = base
+        rows[b, cut:] = [rnd.randrange(1000, 2000) for _ in range(width - cut)]
+    P = np.array([rnd.randint(260, width) for _ in range(B)], np.int64)
+    S = np.array([rnd.randint(1, 150) for _ in range(B)], np.int64)
+    ranges, shared, start, lvl, _ = rc.prefix_stacking_levels(rows, P, S, 8)
+    fold, all_folded = rc.fold_groups(ranges, shared, lvl, P, S)
+    G = len(shared)
+    level = np.repeat(np.arange(len(lvl) - 1), np.diff(lvl))
+    covered = np.zeros(B, bool)
+    for g in range(G):
+        b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
+        leaf = not any(level[h] > level[g] and b0 <= ranges[2 * h] and ranges[2 * h + 1] <= b1
+                       for h in range(G))
+        fits = all(P[b] - shared[g] + S[b] <= rc.FOLD_KEYS for b in range(b0, b1))
+        assert bool(fold[g]) == (leaf and fits), g
+        if fold[g]:
+            covered[b0:b1] = True
+    assert all_folded == bool(covered.all())
