@@ -171,25 +171,74 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
   return d;
 }
 
+// A descriptor advanced by `bytes` (a multiple of 16): only the 14-bit start-address field
+// changes, and shared-memory addresses stay below 2^18, so the low word takes the add without a
+// carry into the next field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 // kind::f16 instruction descriptor: bf16 A and B, fp32 D, M = 128, N = 128
 __host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accum));
-}
 
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+// Eight K = 16 steps of one 128 x 128 x 128 product in one block, issued by the lane whose
+// `leader` is non-zero (the warp runs the schedule converged; one thread issues). Each step
+// advances the low descriptor words by a constant (no carry: see desc_add).
+// Q K^T: A and B K-major SW128 tiles in shared memory; the steps of a 64-column block are
+// 32 bytes apart, the blocks kBlockBytes apart. The first step overwrites D.
+__device__ __forceinline__ void mma_qk8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t leader) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n .reg .pred e, pf, pt;\n .reg .b32 alo, ahi, blo, bhi, x, y;\n .reg .b64 ad, bd;\n"
+      " setp.ne.b32 e, %4, 0;\n setp.ne.b32 pf, %4, %4;\n setp.eq.b32 pt, %4, %4;\n"
+      " mov.b64 {alo, ahi}, %1;\n mov.b64 {blo, bhi}, %2;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n"
+#define RC_QK_STEP(OFF)                                                              \
+      " add.u32 x, alo, " #OFF ";\n mov.b64 ad, {x, ahi};\n"                        \
+      " add.u32 y, blo, " #OFF ";\n mov.b64 bd, {y, bhi};\n"                        \
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, pt;\n"
+      RC_QK_STEP(2) RC_QK_STEP(4) RC_QK_STEP(6) RC_QK_STEP(1024) RC_QK_STEP(1026)
+      RC_QK_STEP(1028) RC_QK_STEP(1030)
+#undef RC_QK_STEP
+      "}\n" ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(leader));
+}
+static_assert(kBlockBytes == 1024 * 16, "step offsets of mma_qk8 are in 16-byte units");
+// P V: A = the weights in TMEM (keys 16 kk.. in columns 8 kk..), B = V MN-major in shared
+// memory (16 key rows of 128 bytes = 2048 bytes = 128 descriptor units per step). The first step
+// accumulates iff `accum`.
+__device__ __forceinline__ void mma_pv8(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                        uint32_t accum, uint32_t leader) {
+  asm volatile(
+      "{\n .reg .pred e, pf, pt;\n .reg .b32 blo, bhi, x, y;\n .reg .b64 bd;\n"
+      " setp.ne.b32 e, %5, 0;\n setp.ne.b32 pf, %4, 0;\n setp.eq.b32 pt, %5, %5;\n"
+      " mov.b64 {blo, bhi}, %2;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n"
+#define RC_PV_STEP(COL, OFF)                                                         \
+      " add.u32 x, %1, " #COL ";\n add.u32 y, blo, " #OFF ";\n mov.b64 bd, {y, bhi};\n" \
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], bd, %3, pt;\n"
+      RC_PV_STEP(8, 128) RC_PV_STEP(16, 256) RC_PV_STEP(24, 384) RC_PV_STEP(32, 512)
+      RC_PV_STEP(40, 640) RC_PV_STEP(48, 768) RC_PV_STEP(56, 896)
+#undef RC_PV_STEP
+      "}\n" ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum), "r"(leader));
+}
+// tcgen05.commit from the issuing lane only
+__device__ __forceinline__ void mma_commit_by(uint32_t bar, uint32_t leader) {
+  asm volatile(
+      "{\n .reg .pred e;\n setp.ne.b32 e, %1, 0;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar),
+      "r"(leader)
       : "memory");
 }
+
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -252,14 +301,6 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 }
 
 
-// tcgen05.mma with the A operand in TMEM (weights) and B in shared memory (V)
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum));
-}
 // Ties 32 registers written by tcgen05.ld to a point after tcgen05.wait::ld, so that no use of
 // them is scheduled before the wait.
 __device__ __forceinline__ void reg_fence32(float* v) {
@@ -558,9 +599,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    // One thread runs the whole schedule (waits, fences, MMAs, commits).
-    if (lane == 0) {
+    // The warp runs the whole schedule converged (waits, fences); lane 0 alone issues the MMAs
+    // and the commits that track them.
+    {
+      const uint32_t leader = lane == 0;
       const uint32_t idq = idesc_bf16(false), idv = idesc_bf16(true);
+      // base descriptors (Q tile A, K stage 0, V stage 0), built once
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sV, kBlockBytes, 1024);
       // local tile t of virtual tile X reads key tile kt; in pair mode key tile j is read first
       // by tile A (if j < nA) and last by tile B (if j < nB), in split mode by one virtual tile
       auto kt_of = [&](int X, int t) { return split ? 2 * t + X : t; };
@@ -571,20 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (first) {
           if (!mbar_wait(&k_full[st], (kt / kStagesKV) & 1, p.status)) return false;
           // K arrived through the generic proxy (cp.async); one fence covers every later
-          // MMA this thread issues on the stage
+          // MMA issued on the stage
           fence_async_smem();
         }
         tc_fence_after();
-        const uint32_t qsrc = sQ + (split ? 0 : X) * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(qsrc + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024);
-          mma_bf16(tmem + X * 128, ad, bd, idq, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&s_full[X]));
-        if (last) mma_commit(smem_u32(&k_empty[st]));
+        mma_qk8(tmem + X * 128, desc_add(dq0, (split ? 0 : X) * kTileBytes),
+                desc_add(dk0, st * kTileBytes), idq, leader);
+        mma_commit_by(smem_u32(&s_full[X]), leader);
+        if (last) mma_commit_by(smem_u32(&k_empty[st]), leader);
         return true;
       };
       auto pv = [&](int X, int t) -> bool {
@@ -597,17 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           fence_async_smem();   // V arrived through the generic proxy (cp.async)
         }
         tc_fence_after();
-        const uint32_t tS = tmem + X * 128;
-#pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          // A = P from TMEM: keys [16 kk, 16 kk + 16) in score columns [8 kk, 8 kk + 8)
-          const uint32_t at = tS + kk * 8;
-          // B = V (MN-major: d contiguous, keys as rows)
-          const uint64_t bd = smem_desc_sw128(sV + st * kTileBytes + kk * 2048, kBlockBytes, 1024);
-          mma_bf16_ts(tmem + 256 + X * 128, at, bd, idv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (t == (X ? nt1 : nt0) - 1) mma_commit(smem_u32(&o_done[X]));
-        if (last) mma_commit(smem_u32(&v_empty[st]));
+        mma_pv8(tmem + 256 + X * 128, tmem + X * 128, desc_add(dv0, st * kTileBytes), idv,
+                t > 0 ? 1u : 0u, leader);
+        if (t == (X ? nt1 : nt0) - 1) mma_commit_by(smem_u32(&o_done[X]), leader);
+        if (last) mma_commit_by(smem_u32(&v_empty[st]), leader);
         return true;
       };
       bool ok = mbar_wait(q_full, 0, p.status);
@@ -625,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         }
       }
       // every MMA issued above completes before TMEM is freed, also when a wait gave up early
-      mma_commit(smem_u32(drain));
+      mma_commit_by(smem_u32(drain), leader);
       mbar_wait(drain, 0, p.status);
     }
     __syncwarp();
