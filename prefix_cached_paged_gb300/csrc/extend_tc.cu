@@ -77,7 +77,7 @@ struct SmemLayout {
   static constexpr int K = Q + 2 * kTileBytes;
   static constexpr int V = K + kStagesKV * kTileBytes;
   static constexpr int BAR = V + kStagesKV * kTileBytes;
-  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] p_full[2] o_done[2] e_done q_full drain
+  // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] (unused)[2] o_done[2] e_done q_full drain
   static constexpr int NBAR = 4 * kStagesKV + 9;
   static constexpr int TMEM_SLOT = BAR + NBAR * 8;
   // split-mode merge: row maxima, rounded and exact sums of each virtual tile [X][row]
@@ -246,6 +246,17 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// Hardware named barriers (not shared memory): the weights hand-off from a softmax warpgroup
+// to the MMA warp. A poll of an mbarrier by the MMA warp queues behind the tensor core's
+// shared-memory operand reads; a named barrier does not.
+constexpr int kHandoffBar0 = 1;                       // ids 1 (tile A) and 2 (tile B); 0 is __syncthreads
+constexpr int kHandoffThreads = 128 + 32;             // a softmax warpgroup and the MMA warp
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -265,23 +276,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -311,6 +317,12 @@ __device__ __forceinline__ void reg_fence32(float* v) {
                  "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
                  "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
                  "+f"(v[30]), "+f"(v[31]));
+}
+__device__ __forceinline__ void reg_fence16(float* v) {
+  asm volatile(""
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
+                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]));
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -448,8 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint64_t* v_full = k_empty + kStagesKV;       // [stage]
   uint64_t* v_empty = v_full + kStagesKV;       // [stage]
   uint64_t* s_full = v_empty + kStagesKV;       // [tile]
-  uint64_t* p_full = s_full + 2;                // [tile]
-  uint64_t* o_done = p_full + 2;                // [tile]
+  uint64_t* o_done = s_full + 4;                // [tile]
   uint64_t* e_done = o_done + 2;                // split-mode merge
   uint64_t* q_full = e_done + 1;                // both Q tiles in shared memory
   uint64_t* drain = q_full + 1;                 // every issued MMA has completed
@@ -465,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], kGroupThreads);
       mbar_init(&o_done[s], 1);
     }
     mbar_init(e_done, 2 * kGroupThreads);
@@ -630,7 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       };
       auto pv = [&](int X, int t) -> bool {
         const int kt = kt_of(X, t), st = kt % kStagesKV;
-        if (!mbar_wait(&p_full[X], t & 1, p.status)) return false;
+        // the weights P of tile X: every softmax thread of the tile arrives once per local tile,
+        // also after a wait of its own gave up, so this sync always completes
+        named_bar_sync(kHandoffBar0 + X, kHandoffThreads);
         const bool first = split || X == 0 || kt >= nA;
         const bool last = split || X == 1 || kt >= nB;
         if (first) {
@@ -748,7 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const uint32_t tO = tmem + 256 + X * 128 + lane_off;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
-    for (int j = 0; j < nX; ++j) {
+    int j = 0;
+    for (; j < nX; ++j) {
       ok = mbar_wait(&s_full[X], j & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -790,47 +803,57 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // a row with no visible key so far keeps m = -inf; subtract 0 so masked scores give 0
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
       const uint64_t negx2 = f2pack(-m_sub, -m_sub);
-      // weights, rounded to bf16, two per column in the first 64 score columns
-      uint64_t rs2 = 0, re2 = 0;   // packed (even, odd) partial sums: rounded and exact
+      // weights, rounded to bf16, two per column in the first 64 score columns (kept in pk for
+      // the rounded sum after the hand-off); the exact sum in packed (even, odd) form, two chains
+      uint32_t pk[kN / 2];
+      uint64_t re2[2] = {0, 0};
 #pragma unroll
       for (int h = 0; h < kN / 32; ++h) {
-        uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           float x0, x1;
           f2unpack(fma2(f2pack(v[32 * h + 2 * u], v[32 * h + 2 * u + 1]), sc2x2, negx2), x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
-          pk[u] = pack_bf16(p0, p1);
-          // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp
-          // output uses the exact sum
-          rs2 = add2(rs2, f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
-          re2 = add2(re2, f2pack(p0, p1));
+          pk[16 * h + u] = pack_bf16(p0, p1);
+          re2[u & 1] = add2(re2[u & 1], f2pack(p0, p1));
         }
-        tmem_st16u(tS + 16 * h, pk);
+        tmem_st16u(tS + 16 * h, pk + 16 * h);
       }
       // rescale O: the last P.V of this tile completed before these scores did
+      // (16 columns at a time: the rounded weights stay live in registers until the hand-off)
       if (__any_sync(0xffffffffu, rescale && m_run != -INFINITY) && j > 0) {
 #pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
-          float o[32];
-          tmem_ld32(tO + c * 32, o);
+        for (int c = 0; c < kD / 16; ++c) {
+          float o[16];
+          tmem_ld16(tO + c * 16, o);
           tmem_wait_ld();
-          reg_fence32(o);
+          reg_fence16(o);
+          uint32_t ou[16];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) o[u] *= alpha;
-          tmem_st32(tO + c * 32, o);
+          for (int u = 0; u < 16; ++u) ou[u] = __float_as_uint(o[u] * alpha);
+          tmem_st16u(tO + c * 16, ou);
         }
       }
       tmem_wait_st();
+      tc_fence_before();
+      named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
+      // The rounded sum is not needed for the hand-off: it runs while the tensor core does P.V.
+      // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp output
+      // uses the exact sum.
+      uint64_t rs2[2] = {0, 0};
+#pragma unroll
+      for (int u = 0; u < kN / 2; ++u)
+        rs2[u & 1] = add2(rs2[u & 1], f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
       float a0, a1, b0, b1;
-      f2unpack(rs2, a0, a1);
-      f2unpack(re2, b0, b1);
+      f2unpack(add2(rs2[0], rs2[1]), a0, a1);
+      f2unpack(add2(re2[0], re2[1]), b0, b1);
       l_run = l_run * alpha + (a0 + a1);
       l_exact = l_exact * alpha + (b0 + b1);
       m_run = m_use;
-      tc_fence_before();
-      mbar_arrive(&p_full[X]);
     }
+    // a wait that gave up ends the loop early: hand the MMA warp its remaining weights anyway
+    // (garbage; the status word already records the failure) so that its syncs complete
+    for (; j < nX; ++j) named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
     // The row's result over this pass's keys is (O, lse2): O the accumulator(s) times `scale`,
     // lse2 its log2-sum-exp. The stacked pass stores it as a partial (O in o, lse2 in the
     // workspace); a group member's per-request pass merges it with that partial, weights
