@@ -652,3 +652,56 @@ def test_extend_fold(Hq, Hkv):
         _check_slot_rows(eng, b)
         _check_scatter(eng, w, ext, b)
 
+
+
+def test_fork_mixed_step_full_size_sampled():
+    """The fork / self-consistency mixed step at full size (300k-slot pool kept full so that LRU
+    eviction runs, 80 extend sequences of 1500 cached + 200 new tokens, 128 decode requests over
+    512..8192-token contexts in fork groups) in the benchmark's launch configuration, on two of
+    its 32 layers (every layer launches the same kernels): two consecutive steps, each checking
+    a seeded sample of extend and decode units against the oracle, the slot rows and the
+    scattered K/V. Decode inputs at step s come from each request's real s-th generated token."""
+    import torch
+    from synth import device as sdev
+    fm = W.fork_mixed_step(layers=2)
+    w = fm.workload
+    m = w.model
+    Bd = len(fm.decode_seqs)
+    eng = H.make_engine(w, max_reqs=Bd + 80 + 8)
+    for ph in w.phases:
+        H.run_cache_phase(eng, m, ph.seqs, keep_locked=False)
+    db = eng.decode_begin([s[:-1] for s in fm.decode_seqs])
+    assert eng.host.pool.available() == 4096
+    mt = int(db.seq_len.sum()) + Bd * 3
+    rng = np.random.default_rng(11)
+    for step in range(2):
+        seqs = fm.extend_seqs(step)
+        eb = eng.extend_begin(seqs, extra=Bd)
+        eng.decode_step(db, new_slots=eb.plan.extra)
+        assert eb.plan.prefix_len.tolist() == [1500] * 80 and eb.num_tokens == 16_000
+        # the pool is full: LRU eviction makes room every step (4096 slots free at the first)
+        assert eb.plan.evicted >= (16_000 + Bd - 4096 if step == 0 else 1)
+        h_ext = sdev.hashes_to_device(H.new_token_hashes(m, seqs, eb.plan.prefix_len))
+        dseqs = fm.decode_step_seqs(step)
+        h_dec = sdev.hashes_to_device(
+            np.array([synth.prefix_hashes(m.seed, s)[-1] for s in dseqs], np.uint64))
+        ext_outs, dec_outs = {}, {}
+        for layer in range(m.layers):
+            q, k, v = H.dense_qkv(m, h_ext, layer, eb.num_tokens)
+            o = torch.empty_like(q)
+            l = torch.empty((eb.num_tokens, m.n_q_heads), dtype=torch.float32, device="cuda")
+            eng.extend_layer(eb, layer, q, k, v, o, lse=l)
+            ext_outs[layer] = (o, l)
+            dq, dk, dv = H.dense_qkv(m, h_dec, layer, Bd)
+            do = torch.empty_like(dq)
+            dl = torch.empty((Bd, m.n_q_heads), dtype=torch.float32, device="cuda")
+            eng.decode_layer(db, layer, dq, dk, dv, do, lse=dl, max_total_tokens=mt)
+            dec_outs[layer] = (do, dl)
+        torch.cuda.synchronize()
+        _check_extend(w, eb, ext_outs, seqs, _sample_units(rng, 80, 2, 32, 40))
+        _check_decode(w, db, dec_outs, dseqs, _sample_units(rng, Bd, 2, 32, 40) +
+                      [(int(np.argmax([len(s) for s in dseqs])), 1, 7)])
+        _check_slot_rows(eng, eb)
+        _check_scatter(eng, w, seqs, eb, sample=rng.choice(eb.num_tokens, 256, replace=False))
+        eng.extend_end(eb)
+    _status_clear()
