@@ -432,6 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const int iB = iA + p.ppt;
   const int nposA = min(p.ppt, S - iA);
   const int nposB = max(0, min(p.ppt, S - iB));
+  // TMEM lane of a query tile's first row: a tile of at most 96 rows starts at lane 32, so that
+  // lane quadrant 0 holds no rows. Its softmax warps share a sub-partition with the MMA warp,
+  // and a busy warp there slows the MMA warp's issue (measured: one tcgen05.mma per ~89 cycles
+  // with idle neighbours, ~123 with one arithmetic-bound warp beside it, ~159 with two).
+  const int shA = nposA * G <= 96 ? 32 : 0;
+  const int shB = nposB * G <= 96 ? 32 : 0;
   const int n_pre = (P - kstart + kN - 1) / kN;     // prefix key tiles: keys [kstart, P)
   // key tiles of each query tile: the prefix, then (per-request pass) new-token keys up to its
   // last position
@@ -576,9 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // stage 0 is free at the start: the first key tile's copies go out before the setup barrier
   if (producer && ntiles > 0) copy_tile(0, rowptr(0, 0, raw(0, 0)), rowptr(0, 1, raw(0, 1)));
 
-  // Q tiles: row m of tile X = (position iX + m / G, head hk * G + m % G); rows past the tile
-  // are zero-filled. Copied asynchronously (every thread, 16 bytes at a time); the MMA warp
-  // waits on q_full, so the copies overlap TMEM allocation and the first K/V loads.
+  // Q tiles: smem row (= TMEM lane) m of tile X holds tile row m - shX = (position
+  // iX + row / G, head hk * G + row % G); rows outside the tile are zero-filled. Copied
+  // asynchronously (every thread, 16 bytes at a time); the MMA warp waits on q_full, so the
+  // copies overlap TMEM allocation and the first K/V loads.
   {
     const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
     const uint32_t sQ0 = smem_u32(smem) + SmemLayout::Q;
@@ -588,10 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       const int e = threadIdx.x + k * kThreads;
       const int X = e >> 11, m = (e >> 4) & 127, c = e & 15;
       const int i0 = X ? iB : iA, np = X ? nposB : nposA;
+      const int mr = m - (X ? shB : shA);           // tile row held by smem row m
       const __nv_bfloat16* src = q;
       uint32_t bytes = 0;
-      if (m < np * G) {
-        const int i = i0 + m / G, hh = m % G;
+      if (mr >= 0 && mr < np * G) {
+        const int i = i0 + mr / G, hh = mr % G;
         src = q + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c * 8;
         bytes = 16;
       }
@@ -746,7 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     const int nX = X ? nt1 : nt0;
     const int iX = (X && !split) ? iB : iA;
     const int rows_used = ((X && !split) ? nposB : nposA) * G;
-    const int ipos = min(iX + r / G, S - 1);          // this row's new-token index (clamped)
+    const int mrow = r - ((X && !split) ? shB : shA);  // tile row of this lane (< 0: none)
+    const bool row_valid = mrow >= 0 && mrow < rows_used;
+    // a warp with no row of the tile only paces the weights hand-off
+    const bool warp_idle = !__any_sync(0xffffffffu, row_valid);
+    const int ipos = min(iX + max(mrow, 0) / G, S - 1);  // this row's new-token index (clamped)
     // folded stacked pass: the member this row belongs to and its index among that member's
     // new tokens (the member's remainder tile is visible to it up to its own position)
     int req_row = -1, i_row = 0;
@@ -765,6 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       ok = mbar_wait(&s_full[X], j & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      if (warp_idle) {
+        // arriving only after this tile's scores exist keeps every arrival in the generation
+        // the MMA warp syncs on next
+        named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
+        continue;
+      }
       tc_fence_after();
       // keys [0, lim) of key tile kt are visible to this row (lim <= 0: none)
       const int kt = split ? 2 * j + X : j;
@@ -892,8 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
       if (ok) {
         tc_fence_after();
-        const bool store = r < rows_used;
-        const int i = iX + r / G, hh = r % G;
+        const bool store = row_valid;
+        const int i = iX + max(mrow, 0) / G, hh = max(mrow, 0) % G;
         const int64_t rowidx = (int64_t)(qo + i) * Hq + hk * G + hh;
         __nv_bfloat16* orow = (__nv_bfloat16*)a.o + rowidx * kD;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -935,8 +953,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const float lt = w0 * xl[r] + w1 * xl[128 + r];
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         tc_fence_after();
-        const bool store = r < rows_used;
-        const int i = iA + r / G, hh = r % G;
+        const bool store = row_valid;
+        const int i = iA + max(mrow, 0) / G, hh = max(mrow, 0) % G;
         const int64_t rowidx = (int64_t)(qo + i) * Hq + hk * G + hh;
         __nv_bfloat16* orow = (__nv_bfloat16*)a.o + rowidx * kD;
         float fs = 1.f, fp = 0.f, lse2 = M + log2f(w0 * xe[r] + w1 * xe[128 + r]);
