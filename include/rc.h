@@ -75,6 +75,13 @@ int rc_kv_pool_alloc(rc_pool* pool, int64_t n, int32_t* out_slots);
  * change if any slot is out of range, already free, or repeated. */
 int rc_kv_pool_free(rc_pool* pool, const int32_t* slots, int64_t n);
 int rc_kv_pool_available(const rc_pool* pool, int64_t* out);
+/* Host fault injection, for testing callers' failure paths without a real shortage (the pages
+ * describe no failure handling; this is a test hook of the library's own). After `after_calls`
+ * further successful rc_kv_pool_alloc calls on this pool, the next one fails with RC_ERR_OOM
+ * and changes nothing; the hook then disarms itself. Slots the radix tree takes internally
+ * (host-tier spills and loads) are not affected. after_calls = -1 disarms it; any other
+ * negative value is RC_ERR_INVALID. */
+int rc_pool_inject_alloc_failure(rc_pool* pool, int64_t after_calls);
 
 /* ---------------------------------------------------------------------------------------- */
 /* Radix tree (paper digest Sec. 3 and Fig. 3; SGLang blog Sec. 2.3; RadixAttention explainer */

@@ -69,6 +69,12 @@ class Pool:
         check(lib().rc_kv_pool_available(self.h, ctypes.byref(v)), "rc_kv_pool_available")
         return int(v.value)
 
+    def inject_alloc_failure(self, after_calls: int) -> None:
+        """Test hook: the alloc() after `after_calls` more successful ones fails with
+        RC_ERR_OOM and changes nothing (one shot; -1 disarms)."""
+        check(lib().rc_pool_inject_alloc_failure(self.h, int(after_calls)),
+              "rc_pool_inject_alloc_failure")
+
 
 class RadixTree:
     """The radix tree over token sequences. rc_radix_*."""

@@ -31,6 +31,7 @@ SIGNATURES = {
     "rc_kv_pool_alloc": (ctypes.c_int, [_P, _I64, _P]),
     "rc_kv_pool_free": (ctypes.c_int, [_P, _P, _I64]),
     "rc_kv_pool_available": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
+    "rc_pool_inject_alloc_failure": (ctypes.c_int, [_P, _I64]),
     "rc_radix_create": (ctypes.c_int, [_P, ctypes.POINTER(_P)]),
     "rc_radix_destroy": (None, [_P]),
     "rc_radix_match_prefix": (ctypes.c_int, [_P, _P, _I64, _P, ctypes.POINTER(_I64),

@@ -50,7 +50,14 @@ int rc_kv_pool_alloc(rc_pool* p, int64_t n, int32_t* out_slots) {
   RC_CHECK_ARG(p != nullptr, "rc_kv_pool_alloc: pool is NULL");
   RC_CHECK_ARG(n >= 0, "rc_kv_pool_alloc: n = %lld", (long long)n);
   RC_CHECK_ARG(n == 0 || out_slots != nullptr, "rc_kv_pool_alloc: out_slots is NULL");
-  return rc::pool_take(p, n, out_slots);
+  if (p->fail_after == 0) {   // the injected failure (rc_pool_inject_alloc_failure)
+    p->fail_after = -1;
+    return fail(RC_ERR_OOM, "kv_pool_alloc: injected failure (%lld requested, %lld free)",
+                (long long)n, (long long)p->count);
+  }
+  const int rc_take = rc::pool_take(p, n, out_slots);
+  if (rc_take == RC_OK && p->fail_after > 0) --p->fail_after;
+  return rc_take;
 }
 
 int rc_kv_pool_free(rc_pool* p, const int32_t* slots, int64_t n) {
@@ -62,6 +69,14 @@ int rc_kv_pool_free(rc_pool* p, const int32_t* slots, int64_t n) {
 int rc_kv_pool_available(const rc_pool* p, int64_t* out) {
   RC_CHECK_ARG(p != nullptr && out != nullptr, "rc_kv_pool_available: NULL argument");
   *out = p->count;
+  return RC_OK;
+}
+
+int rc_pool_inject_alloc_failure(rc_pool* p, int64_t after_calls) {
+  RC_CHECK_ARG(p != nullptr, "rc_pool_inject_alloc_failure: pool is NULL");
+  RC_CHECK_ARG(after_calls >= -1, "rc_pool_inject_alloc_failure: after_calls = %lld",
+               (long long)after_calls);
+  p->fail_after = after_calls;
   return RC_OK;
 }
 

@@ -11,6 +11,7 @@ struct rc_pool {
   std::vector<uint8_t> is_free;  // 1 if the slot is on the free list
   int64_t head = 0;
   int64_t count = 0;
+  int64_t fail_after = -1;       // injected failure: takes left before one fails (-1: none)
 };
 
 namespace rc {

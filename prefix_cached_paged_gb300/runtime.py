@@ -58,6 +58,16 @@ class HostCache:
             self.host_pool = Pool(host_slots, host_order)
             self.tree.attach_host_tier(self.host_pool)
 
+    def _release_on_error(self, nodes, fn, *args):
+        """fn(*args); if it fails, the nodes this plan's match locked are unlocked first, so a
+        failed plan leaves the tree as it found it apart from evictions (which are complete)."""
+        try:
+            return fn(*args)
+        except RcError:
+            for n in nodes:
+                self.tree.unlock(int(n))
+            raise
+
     def _make_room(self, need: int, plan: Plan, nodes) -> None:
         avail = self.pool.available()
         if avail < need:
@@ -98,7 +108,8 @@ class HostCache:
             if host_len.any():
                 # device room for the suffixes and the host-tier tokens, then load those back
                 self._make_room(int((lengths - prefix_len).sum()) + int(extra), pre, nodes)
-                self.tree.load_batch(tokens, indptr, rows, prefix_len, host_len)
+                self._release_on_error(nodes, self.tree.load_batch, tokens, indptr, rows,
+                                       prefix_len, host_len)
         S = lengths - prefix_len
         qo = np.zeros(B + 1, dtype=np.int32)
         np.cumsum(S, out=qo[1:])
@@ -108,7 +119,7 @@ class HostCache:
         self._make_room(need, plan, nodes)
         if pre.evict_request:
             plan.evict_request, plan.evicted = pre.evict_request, pre.evicted
-        new = self.pool.alloc(need)
+        new = self._release_on_error(nodes, self.pool.alloc, need)
         for b in range(B):
             rows[b, prefix_len[b]:lengths[b]] = new[qo[b]:qo[b + 1]]
         plan.out_loc = new[: qo[-1]]
