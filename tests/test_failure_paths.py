@@ -75,3 +75,81 @@ def test_failed_plan_releases_its_locks(evict):
     assert hc.tree.stats()["protected_tokens"] > 0            # now locked by the running batch
     hc.finish(plan)
     assert hc.tree.stats()["protected_tokens"] == 0
+
+
+def _fake(i):
+    # a 16-byte aligned address that is never dereferenced: every call below is rejected (or
+    # returns) before anything reaches a device
+    return 0x10000 + 256 * i
+
+
+def test_extend_rejects_bad_arguments_before_any_device_work():
+    import ctypes
+    from prefix_cached_paged_gb300._lib import RcExtendArgs, lib
+    ptrs = ["q", "k_new", "v_new", "out_loc", "qo_indptr", "prefix_len", "req_idx",
+            "req_to_token", "k_pool", "v_pool", "o"]
+
+    def call(**kw):
+        a = dict(dtype=rc.RC_DTYPE_BF16, num_reqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                 max_reqs=4, max_ctx=64, max_q_len=8, max_prefix_len=8, num_tokens=16,
+                 num_slots=100, sm_scale=0.088)
+        a.update({n: _fake(i) for i, n in enumerate(ptrs)})
+        a.update(kw)
+        return lib().rc_extend_attention(ctypes.byref(RcExtendArgs(**a)), None)
+
+    bad = [dict(dtype=7), dict(num_kv_heads=3), dict(num_q_heads=0), dict(head_dim=96),
+           dict(head_dim=64),                        # 64 only for fp32
+           dict(max_ctx=62), dict(max_reqs=0), dict(num_slots=0), dict(num_tokens=-1),
+           dict(q=0), dict(req_to_token=0), dict(k_pool=_fake(3) + 8), dict(num_groups=-1),
+           dict(num_groups=1),                       # no group arrays
+           dict(num_groups=1, group_range=_fake(20), group_shared=_fake(21), max_group_rows=8,
+                workspace=_fake(22), workspace_bytes=16)]    # workspace too small
+    for kw in bad:
+        assert call(**kw) == rc.RC_ERR_INVALID, kw
+    # levels: at most RC_MAX_STACK_LEVELS; level_indptr (host) from 0 to num_groups, no empty level
+    stack = dict(num_groups=3, group_range=_fake(20), group_shared=_fake(21), max_group_rows=8,
+                 workspace=_fake(22), workspace_bytes=1 << 20)
+    assert call(num_levels=rc.MAX_STACK_LEVELS + 1, **stack) == rc.RC_ERR_INVALID
+    for lv in ([0, 0, 3], [1, 2, 3], [0, 2, 2], [0, 1, 4]):
+        li = np.array(lv, np.int32)
+        assert call(num_levels=2, level_indptr=li.ctypes.data, **stack) == rc.RC_ERR_INVALID, lv
+    # nothing to do is not an error, and touches no device
+    assert call(num_reqs=0) == rc.RC_OK and call(max_q_len=0) == rc.RC_OK
+
+
+def test_decode_rejects_bad_arguments_before_any_device_work():
+    import ctypes
+    from prefix_cached_paged_gb300._lib import RcDecodeArgs, lib
+    ptrs = ["q", "k_new", "v_new", "out_loc", "seq_len", "req_idx", "req_to_token", "k_pool",
+            "v_pool", "o"]
+
+    def args(**kw):
+        a = dict(dtype=rc.RC_DTYPE_BF16, num_reqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                 max_reqs=4, max_ctx=64, kv_chunk=0, max_total_tokens=128, num_slots=100,
+                 sm_scale=0.088)
+        a.update({n: _fake(i) for i, n in enumerate(ptrs)})
+        a.update(kw)
+        return RcDecodeArgs(**a)
+
+    need = ctypes.c_size_t()
+    assert lib().rc_decode_workspace_bytes(ctypes.byref(args()), ctypes.byref(need)) == rc.RC_OK
+    ws = _fake(30)
+
+    def call(ws=ws, ws_bytes=need.value, **kw):
+        return lib().rc_decode_attention(ctypes.byref(args(**kw)), ws, ws_bytes, None)
+
+    bad = [dict(dtype=7), dict(num_q_heads=6),      # group size 3
+           dict(num_q_heads=32),                     # group size 16
+           dict(head_dim=96), dict(kv_chunk=100), dict(kv_chunk=-64), dict(max_ctx=0),
+           dict(num_slots=0), dict(max_total_tokens=-1), dict(num_groups=-1), dict(num_groups=1),
+           dict(q=0), dict(k_pool=_fake(7) + 8)]
+    for kw in bad:
+        assert call(**kw) == rc.RC_ERR_INVALID, kw
+    assert call(ws=None) == rc.RC_ERR_INVALID                     # no workspace
+    assert call(ws=ws + 8) == rc.RC_ERR_INVALID                   # misaligned workspace
+    assert call(ws_bytes=need.value - 1) == rc.RC_ERR_INVALID     # workspace too small
+    assert call(num_reqs=0) == rc.RC_OK
+    # the allocation-free variant rejects work beyond its fixed scratch area
+    big = args(kv_chunk=64, max_total_tokens=10**9)
+    assert lib().rc_decode_attention_noalloc(ctypes.byref(big), None) == rc.RC_ERR_INVALID
+    assert "scratch" in lib().rc_last_error().decode()
