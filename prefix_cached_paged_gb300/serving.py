@@ -117,9 +117,12 @@ class Engine:
             kv_copy(self.host_k, self.host_v, d_lh, self.dev.k, self.dev.v, d_ld)
 
     # ---------------------------------------------------------------- rows
-    def _take_rows(self, n):
+    def _check_rows(self, n):
         if n > len(self._free_rows):
             raise RuntimeError(f"slot table has {len(self._free_rows)} free rows, {n} needed")
+
+    def _take_rows(self, n):
+        self._check_rows(n)
         return np.array([self._free_rows.pop() for _ in range(n)], dtype=np.int32)
 
     def _release_rows(self, rows):
@@ -127,6 +130,8 @@ class Engine:
 
     # ---------------------------------------------------------------- extend
     def extend_begin(self, seqs, extra: int = 0, match_all: bool = False) -> ExtendBatch:
+        # rows first: a plan allocates slots and locks prefixes, which a late failure would leak
+        self._check_rows(len(seqs))
         plan = self.host.plan(seqs, extra=extra, match_all=match_all)
         self._tier_copies(plan.copies)
         B = len(seqs)
@@ -174,6 +179,7 @@ class Engine:
     def decode_begin(self, contexts) -> DecodeBatch:
         """Requests enter decoding: each context must be cached; it is matched and locked, its
         slots written to a fresh slot-table row. The first decode_step allocates the new tokens."""
+        self._check_rows(len(contexts))
         plan = self.host.plan(contexts, match_all=True)
         self._tier_copies(plan.copies)
         if plan.num_tokens:

@@ -153,3 +153,24 @@ def test_decode_rejects_bad_arguments_before_any_device_work():
     big = args(kv_chunk=64, max_total_tokens=10**9)
     assert lib().rc_decode_attention_noalloc(ctypes.byref(big), None) == rc.RC_ERR_INVALID
     assert "scratch" in lib().rc_last_error().decode()
+
+
+def test_engine_checks_slot_table_rows_before_planning():
+    """With too few free slot-table rows, extend_begin and decode_begin fail before planning,
+    so no slot is allocated and no prefix stays locked (the engine's device side is not needed
+    to reach the check)."""
+    from prefix_cached_paged_gb300.serving import Engine
+    hc = runtime.HostCache(1000, 64)
+    pre = synth.tokens(3, 1, 40)
+    _cache(hc, [pre])
+    eng = Engine.__new__(Engine)           # host side only: no device tensors
+    eng.host = hc
+    eng._free_rows = [1, 0]
+    seqs = [np.concatenate([pre, synth.tokens(3, 10 + i, 5)]).astype(np.int32) for i in range(3)]
+    avail = hc.pool.available()
+    with pytest.raises(RuntimeError, match="free rows"):
+        eng.extend_begin(seqs)
+    with pytest.raises(RuntimeError, match="free rows"):
+        eng.decode_begin([pre, pre, pre])
+    assert hc.pool.available() == avail
+    assert hc.tree.stats()["protected_tokens"] == 0
