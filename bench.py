@@ -639,23 +639,21 @@ def _queue_batches(pq, policy, host_slots=0):
     """The batches the scheduler forms over the queue (host only; the engine's host cache makes
     the same decisions): [(request ids, matched lengths incl. tokens loaded from the host
     tier, tokens loaded)]."""
-    from prefix_cached_paged_gb300.runtime import HostCache
+    from prefix_cached_paged_gb300.runtime import HostCache, WaitingQueue
     w = pq.workload
     hc = HostCache(w.pool_slots, w.max_ctx, w.pool_order, host_slots=host_slots)
-    waiting = list(range(len(pq.seqs)))
+    waiting = WaitingQueue(pq.seqs)
     out = []
-    while waiting:
-        idx = hc.schedule([pq.seqs[i] for i in waiting], pq.max_batch, pq.max_new_tokens,
-                          policy=policy)
+    while len(waiting):
+        idx = hc.schedule(waiting, pq.max_batch, pq.max_new_tokens, policy=policy)
         if not idx:
             raise RuntimeError("program queue: no request fits the pool")
-        ids = [waiting[i] for i in idx]
+        ids = [waiting.ids[i] for i in idx]
         p = hc.plan([pq.seqs[i] for i in ids])
         out.append((ids, p.prefix_len.copy(),
                     0 if p.host_len is None else int(p.host_len.sum())))
         hc.finish(p)
-        for i in sorted(idx, reverse=True):
-            waiting.pop(i)
+        waiting.remove(idx)
     return out
 
 
@@ -666,21 +664,21 @@ def _serve_queue(pq, policy, batches, inputs, overlap, host_slots=0, host_planes
     slot-table rows that the host recycles safe). Returns host ms, tree ms, kernel ms (extend),
     wall ms, and the device time of the batches' begin work (slot table, host-tier copies)."""
     import torch
+    from prefix_cached_paged_gb300.runtime import WaitingQueue
     from tests import harness as H
     m = pq.workload.model
     eng = H.make_engine(pq.workload, max_reqs=pq.max_batch + 8, host_tier_slots=host_slots,
                         host_planes=host_planes)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in batches]
-    waiting = list(range(len(pq.seqs)))
+    waiting = WaitingQueue(pq.seqs)
     host_s = 0.0
     torch.cuda.synchronize()
     tree0 = eng.host.host_seconds
     t_start = time.perf_counter()
     for k, (ids_ref, _, _) in enumerate(batches):
         t0 = time.perf_counter()
-        idx = eng.host.schedule([pq.seqs[i] for i in waiting], pq.max_batch, pq.max_new_tokens,
-                                policy=policy)
-        ids = [waiting[i] for i in idx]
+        idx = eng.host.schedule(waiting, pq.max_batch, pq.max_new_tokens, policy=policy)
+        ids = [waiting.ids[i] for i in idx]
         assert ids == ids_ref
         evs[k][0].record()
         b = eng.extend_begin([pq.seqs[i] for i in ids])
@@ -694,8 +692,7 @@ def _serve_queue(pq, policy, batches, inputs, overlap, host_slots=0, host_planes
             torch.cuda.synchronize()
         t0 = time.perf_counter()
         eng.extend_end(b)
-        for i in sorted(idx, reverse=True):
-            waiting.pop(i)
+        waiting.remove(idx)
         host_s += time.perf_counter() - t0
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_start

@@ -224,6 +224,16 @@ int rc_schedule_batch(const rc_radix* tree, const int32_t* tokens, const int64_t
                       int32_t B, const int32_t* match_len, int32_t policy, int32_t max_batch,
                       int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
                       int32_t* out_match, int32_t* out_admitted);
+/* The same batch formation over W waiting sequences given as ranges of one token buffer:
+ * sequence w is tokens[starts[w], starts[w] + lengths[w]) (host int64 arrays of W entries;
+ * ranges may be in any order, with gaps). Outputs, order and admission exactly as
+ * rc_schedule_batch over the same sequences. A caller that keeps its whole queue in one buffer
+ * passes the waiting entries' ranges instead of repacking the queue for every call. */
+int rc_schedule_batch_ranges(const rc_radix* tree, const int32_t* tokens, const int64_t* starts,
+                             const int64_t* lengths, int32_t W, const int32_t* match_len,
+                             int32_t policy, int32_t max_batch, int64_t max_new_tokens,
+                             int64_t reserve_slots, int32_t* out_order, int32_t* out_match,
+                             int32_t* out_admitted);
 
 /* ---------------------------------------------------------------------------------------- */
 /* Device entry points                                                                       */

@@ -218,6 +218,27 @@ class RadixTree:
               "rc_schedule_batch")
         return order, match, int(adm.value)
 
+    def schedule_batch_ranges(self, tokens: np.ndarray, starts: np.ndarray, lengths: np.ndarray,
+                              match_len=None, policy: int = 0, max_batch: int = 1 << 30,
+                              max_new_tokens: int = -1, reserve_slots: int = 0):
+        """schedule_batch over W sequences given as ranges of one buffer: sequence w is
+        tokens[starts[w] : starts[w] + lengths[w]]. Same outputs as schedule_batch."""
+        W = len(starts)
+        order = np.empty(W, dtype=np.int32)
+        match = np.empty(W, dtype=np.int32)
+        adm = ctypes.c_int32()
+        ml = None if match_len is None else _i32(match_len)
+        tok = _i32(tokens)
+        st = np.ascontiguousarray(starts, np.int64)
+        ln = np.ascontiguousarray(lengths, np.int64)
+        check(lib().rc_schedule_batch_ranges(self.h, _p(tok), _p(st), _p(ln), W,
+                                             None if ml is None else _p(ml), int(policy),
+                                             int(max_batch), int(max_new_tokens),
+                                             int(reserve_slots), _p(order), _p(match),
+                                             ctypes.byref(adm)),
+              "rc_schedule_batch_ranges")
+        return order, match, int(adm.value)
+
     def insert_batch(self, tokens, indptr, rows, prefix_len, unlock_nodes, keep_locked=False):
         """Insert B sequences with their slot rows, free duplicates, optionally lock the ends,
         unlock the matched nodes. Returns (end_nodes uint64[B], duplicates freed)."""

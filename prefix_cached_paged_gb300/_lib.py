@@ -53,6 +53,8 @@ SIGNATURES = {
     "rc_radix_tiers": (_I64, [_P, _P, _I64]),
     "rc_schedule_batch": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I64, _I64, _P, _P,
                                          _P]),
+    "rc_schedule_batch_ranges": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I64, _I64,
+                                                _P, _P, _P]),
     "rc_slot_table_write": (ctypes.c_int, [_P, _P]),
     "rc_kv_copy": (ctypes.c_int, [_P, _P]),
     "rc_extend_workspace_bytes": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_size_t)]),

@@ -745,25 +745,25 @@ int rc_radix_insert_batch(rc_radix* t, const int32_t* tokens, const int64_t* ind
   return RC_OK;
 }
 
-int rc_schedule_batch(const rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
-                      const int32_t* match_len, int32_t policy, int32_t max_batch,
-                      int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
-                      int32_t* out_match, int32_t* out_admitted) {
-  RC_CHECK_ARG(t && out_admitted && B >= 0 && max_batch >= 0 && reserve_slots >= 0 &&
-                   (policy == RC_SCHED_LSPF || policy == RC_SCHED_FCFS) &&
-                   (B == 0 || (tokens && indptr && out_order && out_match)),
-               "rc_schedule_batch: bad argument");
+}  // extern "C"
+
+namespace {
+// Batch formation over W waiting sequences; sequence w is tokens[start(w), start(w) + len(w)).
+// Shared by rc_schedule_batch (contiguous sequences) and rc_schedule_batch_ranges.
+template <typename Start, typename Len>
+int schedule_impl(const rc_radix* t, const int32_t* tokens, Start start, Len len_of, int32_t B,
+                  const int32_t* match_len, int32_t policy, int32_t max_batch,
+                  int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
+                  int32_t* out_match, int32_t* out_admitted, const char* what) {
   for (int32_t w = 0; w < B; ++w) {
-    const int64_t len = indptr[w + 1] - indptr[w];
+    const int64_t len = len_of(w);
     const int64_t n = match_len ? (int64_t)match_len[w] : len;
-    RC_CHECK_ARG(indptr[w] >= 0 && len >= 0 && n >= 0 && n <= len,
-                 "rc_schedule_batch: sequence %d: length %lld, match %lld", w, (long long)len,
+    RC_CHECK_ARG(start(w) >= 0 && len >= 0 && n >= 0 && n <= len,
+                 "%s: sequence %d: length %lld, match %lld", what, w, (long long)len,
                  (long long)n);
   }
-  auto seq = [&](int32_t w) { return tokens + indptr[w]; };
-  auto lim = [&](int32_t w) {
-    return match_len ? (int64_t)match_len[w] : indptr[w + 1] - indptr[w];
-  };
+  auto seq = [&](int32_t w) { return tokens + start(w); };
+  auto lim = [&](int32_t w) { return match_len ? (int64_t)match_len[w] : len_of(w); };
   for (int32_t w = 0; w < B; ++w)
     out_match[w] = (int32_t)t->peek(seq(w), lim(w), [](int32_t, int64_t) {});
   for (int32_t w = 0; w < B; ++w) out_order[w] = w;
@@ -783,7 +783,7 @@ int rc_schedule_batch(const rc_radix* t, const int32_t* tokens, const int64_t* i
   int32_t admitted = 0;
   for (int32_t i = 0; i < B && admitted < max_batch; ++i) {
     const int32_t w = out_order[i];
-    const int64_t fresh = indptr[w + 1] - indptr[w] - out_match[w];
+    const int64_t fresh = len_of(w) - out_match[w];
     if (max_new_tokens >= 0 && computed + fresh > max_new_tokens) break;
     int64_t locked = 0;
     ups.clear();
@@ -804,6 +804,38 @@ int rc_schedule_batch(const rc_radix* t, const int32_t* tokens, const int64_t* i
   }
   *out_admitted = admitted;
   return RC_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int rc_schedule_batch(const rc_radix* t, const int32_t* tokens, const int64_t* indptr, int32_t B,
+                      const int32_t* match_len, int32_t policy, int32_t max_batch,
+                      int64_t max_new_tokens, int64_t reserve_slots, int32_t* out_order,
+                      int32_t* out_match, int32_t* out_admitted) {
+  RC_CHECK_ARG(t && out_admitted && B >= 0 && max_batch >= 0 && reserve_slots >= 0 &&
+                   (policy == RC_SCHED_LSPF || policy == RC_SCHED_FCFS) &&
+                   (B == 0 || (tokens && indptr && out_order && out_match)),
+               "rc_schedule_batch: bad argument");
+  return schedule_impl(
+      t, tokens, [&](int32_t w) { return indptr[w]; },
+      [&](int32_t w) { return indptr[w + 1] - indptr[w]; }, B, match_len, policy, max_batch,
+      max_new_tokens, reserve_slots, out_order, out_match, out_admitted, "rc_schedule_batch");
+}
+
+int rc_schedule_batch_ranges(const rc_radix* t, const int32_t* tokens, const int64_t* starts,
+                             const int64_t* lengths, int32_t W, const int32_t* match_len,
+                             int32_t policy, int32_t max_batch, int64_t max_new_tokens,
+                             int64_t reserve_slots, int32_t* out_order, int32_t* out_match,
+                             int32_t* out_admitted) {
+  RC_CHECK_ARG(t && out_admitted && W >= 0 && max_batch >= 0 && reserve_slots >= 0 &&
+                   (policy == RC_SCHED_LSPF || policy == RC_SCHED_FCFS) &&
+                   (W == 0 || (tokens && starts && lengths && out_order && out_match)),
+               "rc_schedule_batch_ranges: bad argument");
+  return schedule_impl(
+      t, tokens, [&](int32_t w) { return starts[w]; }, [&](int32_t w) { return lengths[w]; }, W,
+      match_len, policy, max_batch, max_new_tokens, reserve_slots, out_order, out_match,
+      out_admitted, "rc_schedule_batch_ranges");
 }
 
 }  // extern "C"

@@ -47,6 +47,34 @@ class Plan:
         return int(self.qo_indptr[-1])
 
 
+class WaitingQueue:
+    """Waiting sequences kept in one token buffer. HostCache.schedule passes the entries still
+    waiting as ranges of that buffer (rc_schedule_batch_ranges), so a queue is packed once, not
+    for every scheduling call. `ids` are the queue positions still waiting, in queue order."""
+
+    def __init__(self, seqs):
+        seqs = [np.asarray(s, dtype=np.int32) for s in seqs]
+        self.lengths = np.array([len(s) for s in seqs], dtype=np.int64)
+        self.starts = np.zeros(len(seqs), dtype=np.int64)
+        if len(seqs) > 1:
+            np.cumsum(self.lengths[:-1], out=self.starts[1:])
+        self.tokens = np.concatenate(seqs) if seqs else np.zeros(0, np.int32)
+        self.ids = list(range(len(seqs)))
+
+    def __len__(self) -> int:
+        return len(self.ids)
+
+    def seq(self, qid: int) -> np.ndarray:
+        """The tokens of queue entry qid (a view of the buffer)."""
+        s = int(self.starts[qid])
+        return self.tokens[s:s + int(self.lengths[qid])]
+
+    def remove(self, positions) -> None:
+        """Drop the waiting entries at these positions of `ids`."""
+        for i in sorted(positions, reverse=True):
+            self.ids.pop(i)
+
+
 class HostCache:
     def __init__(self, num_slots: int, row_stride: int, initial_order=None, host_slots: int = 0,
                  host_order=None):
@@ -133,9 +161,18 @@ class HostCache:
                  reserve: int = 0, policy: int = RC_SCHED_LSPF):
         """Batch formation (rc_schedule_batch; longest shared prefix first by default) over the
         waiting sequences, matched like `plan` matches them (all but the last token). Returns
-        the queue positions of the admitted batch, in the order to plan them."""
+        the queue positions of the admitted batch, in the order to plan them. `waiting` is a
+        list of token arrays, or a WaitingQueue (its entries still waiting; no repacking)."""
         t0 = time.perf_counter()
         try:
+            if isinstance(waiting, WaitingQueue):
+                ids = np.asarray(waiting.ids, dtype=np.int64)
+                lengths = waiting.lengths[ids]
+                order, _, admitted = self.tree.schedule_batch_ranges(
+                    waiting.tokens, waiting.starts[ids], lengths,
+                    np.maximum(lengths - 1, 0).astype(np.int32), policy, max_batch,
+                    max_new_tokens, reserve)
+                return order[:admitted].tolist()
             seqs = [np.asarray(s, dtype=np.int32) for s in waiting]
             lengths = np.array([len(s) for s in seqs], dtype=np.int64)
             indptr = np.zeros(len(seqs) + 1, dtype=np.int64)

@@ -176,6 +176,18 @@ def test_schedule_batch_matches_oracle_bit_exact(seed):
                                            rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF,
                                            kw["max_batch"], kw["max_new_tokens"], kw["reserve"])
             assert (list(o1), list(m1), a1) == (o2.tolist(), m2.tolist(), a2)
+            # the same sequences as ranges of one buffer, shuffled and with gaps between them
+            r2 = random.Random(7919 * seed + compared)
+            buf, starts = [], np.zeros(len(waiting), np.int64)
+            for wi in r2.sample(range(len(waiting)), len(waiting)):
+                buf += [r2.randrange(alpha) for _ in range(r2.randint(0, 3))]
+                starts[wi] = len(buf)
+                buf += list(waiting[wi])
+            o3, m3, a3 = pt.schedule_batch_ranges(np.array(buf, np.int32), starts, lens, mlen,
+                                                  rc.RC_SCHED_FCFS if fcfs else rc.RC_SCHED_LSPF,
+                                                  kw["max_batch"], kw["max_new_tokens"],
+                                                  kw["reserve"])
+            assert (o3.tolist(), m3.tolist(), a3) == (o2.tolist(), m2.tolist(), a2)
             compared += 1
             admitted_some += a2 > 0
         np.testing.assert_array_equal(ot.dump(), pt.dump())
