@@ -174,50 +174,3 @@ def test_engine_checks_slot_table_rows_before_planning():
         eng.decode_begin([pre, pre, pre])
     assert hc.pool.available() == avail
     assert hc.tree.stats()["protected_tokens"] == 0
-
-
-@pytest.mark.parametrize("shared", [True, False])
-def test_waiting_queue_schedules_like_the_list(shared):
-    """Serving a program queue through a WaitingQueue (ranges of one buffer, rc_schedule_batch_
-    ranges) forms the same batches as passing the waiting sequences as lists, and leaves the same
-    tree."""
-    from synth import workloads as W
-    pq = W.program_queue(layers=1, shared=shared, n_programs=6)
-    w = pq.workload
-    runs = []
-    for use_queue in (False, True):
-        hc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order)
-        wq = runtime.WaitingQueue(pq.seqs)
-        waiting = list(range(len(pq.seqs)))
-        batches = []
-        while waiting:
-            arg = wq if use_queue else [pq.seqs[i] for i in waiting]
-            idx = hc.schedule(arg, pq.max_batch, pq.max_new_tokens, policy=rc.RC_SCHED_LSPF)
-            assert idx
-            ids = [waiting[i] for i in idx]
-            if use_queue:
-                assert [wq.ids[i] for i in idx] == ids
-                assert all(np.array_equal(wq.seq(q), pq.seqs[q]) for q in ids)
-            p = hc.plan([pq.seqs[i] for i in ids])
-            batches.append((ids, p.prefix_len.tolist()))
-            hc.finish(p)
-            for i in sorted(idx, reverse=True):
-                waiting.pop(i)
-            wq.remove(idx)
-        runs.append((batches, hc.tree.dump()))
-    assert runs[0][0] == runs[1][0]
-    np.testing.assert_array_equal(runs[0][1], runs[1][1])
-
-
-def test_schedule_ranges_rejects_bad_arguments():
-    t = rc.RadixTree(rc.Pool(20))
-    tok = np.arange(6, dtype=np.int32)
-    for starts, lengths, ml in (([-1], [3], None), ([0], [-2], None), ([0], [3], [4])):
-        with pytest.raises(rc.RcError) as e:
-            t.schedule_batch_ranges(tok, np.array(starts), np.array(lengths),
-                                    None if ml is None else np.array(ml, np.int32))
-        assert e.value.code == rc.RC_ERR_INVALID
-    with pytest.raises(rc.RcError):
-        t.schedule_batch_ranges(tok, np.array([0]), np.array([3]), None, policy=9)
-    order, match, adm = t.schedule_batch_ranges(tok, np.zeros(0), np.zeros(0))
-    assert (len(order), adm) == (0, 0)
