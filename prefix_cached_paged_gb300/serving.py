@@ -10,7 +10,8 @@
   decode_begin   requests enter decoding: match their cached context, lock it, take a row;
   decode_step    allocate one slot per request for its new token and write it to the row;
   decode_layer   split-K decode attention of one layer;
-  decode_end     unlock and release rows.
+  decode_end     insert the finished sequences (context + generated tokens) or free the generated
+                 tokens' slots, unlock, release rows.
 
 The model's projections (q, k_new, v_new per layer) are the caller's: this module never
 computes them.
@@ -57,6 +58,9 @@ class DecodeBatch:
     groups: object = None   # device (indptr, members, shared) of shared-context groups, or None
     num_groups: int = 0
     step_id: object = None  # identity of the current step's lengths (a fresh object per step)
+    context_rows: object = None  # host int32 [B, max_ctx]: each context's slots (decode_begin)
+    context_len: object = None   # host int64 [B]
+    gen_slots: list = None       # host int32 [B] per decode_step: the generated tokens' slots
 
 
 # shortest shared prefix worth a stacked pass: two key tiles
@@ -191,7 +195,8 @@ class Engine:
         self.dev.write_rows(row_ids, plan.rows, plan.lengths)
         self._decode_plan = plan
         batch = DecodeBatch(row_ids, plan.nodes, plan.lengths.astype(np.int32),
-                            np.zeros(len(contexts), np.int32))
+                            np.zeros(len(contexts), np.int32), context_rows=plan.rows,
+                            context_len=plan.lengths.astype(np.int64), gen_slots=[])
         if self.share_decode:
             # the contexts' slots never change while they decode (new tokens get new slots), so
             # the groups hold for the whole batch
@@ -216,6 +221,8 @@ class Engine:
         self.dev.write_rows(batch.row_ids, rows, cols + 1, cols=cols)
         batch.seq_len = batch.seq_len + 1
         batch.new_slots = np.asarray(new_slots, dtype=np.int32)
+        if batch.gen_slots is not None:
+            batch.gen_slots.append(batch.new_slots.copy())
         batch.step_id = object()   # the lengths changed: the next layer plans again
         batch.dev_seq_len, batch.dev_req_idx, batch.dev_out_loc = self.dev.upload_i32(
             [batch.seq_len, batch.row_ids, batch.new_slots])
@@ -245,7 +252,34 @@ class Engine:
                          reuse_plan=reuse)
         self._ws_plan = key     # the workspace now holds this step's plan
 
-    def decode_end(self, batch: DecodeBatch):
-        for n in batch.nodes:
-            self.host.tree.unlock(int(n))
+    def decode_end(self, batch: DecodeBatch, seqs=None):
+        """The requests leave decoding. With `seqs` (each request's context followed by the
+        tokens its decode steps fed in, one per step), the sequences are inserted into the tree
+        like a finished extend (the generated tokens' KV stays cached; slots of tokens the tree
+        already holds are freed); without, the generated tokens' slots return to the pool. Then
+        the contexts are unlocked and the slot-table rows released."""
+        B = len(batch.row_ids)
+        gen = (np.stack(batch.gen_slots, axis=1) if batch.gen_slots
+               else np.zeros((B, 0), dtype=np.int32))
+        if seqs is not None:
+            seqs = [np.asarray(s, dtype=np.int32) for s in seqs]
+            want = batch.context_len + gen.shape[1]
+            if len(seqs) != B or any(len(s) != int(n) for s, n in zip(seqs, want)):
+                raise ValueError("decode_end: each sequence must be its context plus one token "
+                                 f"per decode step ({gen.shape[1]})")
+            lengths = want.astype(np.int64)
+            indptr = np.zeros(B + 1, dtype=np.int64)
+            np.cumsum(lengths, out=indptr[1:])
+            rows = np.array(batch.context_rows, dtype=np.int32, copy=True)
+            for b in range(B):
+                rows[b, batch.context_len[b]:lengths[b]] = gen[b]
+            empty = np.zeros(0, dtype=np.int32)
+            self.host.finish(Plan(np.concatenate(seqs) if B else empty, indptr, lengths,
+                                  batch.context_len.astype(np.int32), batch.nodes, rows,
+                                  empty, empty, empty))
+        else:
+            if gen.size:
+                self.host.pool.free(gen.reshape(-1))
+            for n in batch.nodes:
+                self.host.tree.unlock(int(n))
         self._release_rows(batch.row_ids)

@@ -174,3 +174,55 @@ def test_engine_checks_slot_table_rows_before_planning():
         eng.decode_begin([pre, pre, pre])
     assert hc.pool.available() == avail
     assert hc.tree.stats()["protected_tokens"] == 0
+
+
+class _HostOnlyDevice:
+    """Stands in for the engine's device side in host-bookkeeping tests: slot-table writes and
+    metadata uploads are accepted and dropped."""
+
+    def write_rows(self, row_ids, rows, ends, cols=None):
+        pass
+
+    def upload_i32(self, arrays):
+        return [None for _ in arrays]
+
+
+def _host_engine(hc, rows=8, max_ctx=64):
+    from prefix_cached_paged_gb300.serving import Engine
+    eng = Engine.__new__(Engine)
+    eng.host, eng.dev = hc, _HostOnlyDevice()
+    eng._free_rows = list(range(rows - 1, -1, -1))
+    eng.share_decode, eng.kv_chunk, eng.max_ctx = False, 0, max_ctx
+    return eng
+
+
+@pytest.mark.parametrize("insert", [False, True])
+def test_decode_end_returns_or_caches_the_generated_tokens(insert):
+    """Every decode step takes a slot per request; when the requests end, their generated
+    tokens' slots go back to the pool, or the finished sequences are inserted into the tree (the
+    pages' insert after a request finishes) and their generated tokens become reusable."""
+    hc = runtime.HostCache(1000, 64)
+    ctx = [synth.tokens(5, 1 + i, 20 + 3 * i) for i in range(3)]
+    _cache(hc, ctx)
+    eng = _host_engine(hc)
+    avail0 = hc.pool.available()
+    db = eng.decode_begin(ctx)
+    steps = 4
+    for _ in range(steps):
+        eng.decode_step(db)
+    assert hc.pool.available() == avail0 - 3 * steps
+    gen = [synth.tokens(6, 40 + i, steps) for i in range(3)]
+    full = [np.concatenate([c, g]).astype(np.int32) for c, g in zip(ctx, gen)]
+    with pytest.raises(ValueError):
+        eng.decode_end(db, [c for c in ctx])                  # missing the generated tokens
+    eng.decode_end(db, full if insert else None)
+    st = hc.tree.stats()
+    assert st["protected_tokens"] == 0 and len(eng._free_rows) == 8
+    if insert:
+        assert hc.pool.available() == avail0 - 3 * steps        # the generated KV stays cached
+        plan = hc.plan(full, match_all=True)
+        assert plan.prefix_len.tolist() == [len(s) for s in full] and plan.num_tokens == 0
+        hc.finish(plan)
+    else:
+        assert hc.pool.available() == avail0                    # every generated slot returned
+        assert st["cached_tokens"] == sum(len(c) for c in ctx)
