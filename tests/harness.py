@@ -93,21 +93,6 @@ def run_extend_phase(engine, model, seqs, keep_outputs=True, lse=False, layers=N
     return b, outs
 
 
-def run_workload_setup(engine, w, upto=None):
-    """Run the workload's phases (all but the last unless upto is given) through the engine.
-    Returns the last extend batch and its outputs if the last phase run was an extend."""
-    res = None
-    phases = w.phases if upto is None else w.phases[:upto]
-    for ph in phases:
-        if ph.kind == "cache":
-            run_cache_phase(engine, w.model, ph.seqs, ph.keep_locked)
-        elif ph.kind == "extend":
-            res = run_extend_phase(engine, w.model, ph.seqs)
-        else:
-            raise ValueError(ph.kind)
-    return res
-
-
 def run_decode(engine, model, seqs, lse=False, layers=None):
     """Decode phase: contexts (all but the last token) must be cached; each request decodes its
     last token. Returns (decode batch, {layer: (o, lse)}); the batch is left locked."""
