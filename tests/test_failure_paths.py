@@ -193,6 +193,7 @@ def _host_engine(hc, rows=8, max_ctx=64):
     eng.host, eng.dev = hc, _HostOnlyDevice()
     eng._free_rows = list(range(rows - 1, -1, -1))
     eng.share_decode, eng.kv_chunk, eng.max_ctx = False, 0, max_ctx
+    eng.stack_extend = False
     return eng
 
 
@@ -226,3 +227,63 @@ def test_decode_end_returns_or_caches_the_generated_tokens(insert):
     else:
         assert hc.pool.available() == avail0                    # every generated slot returned
         assert st["cached_tokens"] == sum(len(c) for c in ctx)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_engine_bookkeeping_conserves_slots(seed):
+    """Random extend and decode batches through the engine's host side, with duplicates in a
+    batch, eviction under a small pool and injected allocation failures: after every call, each
+    pool slot is either free or holds a cached token, and nothing stays locked."""
+    import random
+    rnd = random.Random(900 + seed)
+    N = 400
+    hc = runtime.HostCache(N, 128, synth.permutation(seed, N))
+    eng = _host_engine(hc, rows=8, max_ctx=128)
+    stems = [synth.tokens(seed, 10 + i, rnd.randint(5, 30)) for i in range(4)]
+
+    def new_seq():
+        s = rnd.choice(stems)[:rnd.randint(0, 30)]
+        tail = np.array([rnd.randrange(3) for _ in range(rnd.randint(1, 25))], np.int32)
+        return np.concatenate([s, tail]).astype(np.int32)
+
+    def check():
+        st = hc.tree.stats()
+        assert st["protected_tokens"] == 0
+        assert hc.pool.available() + st["cached_tokens"] == N
+        assert len(eng._free_rows) == 8
+
+    cached = []
+    for step in range(150):
+        if rnd.random() < 0.15:
+            hc.pool.inject_alloc_failure(rnd.randint(0, 1))
+        try:
+            if rnd.random() < 0.6 or not cached:
+                seqs = [new_seq() for _ in range(rnd.randint(1, 4))]
+                b = eng.extend_begin(seqs)
+                eng.extend_end(b)
+                cached += seqs
+            else:
+                ctx = [rnd.choice(cached) for _ in range(rnd.randint(1, 3))]
+                db = eng.decode_begin(ctx)
+                n = rnd.randint(1, 4)
+                try:
+                    for _ in range(n):
+                        eng.decode_step(db)
+                except rc.RcError:
+                    eng.decode_end(db)          # leave decoding: free what was generated
+                    raise
+                if rnd.random() < 0.5:
+                    done = len(db.gen_slots)
+                    full = [np.concatenate([c, np.array([rnd.randrange(3) for _ in range(done)],
+                                                        np.int32)]).astype(np.int32)
+                            for c in ctx]
+                    eng.decode_end(db, full)
+                    cached += full
+                else:
+                    eng.decode_end(db)
+        except rc.RcError as e:
+            assert e.code in (rc.RC_ERR_OOM, rc.RC_ERR_INSUFFICIENT), e
+        except ValueError:
+            pass        # a decode context evicted before it was matched: not cached any more
+        hc.pool.inject_alloc_failure(-1)
+        check()
