@@ -85,6 +85,24 @@ class HostCache:
         if host_slots:
             self.host_pool = Pool(host_slots, host_order)
             self.tree.attach_host_tier(self.host_pool)
+        # host-tier copies that a failed call left owed, oldest first; the caller performs them
+        # (take_owed) before its next device work
+        self._owed = []
+
+    def _stash_copies(self) -> None:
+        """After a failed call: take the copies its evictions and loads already owe out of the
+        tree (the tree refuses to evict while loads are pending) and keep them for take_owed."""
+        if self.host_pool is None:
+            return
+        c = self.tree.drain_copies()
+        if len(c[0]) or len(c[2]):
+            self._owed.append(c)
+
+    def take_owed(self) -> list:
+        """Copies (spill_dev, spill_host, load_host, load_dev) that failed calls left owed, oldest
+        first: perform them, each spills before loads, before any later device work."""
+        out, self._owed = self._owed, []
+        return out
 
     def _release_on_error(self, nodes, fn, *args):
         """fn(*args); if it fails, the nodes this plan's match locked are unlocked first, so a
@@ -94,6 +112,7 @@ class HostCache:
         except RcError:
             for n in nodes:
                 self.tree.unlock(int(n))
+            self._stash_copies()
             raise
 
     def _make_room(self, need: int, plan: Plan, nodes) -> None:
@@ -105,6 +124,7 @@ class HostCache:
             if rc != RC_OK:
                 for n in nodes:
                     self.tree.unlock(int(n))
+                self._stash_copies()
                 raise RcError(rc, f"make room for {need} slots ({avail} free, {freed} evicted)")
 
     host_seconds = 0.0   # accumulated time spent in the tree / pool calls of plan and finish
@@ -198,7 +218,7 @@ class HostCache:
         """n slots for decode tokens, evicting LRU leaves if the pool is short."""
         p = Plan(*(np.zeros(0),) * 9)
         self._make_room(n, p, [])
-        out = self.pool.alloc(n)
+        out = self._release_on_error([], self.pool.alloc, n)
         self.last_alloc_evicted = p.evicted
         self.last_alloc_copies = (self.tree.drain_copies() if self.host_pool is not None
                                   else None)

@@ -133,9 +133,15 @@ class Engine:
         self._free_rows.extend(int(r) for r in rows[::-1])
 
     # ---------------------------------------------------------------- extend
+    def _owed_copies(self):
+        """Host-tier copies a failed plan or allocation left owed: on the stream first."""
+        for c in self.host.take_owed():
+            self._tier_copies(c)
+
     def extend_begin(self, seqs, extra: int = 0, match_all: bool = False) -> ExtendBatch:
         # rows first: a plan allocates slots and locks prefixes, which a late failure would leak
         self._check_rows(len(seqs))
+        self._owed_copies()
         plan = self.host.plan(seqs, extra=extra, match_all=match_all)
         self._tier_copies(plan.copies)
         B = len(seqs)
@@ -184,6 +190,7 @@ class Engine:
         """Requests enter decoding: each context must be cached; it is matched and locked, its
         slots written to a fresh slot-table row. The first decode_step allocates the new tokens."""
         self._check_rows(len(contexts))
+        self._owed_copies()
         plan = self.host.plan(contexts, match_all=True)
         self._tier_copies(plan.copies)
         if plan.num_tokens:
@@ -212,6 +219,7 @@ class Engine:
         """Append one token per request: allocate its slot (evicting if needed) unless given,
         write it to the request's row at position seq_len, and upload the step's metadata."""
         B = len(batch.row_ids)
+        self._owed_copies()
         if new_slots is None:
             new_slots = self.host.alloc(B)
             self._tier_copies(self.host.last_alloc_copies)

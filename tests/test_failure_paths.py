@@ -229,16 +229,19 @@ def test_decode_end_returns_or_caches_the_generated_tokens(insert):
         assert st["cached_tokens"] == sum(len(c) for c in ctx)
 
 
+@pytest.mark.parametrize("host_slots", [0, 150])
 @pytest.mark.parametrize("seed", range(6))
-def test_engine_bookkeeping_conserves_slots(seed):
+def test_engine_bookkeeping_conserves_slots(seed, host_slots):
     """Random extend and decode batches through the engine's host side, with duplicates in a
-    batch, eviction under a small pool and injected allocation failures: after every call, each
-    pool slot is either free or holds a cached token, and nothing stays locked."""
+    batch, eviction under a small pool (spilling to a host tier and loading back, when there is
+    one) and injected allocation failures: after every call, each device slot is either free or
+    holds a cached token, each host-tier slot likewise, and nothing stays locked."""
     import random
     rnd = random.Random(900 + seed)
     N = 400
-    hc = runtime.HostCache(N, 128, synth.permutation(seed, N))
+    hc = runtime.HostCache(N, 128, synth.permutation(seed, N), host_slots=host_slots)
     eng = _host_engine(hc, rows=8, max_ctx=128)
+    eng._tier_copies = lambda copies: None     # the KV copies themselves are device work
     stems = [synth.tokens(seed, 10 + i, rnd.randint(5, 30)) for i in range(4)]
 
     def new_seq():
@@ -250,6 +253,15 @@ def test_engine_bookkeeping_conserves_slots(seed):
         st = hc.tree.stats()
         assert st["protected_tokens"] == 0
         assert hc.pool.available() + st["cached_tokens"] == N
+        if host_slots:
+            # a plan that failed after loading host-tier nodes back leaves their copies owed
+            # (handed out by the next plan or allocation): their host slots are held until then
+            import ctypes
+            from prefix_cached_paged_gb300._lib import lib
+            ns, nl = ctypes.c_int64(), ctypes.c_int64()
+            assert lib().rc_radix_pending_copies(hc.tree.h, ctypes.byref(ns),
+                                                 ctypes.byref(nl)) == rc.RC_OK
+            assert hc.host_pool.available() + st["host_tokens"] + nl.value == host_slots
         assert len(eng._free_rows) == 8
 
     cached = []
@@ -287,3 +299,33 @@ def test_engine_bookkeeping_conserves_slots(seed):
             pass        # a decode context evicted before it was matched: not cached any more
         hc.pool.inject_alloc_failure(-1)
         check()
+    if host_slots:
+        st = hc.tree.stats()
+        assert st["spilled_tokens"] > 0 and st["loaded_tokens"] > 0
+
+
+def test_failed_tiered_plan_hands_its_copies_to_the_next_call():
+    """A plan that loaded host-tier nodes back and then failed to allocate leaves copies owed.
+    Left in the tree they made every later eviction fail ("loads are pending"); now they come
+    out of take_owed (spills and loads, for the caller to run first) and the next plan that needs
+    eviction succeeds."""
+    hc = runtime.HostCache(100, 128, host_slots=200)
+    a = synth.tokens(8, 1, 60)
+    b = synth.tokens(8, 2, 60)
+    _cache(hc, [a])
+    _cache(hc, [b])                       # evicts a to the host tier (100 slots)
+    assert hc.take_owed() == [] and hc.tree.stats()["host_tokens"] == 60
+    # a + 10 new tokens: loads a back (evicting b to the host tier), then the allocation fails
+    seq = np.concatenate([a, synth.tokens(8, 3, 10)]).astype(np.int32)
+    hc.pool.inject_alloc_failure(0)
+    with pytest.raises(rc.RcError) as e:
+        hc.plan([seq])
+    assert e.value.code == rc.RC_ERR_OOM
+    owed = hc.take_owed()
+    assert len(owed) == 1 and len(owed[0][0]) > 0 and len(owed[0][2]) == 60
+    assert hc.take_owed() == []
+    # the same request again: needs eviction, and works
+    plan = hc.plan([seq])
+    assert plan.prefix_len.tolist() == [60]
+    hc.finish(plan)
+    assert hc.tree.stats()["protected_tokens"] == 0
