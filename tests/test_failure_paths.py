@@ -329,3 +329,52 @@ def test_failed_tiered_plan_hands_its_copies_to_the_next_call():
     assert plan.prefix_len.tolist() == [60]
     hc.finish(plan)
     assert hc.tree.stats()["protected_tokens"] == 0
+
+
+@pytest.mark.parametrize("host_slots", [0, 120])
+@pytest.mark.parametrize("seed", range(4))
+def test_fork_style_steps_conserve_slots(seed, host_slots):
+    """The mixed step's interleaving on the host side: a decode batch lives across steps and takes
+    its new tokens' slots from each extend plan's extra allocation, under a nearly full pool and
+    injected failures. While it lives, free + cached + its generated slots = the pool; after
+    decode_end (inserting or freeing), free + cached = the pool and nothing is locked."""
+    import random
+    rnd = random.Random(seed)
+    N = 500
+    hc = runtime.HostCache(N, 256, synth.permutation(seed, N), host_slots=host_slots)
+    eng = _host_engine(hc, rows=16, max_ctx=256)
+    eng._tier_copies = lambda copies: None
+    ctx = [synth.tokens(seed, 100 + i, rnd.randint(10, 40)) for i in range(3)]
+    _cache(hc, ctx)
+    db = eng.decode_begin(ctx)
+    progs = [synth.tokens(seed, 200 + i, rnd.randint(10, 30)) for i in range(2)]
+    _cache(hc, progs)
+    gen_tok = [[] for _ in ctx]
+    failed = 0
+    for step in range(40):
+        if rnd.random() < 0.15:
+            hc.pool.inject_alloc_failure(rnd.randint(0, 1))
+        seqs = [np.concatenate([rnd.choice(progs),
+                                synth.tokens(seed, 1000 + 10 * step + f, rnd.randint(1, 20))])
+                .astype(np.int32) for f in range(rnd.randint(1, 3))]
+        try:
+            eb = eng.extend_begin(seqs, extra=len(ctx))
+        except rc.RcError:
+            failed += 1
+            hc.pool.inject_alloc_failure(-1)
+            continue
+        eng.decode_step(db, new_slots=eb.plan.extra)
+        for g in gen_tok:
+            g.append(rnd.randrange(5))
+        eng.extend_end(eb)
+        hc.pool.inject_alloc_failure(-1)
+        st = hc.tree.stats()
+        assert hc.pool.available() + st["cached_tokens"] + len(db.gen_slots) * len(ctx) == N
+    assert failed > 0
+    full = [np.concatenate([c, np.array(g, np.int32)]).astype(np.int32)
+            for c, g in zip(ctx, gen_tok)]
+    eng.decode_end(db, full if seed % 2 else None)
+    st = hc.tree.stats()
+    assert st["protected_tokens"] == 0 and hc.pool.available() + st["cached_tokens"] == N
+    if host_slots:
+        assert hc.host_pool.available() + st["host_tokens"] == host_slots
