@@ -436,7 +436,9 @@ int rc_decode_attention(const rc_decode_args* args, void* workspace, size_t work
  *     that device current); make that first call before any stream capture.
  *   - All calls on a device share the area and it keeps the last call's contents (everything
  *     that must start at zero is reset by the call itself). Calls whose kernels overlap on the
- *     GPU -- on different streams without ordering between them -- race on the area. */
+ *     GPU -- on different streams without ordering between them -- race on the area.
+ *   - reuse_plan is ignored: the job list in the shared area may belong to any earlier call on
+ *     the device (another caller's, or one with other arguments), so every call plans afresh. */
 #define RC_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int rc_decode_attention_noalloc(const rc_decode_args* args, void* stream);
 

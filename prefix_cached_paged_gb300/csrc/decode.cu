@@ -910,20 +910,25 @@ template <typename T, int D, int G>
 int launch_t(const Params& p, cudaStream_t s) {
   using C = MainKernel<T, D, G>;
   auto kern = C::fn;
-  static int blocks_per_sm = -1;
-  static int num_sms = 0;
-  static std::once_flag once;
-  static cudaError_t init_err = cudaSuccess;
-  std::call_once(once, [&]() {
-    init_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    int dev = 0;
-    if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
-    if (init_err == cudaSuccess)
-      init_err = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (init_err == cudaSuccess)
-      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kern,
-                                                               kWarps * 32, C::SMEM);
-  });
+  struct Setup {
+    int num_sms = 0, blocks_per_sm = 0;
+  };
+  static PerDevice<Setup> setup;
+  const Setup* su = nullptr;
+  const cudaError_t init_err = setup.get(
+      [&](Setup& st) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        int dev = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+          e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&st.blocks_per_sm, kern,
+                                                            kWarps * 32, C::SMEM);
+        return e;
+      },
+      &su);
   if (init_err != cudaSuccess)
     return fail(RC_ERR_CUDA, "rc_decode_attention: setup: %s", cudaGetErrorString(init_err));
   // bf16 can reuse the plan of the previous call (the main kernel leaves the item counter reset)
@@ -933,7 +938,7 @@ int launch_t(const Params& p, cudaStream_t s) {
     decode_plan_kernel<<<1, 1024, 0, s>>>(p);
     ++n;
   }
-  const int grid = std::max(1, num_sms * std::max(1, blocks_per_sm));
+  const int grid = std::max(1, su->num_sms * std::max(1, su->blocks_per_sm));
   kern<<<grid, kWarps * 32, C::SMEM, s>>>(p);
   ++n;
   dim3 mg(p.a.num_reqs, p.a.num_q_heads);
@@ -1007,8 +1012,7 @@ extern "C" int rc_decode_attention(const rc_decode_args* a, void* workspace,
 // per device (host code may not use the symbol itself as a device pointer).
 namespace {
 __device__ __align__(256) unsigned char g_decode_scratch[RC_DECODE_STATIC_SCRATCH_BYTES];
-constexpr int kMaxScratchDevices = 64;
-void* g_decode_scratch_ptr[kMaxScratchDevices] = {};
+void* g_decode_scratch_ptr[rc::kMaxDevices] = {};
 std::mutex g_decode_scratch_mu;
 }  // namespace
 
@@ -1025,7 +1029,7 @@ extern "C" int rc_decode_attention_noalloc(const rc_decode_args* a, void* stream
                     need, (size_t)RC_DECODE_STATIC_SCRATCH_BYTES);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices)
+  if (e != cudaSuccess || dev < 0 || dev >= rc::kMaxDevices)
     return rc::fail(RC_ERR_CUDA, "rc_decode_attention_noalloc: no usable current device");
   void* ptr = nullptr;
   {
@@ -1039,5 +1043,9 @@ extern "C" int rc_decode_attention_noalloc(const rc_decode_args* a, void* stream
     }
     ptr = g_decode_scratch_ptr[dev];
   }
-  return rc_decode_attention(a, ptr, RC_DECODE_STATIC_SCRATCH_BYTES, stream);
+  // The shared area's job list may come from another caller's call (or from an fp32 call,
+  // which leaves the item counter as it was): always plan afresh.
+  rc_decode_args local = *a;
+  local.reuse_plan = 0;
+  return rc_decode_attention(&local, ptr, RC_DECODE_STATIC_SCRATCH_BYTES, stream);
 }

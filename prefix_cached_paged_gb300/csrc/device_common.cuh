@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "rc.h"
 
 namespace rc {
@@ -19,6 +21,35 @@ enum DeviceStatus : int {
 // Address of the device status word on the current device (host side, cached per device).
 int* device_status_ptr();
 int check_launch(const char* what);
+
+// One-time setup of a kernel launch, done once per device (function attributes such as the
+// shared-memory opt-in, SM counts and occupancies belong to a device): `init(T&)` runs the first
+// time a device is current and its cudaError_t is kept with the result.
+constexpr int kMaxDevices = 64;
+template <typename T>
+class PerDevice {
+ public:
+  template <typename F>
+  cudaError_t get(F init, const T** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (!done_[dev]) {
+      err_[dev] = init(val_[dev]);
+      done_[dev] = true;
+    }
+    *out = &val_[dev];
+    return err_[dev];
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+  cudaError_t err_[kMaxDevices] = {};
+  T val_[kMaxDevices] = {};
+};
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   atomicCAS(status, 0, code);

@@ -37,8 +37,6 @@
 //                grows by more than 8 in log2 units); weights rounded to bf16, normalised by
 //                the sum of the rounded weights; epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
-#include <mutex>
-
 #include "device_common.cuh"
 #include "extend_common.h"
 #include "host_common.h"
@@ -1001,34 +999,35 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   if (a->head_dim != kD) return fail(RC_ERR_INVALID, "extend (tensor cores): head_dim must be 128");
   const int G = a->num_q_heads / a->num_kv_heads;
   if (G > kM) return fail(RC_ERR_INVALID, "extend (tensor cores): group size %d > 128", G);
-  // per instantiation: opt in to the shared memory, and check that the launch allocation
-  // covers the register split (the softmax warpgroups' setmaxnreg.inc would never return)
+  // per instantiation and device: opt in to the shared memory, and check that the launch
+  // allocation covers the register split (the softmax warpgroups' setmaxnreg.inc would never
+  // return)
   struct Setup {
-    cudaError_t err = cudaSuccess;
-    int regs = 0;
+    int regs[2] = {0, 0};
   };
-  auto setup = [](auto kern) {
-    Setup st;
-    st.err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  SmemLayout::ALLOC);
-    cudaFuncAttributes fa;
-    if (st.err == cudaSuccess) st.err = cudaFuncGetAttributes(&fa, kern);
-    if (st.err == cudaSuccess) st.regs = fa.numRegs;
-    return st;
-  };
-  static std::once_flag once;
-  static Setup s_plain, s_stack;
-  std::call_once(once, [&]() {
-    s_plain = setup(extend_tc_kernel<false>);
-    s_stack = setup(extend_tc_kernel<true>);
-  });
-  for (const Setup* st : {&s_plain, &s_stack}) {
-    if (st->err != cudaSuccess)
-      return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(st->err));
-    if (st->regs < kRegsLaunch)
+  static PerDevice<Setup> setup;
+  const Setup* su = nullptr;
+  const cudaError_t err = setup.get(
+      [](Setup& st) {
+        int i = 0;
+        for (const void* kern : {(const void*)extend_tc_kernel<false>,
+                                 (const void*)extend_tc_kernel<true>}) {
+          cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               SmemLayout::ALLOC);
+          cudaFuncAttributes fa;
+          if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+          if (e != cudaSuccess) return e;
+          st.regs[i++] = fa.numRegs;
+        }
+        return cudaSuccess;
+      },
+      &su);
+  if (err != cudaSuccess)
+    return fail(RC_ERR_CUDA, "extend (tensor cores): %s", cudaGetErrorString(err));
+  for (int regs : su->regs)
+    if (regs < kRegsLaunch)
       return fail(RC_ERR_CUDA, "extend (tensor cores): kernel built with %d registers per "
-                  "thread, the register split needs %d", st->regs, kRegsLaunch);
-  }
+                  "thread, the register split needs %d", regs, kRegsLaunch);
   TcParams p;
   p.a = *a;
   p.status = status;

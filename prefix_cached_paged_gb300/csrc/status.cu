@@ -7,8 +7,7 @@
 
 namespace {
 __device__ int g_status_word;
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {};
+int* g_status_ptr[rc::kMaxDevices] = {};
 std::mutex g_status_mu;
 }  // namespace
 

@@ -145,8 +145,12 @@ def test_extend_bf16_ragged_all_units(Hq, Hkv):
 
 
 def _sample_units(rng, n_req, layers, n_kv, k):
-    return sorted({(int(rng.integers(n_req)), int(rng.integers(layers)), int(rng.integers(n_kv)))
-                   for _ in range(k)})
+    """k distinct (request, layer, KV head) units (all of them if there are fewer)."""
+    k = min(k, n_req * layers * n_kv)
+    units = set()
+    while len(units) < k:
+        units.add((int(rng.integers(n_req)), int(rng.integers(layers)), int(rng.integers(n_kv))))
+    return sorted(units)
 
 
 def test_few_shot_extend_full_size_sampled():
@@ -201,9 +205,10 @@ def _decode_scatter(eng, w, seqs, db):
     m = w.model
     h = np.array([synth.prefix_hashes(m.seed, s)[-1] for s in seqs], dtype=np.uint64)
     for layer in range(m.layers):
-        kk = eng.dev.k[layer][db.new_slots].float().cpu().numpy()
-        np.testing.assert_array_equal(
-            kk, synth.values(h, synth.TENSOR_K, layer, range(m.n_kv_heads), m.head_dim, m.dtype))
+        for plane, tensor in ((eng.dev.k, synth.TENSOR_K), (eng.dev.v, synth.TENSOR_V)):
+            got = plane[layer][db.new_slots].float().cpu().numpy()
+            np.testing.assert_array_equal(
+                got, synth.values(h, tensor, layer, range(m.n_kv_heads), m.head_dim, m.dtype))
 
 
 @pytest.mark.parametrize("chunk", [0, 64, 192, 4096])
@@ -664,7 +669,8 @@ def test_fork_mixed_step_full_size_sampled():
     512..8192-token contexts in fork groups) in the benchmark's launch configuration, on two of
     its 32 layers (every layer launches the same kernels): two consecutive steps, each checking
     a seeded sample of extend and decode units against the oracle, the slot rows and the
-    scattered K/V. Decode inputs at step s come from each request's real s-th generated token."""
+    scattered K/V (extend and decode). Decode inputs at step s come from each request's real s-th
+    generated token."""
     import torch
     from synth import device as sdev
     fm = W.fork_mixed_step(layers=2)
@@ -702,10 +708,12 @@ def test_fork_mixed_step_full_size_sampled():
             eng.decode_layer(db, layer, dq, dk, dv, do, lse=dl, max_total_tokens=mt)
             dec_outs[layer] = (do, dl)
         torch.cuda.synchronize()
-        _check_extend(w, eb, ext_outs, seqs, _sample_units(rng, 80, 2, 32, 40))
-        _check_decode(w, db, dec_outs, dseqs, _sample_units(rng, Bd, 2, 32, 40) +
+        # at least 64 sampled (request, layer, head) units per kernel and step
+        _check_extend(w, eb, ext_outs, seqs, _sample_units(rng, 80, 2, 32, 64))
+        _check_decode(w, db, dec_outs, dseqs, _sample_units(rng, Bd, 2, 32, 64) +
                       [(int(np.argmax([len(s) for s in dseqs])), 1, 7)])
         _check_slot_rows(eng, eb)
         _check_scatter(eng, w, seqs, eb, sample=rng.choice(eb.num_tokens, 256, replace=False))
+        _decode_scatter(eng, w, dseqs, db)
         eng.extend_end(eb)
     _status_clear()

@@ -328,3 +328,77 @@ def test_lock_protects_exactly_the_matched_prefix():
     tree.unlock(node)
     ok, freed, _ = tree.evict(3)
     assert ok and freed == 3 and pool.available() == 100
+
+
+def _cache_one(sim, seq):
+    r = sim.extend_prepare([seq], match_all=True)
+    sim.extend_finish([seq], r)
+    return r.rows[0].tolist()
+
+
+def test_decode_prepare_locks_evicts_then_allocates():
+    """Decode entry under memory pressure, expected slots worked out by hand (paper digest
+    App. A.1: a decode step appends one token per request over its cached KV; Sec. 3 and
+    Fig. 3: running requests hold references, eviction takes the least recently used
+    unreferenced leaves, whole nodes, and freed slots go to the tail of the free list).
+    Pool of 12 slots in identity order; A, B, C cached in that order (A oldest):
+      A = [1 2 3 4] -> slots 0-3, B = [5 6 7] -> 4-6, C = [8 9 10 11] -> 7-10; free [11].
+    Decoding A and C: both matched whole and locked (the matches make them newer than B); two
+    new slots are needed, one is free, so eviction frees the shortfall: B, the LRU unreferenced
+    leaf (3 tokens, slots 4 5 6 to the tail: free [11 4 5 6]); then the new tokens get 11 and 4
+    in request order."""
+    sim = oracle.CacheSim(12)
+    A, B, C = [1, 2, 3, 4], [5, 6, 7], [8, 9, 10, 11]
+    assert [_cache_one(sim, s) for s in (A, B, C)] == [[0, 1, 2, 3], [4, 5, 6], [7, 8, 9, 10]]
+    r = sim.decode_prepare([A, C])
+    assert r.prefix_len == [4, 4]
+    assert [x.tolist() for x in r.rows] == [[0, 1, 2, 3], [7, 8, 9, 10]]
+    assert (r.evict_request, r.evicted) == (1, 3)
+    assert r.extra_slots.tolist() == [11, 4]
+    assert sim.pool.available() == 2
+    assert sim.pool.alloc(2).tolist() == [5, 6]   # the rest of B's slots, in token order
+    keys = {tuple(n["key"].tolist()) for n in sim.tree.nodes()}
+    assert keys == {tuple(A), tuple(C)}
+    # the running contexts stay protected: nothing else is unreferenced
+    ok, freed, _ = sim.tree.evict(1)
+    assert not ok and freed == 0
+
+
+def test_decode_prepare_cannot_evict_a_running_context():
+    """Three decoding requests lock every cached node (A, B, C as above); three new slots are
+    needed with one free, so there is nothing to evict: the step must fail rather than take a
+    context that a running request reads (Sec. 3: only nodes with reference count 0 go)."""
+    sim = oracle.CacheSim(12)
+    for s in ([1, 2, 3, 4], [5, 6, 7], [8, 9, 10, 11]):
+        _cache_one(sim, s)
+    with pytest.raises(oracle.OutOfSlots):
+        sim.decode_prepare([[1, 2, 3, 4], [8, 9, 10, 11], [5, 6, 7]])
+    assert sim.pool.available() == 1
+    assert len(sim.tree.nodes()) == 3
+
+
+def test_mixed_step_allocates_extend_suffixes_before_decode_tokens():
+    """A mixed step (extend batch plus `extra` decode tokens), expected slots by hand.
+    Pool of 10 slots in identity order; X = [1 2 3 4 5] -> 0-4, Y = [6 7 8] -> 5-7 and
+    Z = [20 21] -> 8 9 cached in that order; nothing is free. Extending X + [9 10] matches and
+    locks X (5 tokens, the match makes X the newest) and needs 2 suffix slots + 2 decode slots:
+    eviction frees the shortfall of 4 leaf by leaf in LRU order, Y (3) then Z (2), giving free
+    [5 6 7 8 9]; the suffix takes 5 6 (request order first), the decode tokens 7 8."""
+    sim = oracle.CacheSim(10)
+    for s in ([1, 2, 3, 4, 5], [6, 7, 8], [20, 21]):
+        _cache_one(sim, s)
+    seq = [1, 2, 3, 4, 5, 9, 10]
+    r = sim.extend_prepare([seq], extra=2)
+    assert r.prefix_len == [5]
+    assert (r.evict_request, r.evicted) == (4, 5)
+    assert r.rows[0].tolist() == [0, 1, 2, 3, 4, 5, 6]
+    assert r.extra_slots.tolist() == [7, 8]
+    assert sim.pool.available() == 1
+    # without pressure: two requests, suffixes in request order, then the decode slots
+    sim = oracle.CacheSim(16)
+    for s in ([1, 2, 3, 4, 5], [6, 7, 8]):
+        _cache_one(sim, s)
+    r = sim.extend_prepare([[1, 2, 3, 4, 5, 9, 10], [6, 7, 8, 11]], extra=2)
+    assert r.prefix_len == [5, 3] and (r.evict_request, r.evicted) == (0, 0)
+    assert [x.tolist() for x in r.rows] == [[0, 1, 2, 3, 4, 8, 9], [5, 6, 7, 10]]
+    assert r.extra_slots.tolist() == [11, 12]
