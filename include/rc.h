@@ -442,6 +442,13 @@ int rc_decode_attention(const rc_decode_args* args, void* workspace, size_t work
 #define RC_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 int rc_decode_attention_noalloc(const rc_decode_args* args, void* stream);
 
+/* Test hook; the pages have no counterpart. Bound, in nanoseconds, of every wait inside the
+ * extend kernel (0 restores the default, 2 s). With a short bound waits give up: the kernel
+ * records code 3 in the device status word, stops issuing work and returns without hanging; its
+ * outputs are then not written. The wait that guards the release of tensor memory keeps the
+ * default. Applies to launches made after the call, on every device. */
+int rc_debug_set_wait_limit_ns(uint64_t ns);
+
 /* Read and clear the device status word of the current device (synchronises `stream`).
  * *out_code = 0 if no kernel reported bad data since the last call, else the first code seen:
  * 1 slot out of range, 2 position beyond the slot-table row, 3 a wait expired. */

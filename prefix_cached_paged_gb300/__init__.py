@@ -39,6 +39,12 @@ def launch_count() -> int:
     return int(lib().rc_launch_count())
 
 
+def set_wait_limit_ns(ns: int) -> None:
+    """Test hook (rc_debug_set_wait_limit_ns): bound of the extend kernel's waits for later
+    launches; 0 restores the default."""
+    check(lib().rc_debug_set_wait_limit_ns(int(ns)), "rc_debug_set_wait_limit_ns")
+
+
 class Pool:
     """The token pool (free list of KV slots). rc_pool_* / rc_kv_pool_*."""
 

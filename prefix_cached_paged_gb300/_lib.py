@@ -63,6 +63,7 @@ SIGNATURES = {
     "rc_decode_attention": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
     "rc_decode_attention_noalloc": (ctypes.c_int, [_P, _P]),
     "rc_device_status": (ctypes.c_int, [ctypes.POINTER(_I32), _P]),
+    "rc_debug_set_wait_limit_ns": (ctypes.c_int, [_U64]),
 }
 
 

@@ -21,6 +21,9 @@ enum DeviceStatus : int {
 // Address of the device status word on the current device (host side, cached per device).
 int* device_status_ptr();
 int check_launch(const char* what);
+// Bound of the waits inside the kernels that take one from the host (default 2 s; a test hook
+// shortens it).
+uint64_t wait_limit_ns();
 
 // One-time setup of a kernel launch, done once per device (function attributes such as the
 // shared-memory opt-in, SM counts and occupancies belong to a device): `init(T&)` runs the first

@@ -77,7 +77,8 @@ struct SmemLayout {
   static constexpr int BAR = V + kStagesKV * kTileBytes;
   // k_full[2] k_empty[2] v_full[2] v_empty[2] s_full[2] (unused)[2] o_done[2] e_done q_full drain
   static constexpr int NBAR = 4 * kStagesKV + 9;
-  static constexpr int TMEM_SLOT = BAR + NBAR * 8;
+  static constexpr int TMEM_SLOT = BAR + NBAR * 8;   // TMEM address; MMA_DONE 8 bytes on
+  static constexpr int MMA_DONE = TMEM_SLOT + 8;     // set once the MMA warp syncs no more
   // split-mode merge: row maxima, rounded and exact sums of each virtual tile [X][row]
   static constexpr int XMRG = TMEM_SLOT + 16;
   static constexpr int TOTAL = XMRG + 3 * 2 * 128 * 4;
@@ -95,6 +96,7 @@ struct TcParams {
   int group_lo;      // stacked pass: group of CTA z = group_lo + z (one launch per level)
   int nlevels;       // levels of stacking groups (>= 1 when num_groups > 0)
   int level_lo[RC_MAX_STACK_LEVELS + 1];   // groups of level l: [level_lo[l], level_lo[l+1])
+  uint64_t wait_limit_ns;   // bound of every wait except the final drain
 };
 
 // The group among groups [g0, g1) holding request b (ranges ascending and disjoint within a
@@ -337,6 +339,35 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
       : "memory");
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for a phase for at most limit_ns (the launch's bound: 2 s, or a test hook's shorter
+// one). On expiry: status code, false. done != nullptr: also give up (without a status code)
+// once *done is set. A bound under 1 ms polls without suspending (test_wait): a suspended
+// try_wait may sleep until the phase completes, which would hide a short bound.
+__device__ __forceinline__ bool wait_lim(uint64_t* bar, uint32_t parity, int* status,
+                                         uint64_t limit_ns, volatile int* done = nullptr) {
+  const bool short_limit = limit_ns < 1000000;
+  if (!short_limit && mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!(short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
+    if (done && *done) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      set_status(status, kStatusWaitExpired);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- the kernel
 template <bool kStack>
 __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_constant__ TcParams p) {
@@ -470,6 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   uint64_t* drain = q_full + 1;                 // every issued MMA has completed
   static_assert(4 * kStagesKV + 9 == SmemLayout::NBAR, "barrier count");
   uint32_t* tmem_slot = (uint32_t*)(smem + SmemLayout::TMEM_SLOT);
+  volatile int* mma_done = (volatile int*)(smem + SmemLayout::MMA_DONE);
+  const uint64_t lim = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesKV; ++s) {
@@ -485,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     mbar_init(e_done, 2 * kGroupThreads);
     mbar_init(q_full, kThreads);
     mbar_init(drain, 1);
+    *mma_done = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -632,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const bool first = split || X == 0 || kt >= nA;
         const bool last = split || X == 1 || kt >= nB;
         if (first) {
-          if (!mbar_wait(&k_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+          if (!wait_lim(&k_full[st], (kt / kStagesKV) & 1, p.status, lim)) return false;
           // K arrived through the generic proxy (cp.async); one fence covers every later
           // MMA issued on the stage
           fence_async_smem();
@@ -652,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         const bool first = split || X == 0 || kt >= nA;
         const bool last = split || X == 1 || kt >= nB;
         if (first) {
-          if (!mbar_wait(&v_full[st], (kt / kStagesKV) & 1, p.status)) return false;
+          if (!wait_lim(&v_full[st], (kt / kStagesKV) & 1, p.status, lim)) return false;
           fence_async_smem();   // V arrived through the generic proxy (cp.async)
         }
         tc_fence_after();
@@ -662,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (last) mma_commit_by(smem_u32(&v_empty[st]), leader);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, p.status);
+      bool ok = wait_lim(q_full, 0, p.status, lim);
       fence_async_smem();   // Q arrived through the generic proxy (cp.async)
       if (ok) ok = qk(0, 0);
       if (ok && nt1 > 0) ok = qk(1, 0);
@@ -676,7 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
           if (ok && t + 1 < nt1) ok = qk(1, t + 1);
         }
       }
+      // no weights sync follows: a softmax group shadowing this warp may stop
+      if (leader) *mma_done = 1;
       // every MMA issued above completes before TMEM is freed, also when a wait gave up early
+      // (this wait keeps the full bound whatever the launch's: it guards the deallocation)
       mma_commit_by(smem_u32(drain), leader);
       mbar_wait(drain, 0, p.status);
     }
@@ -697,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         n0 = raw(j + 1, 0);
         n1 = raw(j + 1, 1);
       }
-      if (j >= kStagesKV) ok = mbar_wait(&empty[st], ((j / kStagesKV) - 1) & 1, p.status);
+      if (j >= kStagesKV) ok = wait_lim(&empty[st], ((j / kStagesKV) - 1) & 1, p.status, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       copy_tile(j, p0, p1);
@@ -772,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     bool ok = true;
     int j = 0;
     for (; j < nX; ++j) {
-      ok = mbar_wait(&s_full[X], j & 1, p.status);
+      ok = wait_lim(&s_full[X], j & 1, p.status, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       if (warp_idle) {
@@ -867,9 +904,17 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       l_exact = l_exact * alpha + (b0 + b1);
       m_run = m_use;
     }
-    // a wait that gave up ends the loop early: hand the MMA warp its remaining weights anyway
-    // (garbage; the status word already records the failure) so that its syncs complete
-    for (; j < nX; ++j) named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
+    // A wait that gave up ends the loop early (the status word records the failure; the
+    // outputs are not valid). The MMA warp's weights syncs cannot time out, so the group keeps
+    // answering them: one arrival for each further Q.K^T of its tile the MMA warp completes (an
+    // arrival thus never runs ahead of the sync it answers), until the MMA warp has left its
+    // schedule (mma_done); the bound is a backstop beyond any wait of the MMA warp.
+    const uint64_t shadow_lim = 8 * lim + 1000000000ull;
+    for (; j < nX; ++j) {
+      if (!__all_sync(0xffffffffu, wait_lim(&s_full[X], j & 1, p.status, shadow_lim, mma_done)))
+        break;
+      named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
+    }
     // The row's result over this pass's keys is (O, lse2): O the accumulator(s) times `scale`,
     // lse2 its log2-sum-exp. The stacked pass stores it as a partial (O in o, lse2 in the
     // workspace); a group member's per-request pass merges it with that partial, weights
@@ -905,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     };
     if (nX > 0 && !split) {
       // epilogue: O / l for this thread's row
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, wait_lim(&o_done[X], 0, p.status, lim));
       if (ok) {
         tc_fence_after();
         const bool store = row_valid;
@@ -934,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     } else if (split) {
       // merge the two virtual tiles: every softmax thread publishes its row max and sums;
       // thread (X, row) then writes columns [64 X, 64 X + 64) of the merged row
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[X], 0, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, wait_lim(&o_done[X], 0, p.status, lim));
       float* xm = (float*)(smem + SmemLayout::XMRG);     // [X][row] maxima
       float* xl = xm + 2 * 128;                          // [X][row] rounded-weight sums
       float* xe = xl + 2 * 128;                          // [X][row] exact sums
@@ -942,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       xl[X * 128 + r] = l_run;
       xe[X * 128 + r] = l_exact;
       mbar_arrive(e_done);
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(e_done, 0, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, wait_lim(e_done, 0, p.status, lim));
       if (ok) {
         const float m0 = xm[r], m1 = xm[128 + r];
         const float M = fmaxf(m0, m1);
@@ -1034,6 +1079,7 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   p.ppt = kM / G;
   p.scale2 = a->sm_scale * kLog2e;
   p.lse_part = (float*)a->workspace;
+  p.wait_limit_ns = wait_limit_ns();
   int launches = 0;
   p.group_lo = 0;
   p.nlevels = a->num_levels > 1 ? a->num_levels : 1;

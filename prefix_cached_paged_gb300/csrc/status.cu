@@ -1,5 +1,6 @@
 // The device status word: kernels that meet bad data (an out-of-range slot or position, an
 // expired wait) record a code here instead of trapping, and the host reads it back.
+#include <atomic>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -25,6 +26,15 @@ int* device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{0};
+}  // namespace
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load();
+  return v ? v : 2000000000ull;
+}
+
 int check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RC_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
@@ -45,5 +55,10 @@ extern "C" int rc_device_status(int32_t* out_code, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return rc::fail(RC_ERR_CUDA, "rc_device_status: %s", cudaGetErrorString(e));
   *out_code = v;
+  return RC_OK;
+}
+
+extern "C" int rc_debug_set_wait_limit_ns(uint64_t ns) {
+  rc::g_wait_limit_ns.store(ns);
   return RC_OK;
 }
