@@ -362,6 +362,46 @@ typedef struct rc_extend_args {
 int rc_extend_workspace_bytes(const rc_extend_args* args, size_t* out_bytes);
 int rc_extend_attention(const rc_extend_args* args, void* stream);
 
+/* Planner of the extend call's prefix stacking (the shared-prefix query stacking of the paper
+ * digest's related work, Sec. 7; host only). From the batch's host slot rows (rows[b] the slots
+ * of request b, its prefix_len[b] matched tokens first; row_stride int32 per row) it finds, level
+ * by level of the radix tree, runs of consecutive requests whose rows hold the same slots over
+ * at least min_shared positions past their parent's shared length (level 0: from 0); a run's
+ * shared length is its members' smallest agreement with its first member. Under RC_STACK_COST a
+ * run is kept where a cost model of the extend kernel (calibrated on GB300) estimates stacking
+ * to save 10% or more; a run not kept is not searched further. An innermost kept group folds
+ * (takes its members' remainders in its own pass) under RC_FOLD_ALL, or under RC_FOLD_COST where
+ * the model estimates the folded pass at no more than the stacked pass plus the members' own;
+ * a group folds only if each CTA of its pass has at most 512 remainder key tiles and 256
+ * members. group_size = query heads per KV head. The outputs fill rc_extend_args: group_range,
+ * group_shared, group_start, group_fold (capacity entries; num_reqs * max_levels suffice),
+ * level_indptr (num_levels + 1 entries used), max_group_rows, skip_request_pass = all_folded.
+ * RC_ERR_INVALID if an argument is out of range or more groups than capacity are found. */
+enum { RC_STACK_COST = 0, RC_STACK_ALL = 1 };
+enum { RC_FOLD_NONE = 0, RC_FOLD_COST = 1, RC_FOLD_ALL = 2 };
+typedef struct rc_stack_plan_args {
+  int32_t num_reqs;
+  const int32_t* rows;           /* host [num_reqs, row_stride] */
+  int64_t row_stride;
+  const int32_t* prefix_len;     /* host [num_reqs] matched tokens, <= row_stride */
+  const int32_t* new_len;        /* host [num_reqs] new tokens */
+  int32_t min_shared;            /* >= 1 */
+  int32_t group_size;            /* >= 1 */
+  int32_t max_levels;            /* 1 .. RC_MAX_STACK_LEVELS */
+  int32_t policy;                /* RC_STACK_COST or RC_STACK_ALL */
+  int32_t fold;                  /* RC_FOLD_NONE, RC_FOLD_COST or RC_FOLD_ALL */
+} rc_stack_plan_args;
+typedef struct rc_stack_plan {
+  int32_t capacity;              /* in: entries of the four arrays below */
+  int32_t* group_range;          /* out: [2 capacity] host */
+  int32_t* group_shared;         /* out: [capacity] */
+  int32_t* group_start;          /* out: [capacity] */
+  int32_t* group_fold;           /* out: [capacity] */
+  int32_t level_indptr[RC_MAX_STACK_LEVELS + 1];   /* out; entries past num_levels = num_groups */
+  int32_t num_groups, num_levels, max_group_rows, all_folded;   /* out */
+} rc_stack_plan;
+int rc_plan_extend_stacking(const rc_stack_plan_args* args, rc_stack_plan* out);
+
 /* Decode attention (paper digest App. A.1; RadixAttention explainer: each generated token
  * attends to the KV of all previous tokens). Request b has seq_len[b] tokens including its new
  * one, whose slot is out_loc[b] == req_to_token[req_idx[b], seq_len[b]-1]. Its query q[b]
@@ -418,6 +458,19 @@ typedef struct rc_decode_args {
 } rc_decode_args;
 /* Workspace bytes rc_decode_attention needs for these arguments (device memory, 256-B aligned,
  * no initialisation needed). */
+/* Planner of decode's shared-context groups (host only): requests whose host slot rows
+ * (rows[b], lengths[b] context tokens, row_stride int32 per row) start with the same slot share
+ * that prefix's KV. Greedy, bucket by bucket in order of first appearance of the first slot: the
+ * bucket's first request leads; the others with the longest common slot prefix join (ties: the
+ * later request first), up to group_size members in all, while that prefix is at least
+ * min_shared tokens; the group's shared length is its members' smallest common prefix. Requests
+ * shorter than max(min_shared, 1) take part in none. Outputs (host; num_reqs + 1, num_reqs and
+ * num_reqs entries suffice) fill rc_decode_args' group_indptr, group_members and group_shared.
+ * group_size < 2 or fewer than two requests: no group. */
+int rc_plan_decode_groups(const int32_t* rows, int64_t row_stride, const int64_t* lengths,
+                          int32_t num_reqs, int32_t group_size, int64_t min_shared,
+                          int32_t* out_indptr, int32_t* out_members, int32_t* out_shared,
+                          int32_t* out_num_groups);
 int rc_decode_workspace_bytes(const rc_decode_args* args, size_t* out_bytes);
 int rc_decode_attention(const rc_decode_args* args, void* workspace, size_t workspace_bytes,
                         void* stream);

@@ -17,7 +17,8 @@ import numpy as np
 
 from ._lib import (RC_DTYPE_BF16, RC_DTYPE_F32, RC_ERR_CUDA, RC_ERR_DEVICE, RC_ERR_INSUFFICIENT,
                    RC_ERR_INVALID, RC_ERR_OOM, RC_OK, RC_SCHED_FCFS, RC_SCHED_LSPF, RcDecodeArgs,
-                   RcError, RcExtendArgs, RcKvCopyArgs, RcSlotWriteArgs, RcStats, check, lib)
+                   RcError, RcExtendArgs, RcKvCopyArgs, RcSlotWriteArgs, RcStackPlan,
+                   RcStackPlanArgs, RcStats, check, lib)
 
 __all__ = [
     "Pool", "RadixTree", "RcError", "slot_table_write", "extend_attention", "decode_attention",
@@ -425,174 +426,55 @@ def decode_attention(q, k_new, v_new, out_loc, seq_len, req_idx, req_to_token, k
 DEFAULT_KV_CHUNK = 512   # tokens per split-K chunk when kv_chunk = 0 (rc.h)
 
 
-# Cost model of one extend CTA, calibrated on GB300 (fork, two-level and few-shot replays):
-# about 2.15 us per 128-key tile for a pair of query tiles (half that for a lone tile, whose
-# key tiles split across the two softmax groups), 10 us of fixed cost per CTA, 1 us to merge.
-_T_TILE_US, _C_CTA_US, _C_MERGE_US = 2.15, 10.0, 1.0
-
-
-def _extend_cost_us(P, S, key0, ppt, merge):
-    """Estimated CTA-time of one request's per-request pass over keys [key0, P) and its S new
-    tokens, ppt query positions per tile."""
-    if S <= 0:
-        return 0.0
-    tiles = -(-(P - key0) // 128) + -(-S // 128)
-    pairs = -(-S // (2 * ppt))
-    per = tiles * (_T_TILE_US if S > ppt else _T_TILE_US / 2)
-    return pairs * (per + _C_CTA_US + (_C_MERGE_US if merge else 0.0))
-
-
-def stacking_pays(prefix_len, new_len, shared: int, group: int, start: int = 0) -> bool:
-    """Whether a stacked prefix pass over keys [start, shared) for these requests (one group of
-    consecutive requests; start > 0: a deeper level whose parent covers the keys before it) is
-    estimated to save at least 10% of their extend time over those keys. It pays when stacking
-    fills query tiles that short suffixes leave mostly empty; with long suffixes or many query
-    heads per KV head the tiles are full already and the extra pass only adds CTAs."""
-    ppt = max(128 // group, 1)
-    P = [int(x) for x in prefix_len]
-    S = [int(x) for x in new_len]
-    alone = sum(_extend_cost_us(p, s, start, ppt, start > 0) for p, s in zip(P, S))
-    U = sum(S)
-    if U <= 0:
-        return False
-    stacked_tiles = -(-(shared - start) // 128)
-    first = -(-U // (2 * ppt)) * (stacked_tiles * (_T_TILE_US if U > ppt else _T_TILE_US / 2)
-                                 + _C_CTA_US + (_C_MERGE_US if start > 0 else 0.0))
-    second = sum(_extend_cost_us(p, s, shared, ppt, True) for p, s in zip(P, S))
-    return first + second < 0.9 * alone
-
-
-def prefix_stacking_groups(rows, prefix_len, new_len, min_shared: int):
-    """Host-side grouping for extend: runs of consecutive requests whose slot rows hold the same
-    slots over at least min_shared of their matched prefixes. A run grows while the next
-    request agrees with the run's first over min_shared or more positions; its shared length is
-    the smallest such agreement. Returns (ranges [2 G], shared [G], max_group_rows) -- ranges as
-    (first, end) request pairs, max_group_rows the largest total of new tokens of a group."""
-    rows = np.asarray(rows)
-    P = np.asarray(prefix_len, dtype=np.int64)
-    S = np.asarray(new_len, dtype=np.int64)
-    B = len(P)
-    ranges, shared, max_rows = [], [], 0
-    b = 0
-    while b < B:
-        e, sh = b + 1, int(P[b])
-        while e < B:
-            n = int(min(sh, P[e]))
-            diff = np.flatnonzero(rows[b, :n] != rows[e, :n])
-            agree = int(diff[0]) if diff.size else n
-            if agree < min_shared:
-                break
-            sh = agree
-            e += 1
-        if e - b >= 2 and sh >= min_shared and int(S[b:e].sum()) > 0:
-            ranges += [b, e]
-            shared.append(sh)
-            max_rows = max(max_rows, int(S[b:e].sum()))
-        b = e
-    return np.asarray(ranges, np.int32), np.asarray(shared, np.int32), max_rows
-
-
 MAX_STACK_LEVELS = 4   # RC_MAX_STACK_LEVELS
+_FOLD_MODES = {False: 0, True: 1, "always": 2}   # RC_FOLD_NONE / RC_FOLD_COST / RC_FOLD_ALL
 
 
-FOLD_KEYS = 128   # a folded member's remainder fits one key tile
-
-
-def fold_groups(ranges, shared, level_indptr, prefix_len, new_len):
-    """Groups whose stacked pass can also take their members' remainders (rc_extend_args
-    group_fold): no deeper group lies inside, and every member's keys past the shared prefix
-    (its own cached tokens, then its new tokens) fit one 128-key tile. Returns (fold int32 [G],
-    every request of the batch folded)."""
-    P = np.asarray(prefix_len, dtype=np.int64)
-    S = np.asarray(new_len, dtype=np.int64)
-    G = len(shared)
-    fold = np.zeros(G, np.int32)
-    level = np.zeros(G, np.int64)
-    for l in range(len(level_indptr) - 1):
-        level[level_indptr[l]:level_indptr[l + 1]] = l
-    covered = np.zeros(len(P), bool)
-    for g in range(G):
-        b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
-        inner = any(level[h] > level[g] and b0 <= ranges[2 * h] and ranges[2 * h + 1] <= b1
-                    for h in range(G))
-        if not inner and np.all(P[b0:b1] - int(shared[g]) + S[b0:b1] <= FOLD_KEYS):
-            fold[g] = 1
-            covered[b0:b1] = True
-    return fold, bool(covered.all())
-
-
-def prefix_stacking_levels(rows, prefix_len, new_len, min_shared: int, pays=None,
-                           max_levels: int = MAX_STACK_LEVELS):
-    """Stacking groups over the levels of the tree (cascade): level 0 as prefix_stacking_groups;
-    inside each kept group of level l (shared length s), runs whose members agree over at least
-    s + min_shared positions form level l + 1, with key start s. pays(b0, b1, shared, start)
-    decides whether a candidate is kept (None: all); a group not kept is not searched further.
-    Returns (ranges [2 G], shared [G], start [G], level_indptr [L + 1], max_group_rows) as int32
-    numpy arrays (and an int), groups listed level by level; G = 0 when there is none."""
-    rows = np.asarray(rows)
-    P = np.asarray(prefix_len, dtype=np.int64)
-    S = np.asarray(new_len, dtype=np.int64)
-    parents = [(0, len(P), 0)]
-    ranges, shared, start, level_indptr, max_rows = [], [], [], [0], 0
-    for _ in range(max_levels):
-        found = []
-        for p0, p1, psh in parents:
-            r, sh, _ = prefix_stacking_groups(rows[p0:p1], P[p0:p1], S[p0:p1], psh + min_shared)
-            for g in range(len(sh)):
-                b0, b1 = p0 + int(r[2 * g]), p0 + int(r[2 * g + 1])
-                if pays is None or pays(b0, b1, int(sh[g]), psh):
-                    found.append((b0, b1, int(sh[g]), psh))
-        if not found:
-            break
-        for b0, b1, sh, st in found:
-            ranges += [b0, b1]
-            shared.append(sh)
-            start.append(st)
-            max_rows = max(max_rows, int(S[b0:b1].sum()))
-        level_indptr.append(len(shared))
-        parents = [(b0, b1, sh) for b0, b1, sh, _ in found]
-    return (np.asarray(ranges, np.int32), np.asarray(shared, np.int32),
-            np.asarray(start, np.int32), np.asarray(level_indptr, np.int32), max_rows)
+def plan_extend_stacking(rows, prefix_len, new_len, min_shared: int, group: int,
+                         max_levels: int = MAX_STACK_LEVELS, policy="cost", fold=True):
+    """rc_plan_extend_stacking: the extend batch's stacking groups over the levels of the tree.
+    rows: int32 [B, stride] host slot rows; policy "cost" (groups estimated to pay) or "all";
+    fold True (where estimated to pay), "always" or False. Returns (ranges [2 G], shared [G],
+    start [G], level_indptr [L + 1], max_group_rows, fold [G], all_folded) as int32 numpy arrays
+    (and an int and a bool); G = 0 when there is none."""
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    B = rows.shape[0]
+    P, S = _i32(prefix_len), _i32(new_len)
+    a = RcStackPlanArgs(num_reqs=B, rows=_p(rows), row_stride=rows.shape[1] if rows.ndim == 2 else 0,
+                        prefix_len=_p(P), new_len=_p(S), min_shared=int(min_shared),
+                        group_size=int(group), max_levels=int(max_levels),
+                        policy={"cost": 0, "all": 1}[policy], fold=_FOLD_MODES[fold])
+    cap = max(B * int(max_levels), 1)
+    rng, sh, st, fo = (np.zeros(2 * cap, np.int32), np.zeros(cap, np.int32),
+                       np.zeros(cap, np.int32), np.zeros(cap, np.int32))
+    out = RcStackPlan(capacity=cap, group_range=_p(rng), group_shared=_p(sh), group_start=_p(st),
+                      group_fold=_p(fo))
+    check(lib().rc_plan_extend_stacking(ctypes.byref(a), ctypes.byref(out)),
+          "rc_plan_extend_stacking")
+    G, L = out.num_groups, out.num_levels
+    return (rng[:2 * G].copy(), sh[:G].copy(), st[:G].copy(),
+            np.asarray(out.level_indptr[:L + 1], np.int32), int(out.max_group_rows),
+            fo[:G].copy(), bool(out.all_folded))
 
 
 def shared_context_groups(rows, lengths, group_size: int, min_shared: int):
-    """Host-side grouping for decode: requests whose slot rows start with the same slots share
-    that prefix's KV. rows: int32 [B, >= max(lengths)] slot rows, lengths: context tokens per
-    request. Greedy: the first request of each same-first-slot bucket leads; the others with the
-    longest common slot prefix join it, up to group_size members, as long as that prefix is at
-    least min_shared tokens; a group's shared length is its members' smallest common prefix.
-    Returns (indptr, members, shared) int32 numpy arrays (no groups: three empty arrays)."""
-    rows = np.asarray(rows)
-    lengths = np.asarray(lengths, dtype=np.int64)
-    B = len(lengths)
-    indptr, members, shared = [0], [], []
-    if group_size < 2 or B < 2:
-        return (np.zeros(1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.int32))
-    eligible = np.flatnonzero(lengths >= max(min_shared, 1))
-    buckets = {}
-    for b in eligible:
-        buckets.setdefault(int(rows[b, 0]), []).append(int(b))
-
-    def lcp(x, y):
-        n = int(min(lengths[x], lengths[y]))
-        diff = np.flatnonzero(rows[x, :n] != rows[y, :n])
-        return int(diff[0]) if diff.size else n
-
-    for rest in buckets.values():
-        while len(rest) >= 2:
-            lead = rest[0]
-            cand = sorted(((lcp(lead, m), m) for m in rest[1:]), reverse=True)
-            take = [(l, m) for l, m in cand[:group_size - 1] if l >= min_shared]
-            if not take:
-                rest = rest[1:]
-                continue
-            members += [lead] + [m for _, m in take]
-            shared.append(min(l for l, _ in take))
-            indptr.append(len(members))
-            used = {lead} | {m for _, m in take}
-            rest = [m for m in rest if m not in used]
-    return (np.asarray(indptr, np.int32), np.asarray(members, np.int32),
-            np.asarray(shared, np.int32))
+    """rc_plan_decode_groups: decode requests whose slot rows start with the same slots share
+    that prefix's KV. rows: int32 [B, >= max(lengths)] host slot rows, lengths: context tokens
+    per request. Returns (indptr, members, shared) int32 numpy arrays (no groups: [0] and two
+    empty arrays)."""
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    L = np.ascontiguousarray(lengths, dtype=np.int64)
+    B = len(L)
+    indptr = np.zeros(B + 1, np.int32)
+    members = np.zeros(max(B, 1), np.int32)
+    shared = np.zeros(max(B, 1), np.int32)
+    ng = ctypes.c_int32()
+    check(lib().rc_plan_decode_groups(_p(rows), rows.shape[1] if rows.ndim == 2 else 0, _p(L),
+                                      B, int(group_size), int(min_shared), _p(indptr),
+                                      _p(members), _p(shared), ctypes.byref(ng)),
+          "rc_plan_decode_groups")
+    G = ng.value
+    return indptr[:G + 1].copy(), members[:indptr[G]].copy(), shared[:G].copy()
 
 
 STATIC_SCRATCH_BYTES = 32 << 20

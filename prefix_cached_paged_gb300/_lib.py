@@ -16,6 +16,12 @@ RC_DTYPE_BF16 = 0
 RC_DTYPE_F32 = 1
 RC_SCHED_LSPF = 0
 RC_SCHED_FCFS = 1
+RC_STACK_COST = 0
+RC_STACK_ALL = 1
+RC_FOLD_NONE = 0
+RC_FOLD_COST = 1
+RC_FOLD_ALL = 2
+RC_MAX_STACK_LEVELS = 4
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -64,6 +70,9 @@ SIGNATURES = {
     "rc_decode_attention_noalloc": (ctypes.c_int, [_P, _P]),
     "rc_device_status": (ctypes.c_int, [ctypes.POINTER(_I32), _P]),
     "rc_debug_set_wait_limit_ns": (ctypes.c_int, [_U64]),
+    "rc_plan_extend_stacking": (ctypes.c_int, [_P, _P]),
+    "rc_plan_decode_groups": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _I64, _P, _P, _P,
+                                             ctypes.POINTER(_I32)]),
 }
 
 
@@ -85,6 +94,19 @@ class RcSlotWriteArgs(ctypes.Structure):
     _fields_ = [("num_segments", _I32), ("max_reqs", _I32), ("max_ctx", _I32),
                 ("total_values", _I64), ("seg_row", _P), ("seg_col", _P), ("seg_indptr", _P),
                 ("values", _P), ("req_to_token", _P)]
+
+
+class RcStackPlanArgs(ctypes.Structure):
+    _fields_ = [("num_reqs", _I32), ("rows", _P), ("row_stride", _I64), ("prefix_len", _P),
+                ("new_len", _P), ("min_shared", _I32), ("group_size", _I32),
+                ("max_levels", _I32), ("policy", _I32), ("fold", _I32)]
+
+
+class RcStackPlan(ctypes.Structure):
+    _fields_ = [("capacity", _I32), ("group_range", _P), ("group_shared", _P),
+                ("group_start", _P), ("group_fold", _P),
+                ("level_indptr", _I32 * (RC_MAX_STACK_LEVELS + 1)), ("num_groups", _I32),
+                ("num_levels", _I32), ("max_group_rows", _I32), ("all_folded", _I32)]
 
 
 class RcExtendArgs(ctypes.Structure):

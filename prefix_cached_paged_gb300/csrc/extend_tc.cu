@@ -69,6 +69,8 @@ template <bool kStack> struct Regs {
                 "a register split above the launch allocation never completes");
 };
 constexpr float kRescaleThreshold = 8.0f; // log2 units: rescale O only if the max grows by 2^8
+constexpr int kFoldTiles = 512;           // remainder tiles of one CTA of a folded pass, at most
+constexpr int kFoldMembers = 256;         // members of one CTA of a folded pass, at most
 
 struct SmemLayout {
   static constexpr int Q = 0;                                   // Q_A, Q_B
@@ -81,7 +83,11 @@ struct SmemLayout {
   static constexpr int MMA_DONE = TMEM_SLOT + 8;     // set once the MMA warp syncs no more
   // split-mode merge: row maxima, rounded and exact sums of each virtual tile [X][row]
   static constexpr int XMRG = TMEM_SLOT + 16;
-  static constexpr int TOTAL = XMRG + 3 * 2 * 128 * 4;
+  // folded stacked pass: remainder tile u -> (member offset << 16 | tile of member), and the
+  // first remainder tile of each member of the CTA
+  static constexpr int FMAP = XMRG + 3 * 2 * 128 * 4;
+  static constexpr int FU0 = FMAP + 4 * 512;
+  static constexpr int TOTAL = FU0 + 4 * 260;
   static constexpr int ALLOC = TOTAL + 1024;  // room to align the base to 1024 bytes
 };
 static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
@@ -123,6 +129,16 @@ __device__ __forceinline__ int request_of_pos(const rc_extend_args& a, int b0, i
     else hi = mid - 1;
   }
   return lo;
+}
+
+// Folded stacked pass: member r of the group (new tokens at stacked positions [st, en) from
+// the group's first) has priv = prefix_len[r] - P cached keys past the shared prefix P, then
+// its new tokens. Its remainder keys in the CTA, in 128-key tiles: up to the key its last row
+// before stacked position `end` sees.
+__device__ __forceinline__ int fold_tiles(const rc_extend_args& a, int r, int qo, int P, int end) {
+  const int st = a.qo_indptr[r] - qo, en = a.qo_indptr[r + 1] - qo;
+  const int last = min(en, end) - 1 - st;   // member-relative index of its last row here
+  return last < 0 ? 0 : (a.prefix_len[r] - P + last + 1 + kN - 1) / kN;
 }
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -385,10 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // members, stacked in batch order, against keys [0, shared) only.
   const bool stacked = kStack && p.pass == 1;
   int b, qo, S, P, row, kstart = 0;
-  // folded stacked pass: the CTA also takes each of its members' remainders (one key tile per
-  // member, members r_first .. r_first + n_rem - 1 of the group [gb0, gb1)) and is final
+  // folded stacked pass: the CTA also takes each of its members' remainders -- a run of key
+  // tiles per member, members r_first, r_first + 1, ... of the group [gb0, gb1) in order, n_rem
+  // tiles in all, of which query tile A needs the first n_rem_a -- and is final
   bool fold = false;
-  int gb0 = 0, gb1 = 0, r_first = 0, n_rem = 0, n_rem_a = 0;
+  int gb0 = 0, gb1 = 0, r_first = 0, r_last = 0, n_rem = 0, n_rem_a = 0;
   if (stacked) {
     const int g = p.group_lo + blockIdx.z;
     const int b0 = a.group_range[2 * g], b1 = a.group_range[2 * g + 1];
@@ -407,19 +424,30 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     if (threadIdx.x == 0 && blockIdx.x == 0 && hk == 0) {
       for (int bb = b0; bb < b1; ++bb) {  // every member matched the shared prefix
         if (a.prefix_len[bb] < P) set_status(p.status, kStatusPosRange);
-        // a folded member's remainder fits one key tile
-        if (fold && a.prefix_len[bb] - P + (a.qo_indptr[bb + 1] - a.qo_indptr[bb]) > kN)
-          set_status(p.status, kStatusPosRange);
       }
     }
     if (S <= 0 || iA >= S) return;
     // a deeper level covers only the keys after its parent's shared prefix
     kstart = a.group_start ? a.group_start[g] : 0;
     if (fold) {
+      const int endA = min(iA + p.ppt, S), endC = min(iA + 2 * p.ppt, S);
       r_first = request_of_pos(a, b0, b1, qo, iA);
-      n_rem = request_of_pos(a, b0, b1, qo, min(iA + 2 * p.ppt, S) - 1) - r_first + 1;
-      // query tile A needs the remainder tiles of its own members only, which come first
-      n_rem_a = request_of_pos(a, b0, b1, qo, min(iA + p.ppt, S) - 1) - r_first + 1;
+      const int r_lastA = request_of_pos(a, b0, b1, qo, endA - 1);
+      r_last = request_of_pos(a, b0, b1, qo, endC - 1);
+      // query tile A needs the remainder tiles of its own members only, which come first (of
+      // its last member, those up to its last row in A)
+      for (int r = r_first; r <= r_last; ++r) {
+        const int nt = fold_tiles(a, r, qo, P, endC);
+        n_rem += nt;
+        if (r < r_lastA) n_rem_a += nt;
+        else if (r == r_lastA) n_rem_a += fold_tiles(a, r, qo, P, endA);
+      }
+      // the CTA's remainder-tile map must fit its shared-memory table (the host folds only
+      // groups whose CTAs do)
+      if (n_rem > kFoldTiles || r_last - r_first + 1 > kFoldMembers) {
+        if (threadIdx.x == 0) set_status(p.status, kStatusPosRange);
+        return;
+      }
     }
     if (P < 1 || P > a.prefix_len[b0] || P > a.max_ctx || row < 0 || row >= a.max_reqs ||
         qo < 0 || (int64_t)qo + S > a.num_tokens || kstart < 0 || kstart >= P) {
@@ -551,17 +579,26 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   const uint32_t sbuf = (is_v ? sV : sK) + (uint32_t)(w * kRowsPerWarp * 128);
   // raw(j, q) only issues the slot load; rowptr() checks it when the tile is issued, so the
   // loads of tile j+1 stay in flight while tile j is being copied
-  // folded remainder tile j >= n_pre: member r_first + j - n_pre; its key k is its own cached
-  // token P + k while k < priv (= its prefix past the shared P), then its new token k - priv
-  auto fold_req = [&](int j) { return min(r_first + (j - n_pre), gb1 - 1); };
+  // folded remainder tile j >= n_pre: tile qt of member r (the CTA's map, filled before the
+  // set-up barrier); the member's key k = 128 qt + row is its own cached token P + k while
+  // k < priv (= its prefix past the shared P), then its new token k - priv
+  const int endC = min(iA + 2 * p.ppt, S);
+  const uint32_t* fmap = (const uint32_t*)(smem + SmemLayout::FMAP);
+  const int* fu0 = (const int*)(smem + SmemLayout::FU0);
+  auto fold_tile = [&](int j, int& qt) -> int {
+    const uint32_t e = fmap[min(max(j - n_pre, 0), kFoldTiles - 1)];
+    qt = (int)(e & 0xFFFFu);
+    return min(r_first + (int)(e >> 16), gb1 - 1);
+  };
   auto raw = [&](int j, int q) -> int {
     if (j < n_pre) {
       const int key = kstart + j * kN + w * kRowsPerWarp + q * 32 + lane;
       return rt[key < P ? key : P - 1];
     }
     if (fold) {
-      const int r = fold_req(j);
-      const int k = w * kRowsPerWarp + q * 32 + lane;
+      int qt;
+      const int r = fold_tile(j, qt);
+      const int k = qt * kN + w * kRowsPerWarp + q * 32 + lane;
       const int rr = a.req_idx[r];
       if (k < a.prefix_len[r] - P && rr >= 0 && rr < a.max_reqs && P + k < a.max_ctx)
         return a.req_to_token[(int64_t)rr * a.max_ctx + P + k];
@@ -571,8 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   };
   auto rowptr = [&](int j, int q, int rv) -> const __nv_bfloat16* {
     if (fold && j >= n_pre) {
-      const int r = fold_req(j);
-      const int k = w * kRowsPerWarp + q * 32 + lane;
+      int qt;
+      const int r = fold_tile(j, qt);
+      const int k = qt * kN + w * kRowsPerWarp + q * 32 + lane;
       const int priv = a.prefix_len[r] - P;
       if (k < priv) {
         int sl = rv;
@@ -636,6 +674,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         bytes = 16;
       }
       cp_async16_zfill(sQ0 + X * kTileBytes + sw128_off(m, c), src, bytes);
+    }
+  }
+  // the folded pass's remainder-tile map: one thread walks the CTA's members (its loads overlap
+  // the other threads' first copies)
+  if (fold && threadIdx.x == kThreads - 1) {
+    uint32_t* map = (uint32_t*)(smem + SmemLayout::FMAP);
+    int* u0 = (int*)(smem + SmemLayout::FU0);
+    int u = 0;
+    for (int r = r_first; r <= r_last; ++r) {
+      u0[r - r_first] = u;
+      const int nt = fold_tiles(a, r, qo, P, endC);
+      for (int qt = 0; qt < nt; ++qt) map[u++] = ((uint32_t)(r - r_first) << 16) | (uint32_t)qt;
     }
   }
   tc_fence_before();
@@ -794,12 +844,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
     // a warp with no row of the tile only paces the weights hand-off
     const bool warp_idle = !__any_sync(0xffffffffu, row_valid);
     const int ipos = min(iX + max(mrow, 0) / G, S - 1);  // this row's new-token index (clamped)
-    // folded stacked pass: the member this row belongs to and its index among that member's
-    // new tokens (the member's remainder tile is visible to it up to its own position)
-    int req_row = -1, i_row = 0;
+    // folded stacked pass: the member this row belongs to, its index among that member's new
+    // tokens, the remainder keys it sees (its member's cached keys past P, then its new tokens up
+    // to its own), and where its member's remainder tiles start in the CTA's list (u0_row)
+    int req_row = -1, row_keys = 0, u0_row = 0;
     if (fold) {
       req_row = request_of_pos(a, gb0, gb1, qo, ipos);
-      i_row = ipos - (a.qo_indptr[req_row] - qo);
+      row_keys = a.prefix_len[req_row] - P + ipos - (a.qo_indptr[req_row] - qo) + 1;
+      u0_row = fu0[min(max(req_row - r_first, 0), kFoldMembers - 1)];
     }
     const float sc2 = p.scale2;
     const uint64_t sc2x2 = f2pack(sc2, sc2);
@@ -825,8 +877,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       if (kt < n_pre) {
         lim = min(kN, P - kstart - kt * kN);
       } else if (fold) {
-        const int rk = min(r_first + (kt - n_pre), gb1 - 1);
-        lim = rk == req_row ? min(kN, a.prefix_len[rk] - P + i_row + 1) : 0;
+        // remainder tiles of other members are invisible to this row
+        const int qt = kt - n_pre - u0_row;
+        lim = qt < 0 ? 0 : min(kN, row_keys - qt * kN);
       } else {
         lim = min(kN, ipos - (kt - n_pre) * kN + 1);
       }

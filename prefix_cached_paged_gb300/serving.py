@@ -23,8 +23,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import (DEFAULT_KV_CHUNK, decode_attention, decode_workspace_bytes, extend_attention,
-               extend_workspace_bytes, fold_groups, kv_copy, prefix_stacking_levels,
-               shared_context_groups, stacking_pays, MAX_STACK_LEVELS)
+               extend_workspace_bytes, kv_copy, plan_extend_stacking, shared_context_groups,
+               MAX_STACK_LEVELS)
 from .runtime import DeviceKV, HostCache, Plan
 
 
@@ -99,7 +99,8 @@ class Engine:
         # that is estimated to pay (True), for every group found ("always"), or never (False)
         self.stack_extend = stack_extend
         self.stack_levels = stack_levels   # tree levels stacked (1: the shallowest group only)
-        # a stacked group whose members' remainders fit one key tile takes them in its own pass
+        # an innermost stacked group takes its members' remainders in its own pass where that is
+        # estimated to pay (True), always ("always"), or never (False)
         self.fold_extend = fold_extend
         self._ext_ws = None
         self._free_rows = list(range(max_reqs - 1, -1, -1))
@@ -155,15 +156,11 @@ class Engine:
         if self.stack_extend and B > 1:
             # stacking groups over the levels of the tree, each kept where it is estimated to pay
             G = self.n_q_heads // self.n_kv_heads
-            plen = plan.prefix_len
-            pays = None if self.stack_extend == "always" else (
-                lambda b0, b1, sh, st: stacking_pays(plen[b0:b1], S[b0:b1], sh, G, st))
-            ranges, shared, start, level_indptr, max_rows = prefix_stacking_levels(
-                plan.rows, plen, S, STACK_MIN_SHARED, pays, self.stack_levels)
+            ranges, shared, start, level_indptr, max_rows, fold, all_folded = plan_extend_stacking(
+                plan.rows, plan.prefix_len, S, STACK_MIN_SHARED, G, self.stack_levels,
+                policy="all" if self.stack_extend == "always" else "cost",
+                fold=self.fold_extend)
             if len(shared):
-                fold, all_folded = (fold_groups(ranges, shared, level_indptr, plen, S)
-                                    if self.fold_extend else (np.zeros(len(shared), np.int32),
-                                                              False))
                 r, sh, st, fo = self.dev.upload_i32([ranges, shared, start, fold])
                 batch.stack = (r, sh, max_rows, st, level_indptr, fo, all_folded)
                 need = extend_workspace_bytes(plan.num_tokens, self.n_q_heads)

@@ -635,26 +635,32 @@ def test_decode_plan_reuse_across_layers(groups):
 
 _FOLD_SPEC = [(600, [(20, 30), (50, 60), (0, 128), (100, 1)]),   # private cached keys, a full tile
               (300, [(0, 5)] * 7),                                # few-shot like
-              (900, [(10, 100), (0, 200)])]                       # too long to fold
+              (900, [(10, 100), (0, 200)]),                       # remainders of 1 and 2 tiles
+              (400, [(0, 200)] * 5),                              # forks: 1000 stacked rows
+              (260, [(140, 190), (3, 260)])]                      # 3 remainder tiles
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 2), (16, 8)])
 def test_extend_fold(Hq, Hkv):
     """Folded stacked passes (each member's remainder -- its own cached tokens past the shared
-    prefix, then its new tokens -- in the group's pass, final outputs written there) next to an
-    unfolded group in the same batch: every unit within tolerance of the oracle, the new K/V
-    scattered bit-exactly, the same without stacking."""
+    prefix, then its new tokens, in as many key tiles as it takes -- in the group's pass, final
+    outputs written there): all groups folded, the cost model's choice (folded and unfolded
+    groups side by side), and none folded; every unit within tolerance of the oracle, the new
+    K/V scattered bit-exactly."""
     m = W.Model(1, Hq, Hkv, 128, "bf16", 13)
     cache, ext = _stack_families(13, _FOLD_SPEC)
     w = W.Workload("ext_fold", m, 40_000, synth.permutation(13, 40_000), max_ctx=1216)
-    for fold in (True, False):
+    for fold in ("always", True, False):
         eng = H.make_engine(w, max_reqs=64, stack_extend="always", fold_extend=fold)
         for c in cache:
             H.run_cache_phase(eng, m, [c])
         b, outs = H.run_extend_phase(eng, m, ext, lse=True)
         assert b.stack is not None
-        assert b.stack[5].cpu().tolist() == ([1, 1, 0] if fold else [0, 0, 0])
-        assert not b.stack[6]
+        flags = b.stack[5].cpu().tolist()
+        if fold == "always":
+            assert flags == [1] * len(_FOLD_SPEC) and b.stack[6]
+        elif not fold:
+            assert flags == [0] * len(_FOLD_SPEC) and not b.stack[6]
         _status_clear()
         units = [(i, 0, h) for i in range(len(ext)) for h in range(Hkv)]
         _check_extend(w, b, outs, ext, units)

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import prefix_cached_paged_gb300 as rc
+from tests import planner_ref
 from prefix_cached_paged_gb300 import runtime
 from prefix_cached_paged_gb300._lib import SIGNATURES, lib
 from synth import workloads as W
@@ -373,7 +374,7 @@ def test_prefix_stacking_groups_are_valid(seed):
     """Ranges ascending and disjoint, at least two requests each, rows identical over the shared
     length, which is at least min_shared, within every member's prefix, and the smallest
     agreement with the run's first request; max_group_rows bounds each group's new tokens."""
-    from prefix_cached_paged_gb300 import prefix_stacking_groups
+    from tests.planner_ref import prefix_stacking_groups
     rng = np.random.default_rng(100 + seed)
     B, W_ = 30, 400
     rows = rng.integers(0, 10_000, (B, W_)).astype(np.int32)
@@ -406,10 +407,12 @@ def test_prefix_stacking_groups_are_valid(seed):
 
 
 def test_stacking_policy_on_the_measured_workloads():
-    """The calibrated cost model stacks the few-shot batch (50-token suffixes over 2000 shared
-    tokens, MHA) and leaves the fork step (200-token suffixes) and the two-level GQA batch alone,
-    as their measurements with stacking forced on showed."""
-    from prefix_cached_paged_gb300 import stacking_pays
+    """The calibrated cost model makes the choices the kernel replays measured best on GB300:
+    it stacks the few-shot batch (50-token suffixes over 2000 shared tokens, MHA; folded 586 vs
+    368 TFLOP/s unstacked) and leaves each program of the fork step (5 x 200-token suffixes over
+    1500 shared tokens; unstacked 813 vs 709 folded) and the two-level GQA batch (unstacked 636
+    vs 603 folded) alone."""
+    from tests.planner_ref import stacking_pays
     assert stacking_pays([2000] * 64, [50] * 64, 2000, 1)
     assert not stacking_pays([1500] * 5, [200] * 5, 1500, 1)
     v = np.random.default_rng(0).integers(1, 99, 64)
@@ -649,7 +652,8 @@ def test_prefix_stacking_levels_are_valid(seed):
         rows[b, cut:] = [rnd.randrange(1000, 2000) for _ in range(width - cut)]
     P = np.full(B, width, np.int64)
     S = np.array([rnd.randint(0, 30) for _ in range(B)], np.int64)
-    ranges, shared, start, lvl, max_rows = rc.prefix_stacking_levels(rows, P, S, min_shared)
+    ranges, shared, start, lvl, max_rows = planner_ref.prefix_stacking_levels(rows, P, S,
+                                                                              min_shared)
     assert lvl[0] == 0 and lvl[-1] == len(shared) and np.all(np.diff(lvl) > 0)
     spans = {}
     for l in range(len(lvl) - 1):
@@ -719,9 +723,10 @@ def test_new_entry_points_reject_bad_arguments():
 
 @pytest.mark.parametrize("seed", range(8))
 def test_fold_groups_follow_their_rule(seed):
-    """fold_groups marks exactly the groups that no deeper group lies inside and whose every
-    member's remainder (cached tokens past the shared prefix + new tokens) fits one key tile;
-    all_folded is whether every request is in such a group."""
+    """fold_groups marks exactly the groups that no deeper group lies inside and whose folded
+    pass the cost model puts at no more than the stacked pass plus the members' own passes
+    (every innermost group with force); all_folded is whether every request is in such a
+    group."""
     rnd = random.Random(600 + seed)
     B, width = rnd.randint(2, 20), 400
     rows = np.zeros((B, width), np.int32)
@@ -732,20 +737,26 @@ def test_fold_groups_follow_their_rule(seed):
         rows[b, cut:] = [rnd.randrange(1000, 2000) for _ in range(width - cut)]
     P = np.array([rnd.randint(260, width) for _ in range(B)], np.int64)
     S = np.array([rnd.randint(1, 150) for _ in range(B)], np.int64)
-    ranges, shared, start, lvl, _ = rc.prefix_stacking_levels(rows, P, S, 8)
-    fold, all_folded = rc.fold_groups(ranges, shared, lvl, P, S)
-    G = len(shared)
-    level = np.repeat(np.arange(len(lvl) - 1), np.diff(lvl))
-    covered = np.zeros(B, bool)
-    for g in range(G):
-        b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
-        leaf = not any(level[h] > level[g] and b0 <= ranges[2 * h] and ranges[2 * h + 1] <= b1
-                       for h in range(G))
-        fits = all(P[b] - shared[g] + S[b] <= rc.FOLD_KEYS for b in range(b0, b1))
-        assert bool(fold[g]) == (leaf and fits), g
-        if fold[g]:
-            covered[b0:b1] = True
-    assert all_folded == bool(covered.all())
+    grp = rnd.choice([1, 4, 8])
+    ranges, shared, start, lvl, _ = planner_ref.prefix_stacking_levels(rows, P, S, 8)
+    for force in (False, True):
+        fold, all_folded = planner_ref.fold_groups(ranges, shared, lvl, P, S, grp, start,
+                                                   force=force)
+        G = len(shared)
+        level = np.repeat(np.arange(len(lvl) - 1), np.diff(lvl))
+        covered = np.zeros(B, bool)
+        for g in range(G):
+            b0, b1 = int(ranges[2 * g]), int(ranges[2 * g + 1])
+            leaf = not any(level[h] > level[g] and b0 <= ranges[2 * h] and ranges[2 * h + 1] <= b1
+                           for h in range(G))
+            _, unfolded, folded = planner_ref._stacking_costs(P[b0:b1], S[b0:b1], int(shared[g]),
+                                                              grp, int(start[g]))
+            fits = planner_ref._folded_cost_us(P[b0:b1], S[b0:b1], int(shared[g]),
+                                               int(start[g]), max(128 // grp, 1), limits=True)
+            assert bool(fold[g]) == (leaf and fits and (force or folded <= unfolded)), g
+            if fold[g]:
+                covered[b0:b1] = True
+        assert all_folded == bool(covered.all())
 
 
 @pytest.mark.parametrize("shared", [True, False])
@@ -793,3 +804,140 @@ def test_schedule_ranges_rejects_bad_arguments():
         t.schedule_batch_ranges(tok, np.array([0]), np.array([3]), None, policy=9)
     order, match, adm = t.schedule_batch_ranges(tok, np.zeros(0), np.zeros(0))
     assert (len(order), adm) == (0, 0)
+
+
+def _random_stacking_case(rnd):
+    """Families of consecutive requests sharing slot prefixes of random lengths (some nested),
+    random private parts and new-token counts."""
+    B, width = rnd.randint(2, 24), 700
+    rows = np.zeros((B, width), np.int32)
+    P = np.zeros(B, np.int64)
+    S = np.zeros(B, np.int64)
+    b = 0
+    fresh = iter(range(10_000, 10_000_000))
+    while b < B:
+        n = min(rnd.randint(1, 7), B - b)
+        base = [next(fresh) for _ in range(width)]
+        sub = rnd.choice([0, 0, rnd.randint(1, 600)])
+        for i in range(n):
+            row = list(base)
+            cut = rnd.choice([rnd.randint(0, 80), rnd.randint(200, 690)])
+            if sub and i % 2:
+                cut = max(cut, sub)
+            for c in range(cut, width):
+                row[c] = next(fresh)
+            rows[b + i] = row
+            P[b + i] = rnd.randint(min(cut + 1, width - 1) if rnd.random() < 0.5 else 0, width - 1)
+            S[b + i] = rnd.choice([0, 1, rnd.randint(1, 60), rnd.randint(60, 400)])
+        b += n
+    return rows, P, S
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_stacking_planner_matches_reference(seed):
+    """rc_plan_extend_stacking makes exactly the reference planner's decisions (groups, levels,
+    shared lengths, key starts, folds, max rows, all folded) on random batches, for every policy,
+    fold mode, group size and depth."""
+    rnd = random.Random(900 + seed)
+    rows, P, S = _random_stacking_case(rnd)
+    for grp in (1, 8):
+        for policy in ("cost", "all"):
+            for fold in (False, True, "always"):
+                levels = rnd.randint(1, 4)
+                got = rc.plan_extend_stacking(rows, P, S, 256, grp, levels, policy, fold)
+                pays = None if policy == "all" else (
+                    lambda b0, b1, sh, st: planner_ref.stacking_pays(P[b0:b1], S[b0:b1], sh, grp,
+                                                                     st))
+                ranges, shared, start, lvl, max_rows = planner_ref.prefix_stacking_levels(
+                    rows, P, S, 256, pays, levels)
+                if len(shared) and fold:
+                    fo, allf = planner_ref.fold_groups(ranges, shared, lvl, P, S, grp, start,
+                                                       force=fold == "always")
+                else:
+                    fo, allf = np.zeros(len(shared), np.int32), False
+                assert got[0].tolist() == ranges.tolist()
+                assert got[1].tolist() == shared.tolist()
+                assert got[2].tolist() == start.tolist()
+                assert got[3].tolist() == lvl.tolist()
+                assert got[4] == max_rows
+                assert got[5].tolist() == fo.tolist()
+                assert got[6] == (bool(allf) and len(shared) > 0)
+
+
+@pytest.mark.parametrize("name", ["few_shot_extend", "two_level_extend", "fork_extend"])
+def test_stacking_planner_on_the_target_batches(name):
+    """The C planner and the reference agree on the target workloads' extend batches (host
+    plans built through the product's tree): few-shot, two-level tree, and one step of the fork
+    mixed step."""
+    from synth import workloads as W
+    if name == "fork_extend":
+        fm = W.fork_mixed_step(layers=1)
+        w = fm.workload
+        cache, ext = fm.programs, fm.extend_seqs(0)
+    else:
+        w = W.CONFIGS[name]()
+        cache = [s for ph in w.phases[:-1] for s in ph.seqs]
+        ext = w.phases[-1].seqs
+    hc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order)
+    for s in cache:
+        p = hc.plan([s], match_all=True)
+        hc.finish(p)
+    plan = hc.plan(ext)
+    S = plan.lengths - plan.prefix_len
+    G = w.model.n_q_heads // w.model.n_kv_heads
+    got = rc.plan_extend_stacking(plan.rows, plan.prefix_len, S, 256, G, 4, "cost", True)
+    pays = lambda b0, b1, sh, st: planner_ref.stacking_pays(plan.prefix_len[b0:b1], S[b0:b1], sh,
+                                                            G, st)
+    ranges, shared, start, lvl, max_rows = planner_ref.prefix_stacking_levels(
+        plan.rows, plan.prefix_len, S, 256, pays, 4)
+    assert got[0].tolist() == ranges.tolist() and got[1].tolist() == shared.tolist()
+    assert got[2].tolist() == start.tolist() and got[3].tolist() == lvl.tolist()
+    assert got[4] == max_rows
+    if len(shared):
+        fo, allf = planner_ref.fold_groups(ranges, shared, lvl, plan.prefix_len, S, G, start)
+        assert got[5].tolist() == fo.tolist() and got[6] == allf
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_decode_planner_matches_reference(seed):
+    """rc_plan_decode_groups forms exactly the reference's shared-context groups on random slot
+    rows (buckets by first slot, ties, caps, short contexts)."""
+    rnd = random.Random(1300 + seed)
+    B, width = rnd.randint(0, 40), 300
+    rows = np.zeros((B, width), np.int32)
+    lengths = np.zeros(B, np.int64)
+    bases = [[rnd.randrange(5) * 1000 + c for c in range(width)] for _ in range(4)]
+    for b in range(B):
+        rows[b] = bases[rnd.randrange(4)]
+        cut = rnd.choice([0, rnd.randint(1, 100), rnd.randint(100, 299)])
+        rows[b, cut:] = [rnd.randrange(10**6, 10**7) for _ in range(width - cut)]
+        lengths[b] = rnd.randint(0, width)
+    for cap in (1, 2, 4, 8):
+        for min_shared in (1, 32, 128):
+            got = rc.shared_context_groups(rows, lengths, cap, min_shared)
+            ref = planner_ref.shared_context_groups(rows, lengths, cap, min_shared)
+            for x, y in zip(got, ref):
+                assert x.tolist() == y.tolist(), (cap, min_shared)
+
+
+def test_decode_planner_on_the_target_batches():
+    """Both decode planners agree on the multi-turn decode contexts and the fork step's decode
+    requests."""
+    from synth import workloads as W
+    for w, ctx in ((W.multi_turn_decode(), None), (W.fork_mixed_step(layers=1).workload, "fork")):
+        hc = runtime.HostCache(w.pool_slots, w.max_ctx, w.pool_order)
+        for ph in w.phases[:-1] if ctx is None else w.phases:
+            for s in ph.seqs:
+                p = hc.plan([s], match_all=True)
+                hc.finish(p)
+        if ctx is None:
+            seqs = [s[:-1] for s in w.phases[-1].seqs]
+        else:
+            seqs = [s[:-1] for s in W.fork_mixed_step(layers=1).decode_seqs]
+        plan = hc.plan(seqs, match_all=True)
+        G = w.model.n_q_heads // w.model.n_kv_heads
+        got = rc.shared_context_groups(plan.rows, plan.lengths, 8 // G, 512)
+        ref = planner_ref.shared_context_groups(plan.rows, plan.lengths, 8 // G, 512)
+        assert got[1].size > 0
+        for x, y in zip(got, ref):
+            assert x.tolist() == y.tolist()
