@@ -429,10 +429,11 @@ def bench_ours(args, rank, world, local):
                                    for l in range(m.layers)), world)
         e_dec = max_over_ranks(sum(e[l][1].elapsed_time(e[l][2]) for e in eevs
                                    for l in range(m.layers)), world)
+        link = host_link(hb["xq"])
         e2e = {"value": round(world * ef / (e_ext * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "decode_gbs": round(world * dbb / (e_dec * 1e-3) / 1e9, 1),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": ne,
+               "steps": ne, "host_link": link,
                "note": "every layer's q/k_new/v_new (extend and decode) copied in from pinned "
                        "host memory and its outputs copied back, overlapped with the kernels "
                        "(two copy streams, double buffers); phases timed on the compute stream "
@@ -508,6 +509,42 @@ def bench_ours(args, rank, world, local):
     return out
 
 
+def host_link(pinned):
+    """The host link the end-to-end leg goes through: NUMA nodes of the host, the GPU's node, and
+    the copy rate of one contiguous pinned buffer (the e2e leg's own) each way."""
+    import torch
+    nodes = sorted(int(d[4:]) for d in os.listdir("/sys/devices/system/node")
+                   if d.startswith("node") and d[4:].isdigit()) \
+        if os.path.isdir("/sys/devices/system/node") else []
+    gpu_node = None
+    try:
+        bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              f"--id={torch.cuda.current_device()}"], capture_output=True,
+                             text=True, timeout=20).stdout.strip().lower()
+        path = f"/sys/bus/pci/devices/{bus[4:] if len(bus.split(':')[0]) == 8 else bus}/numa_node"
+        gpu_node = int(open(path).read().strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    flat = pinned.view(-1)
+    dev = torch.empty_like(flat, device="cuda")
+    rates = {}
+    for name, (dst, src) in (("h2d_gbs", (dev, flat)), ("d2h_gbs", (flat, dev))):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(5):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        rates[name] = round(5 * flat.numel() * flat.element_size() / (e0.elapsed_time(e1) * 1e-3)
+                            / 1e9, 1)
+    del dev
+    return {"numa_nodes": nodes, "gpu_numa_node": gpu_node, **rates,
+            "bytes": int(flat.numel() * flat.element_size())}
+
+
 def cpu_baseline(ctx, args, budget_s=None):
     """The oracle, as it stands, on a bounded sample of the step's extend units (fp64 attention
     of (request, layer, head) units on all host cores). Returns the metric in TFLOP/s."""
@@ -519,8 +556,9 @@ def cpu_baseline(ctx, args, budget_s=None):
     threads = os.cpu_count() or 1
     rng = np.random.default_rng(7)
     units, flops = [], 0.0
-    # one unit: a request's 200 queries of one head over 1700 keys
-    n_units = threads * 2
+    # one unit: a request's 200 queries of one head over 1700 keys; passes over the sample repeat
+    # until the budget (10-30 s of CPU work by default) is spent
+    n_units = threads * 8
     for _ in range(n_units):
         b, layer, h = (int(rng.integers(len(seqs))), int(rng.integers(m.layers)),
                        int(rng.integers(m.n_kv_heads)))
@@ -536,7 +574,7 @@ def cpu_baseline(ctx, args, budget_s=None):
     oracle.attention_units(units, m.sm_scale, 1, 1, threads)
     dt = time.perf_counter() - t0
     reps = 1
-    while dt * (reps + 1) / reps < budget_s and reps < 8:
+    while dt * (reps + 1) / reps < budget_s and reps < 256:
         t1 = time.perf_counter()
         oracle.attention_units(units, m.sm_scale, 1, 1, threads)
         dt += time.perf_counter() - t1
