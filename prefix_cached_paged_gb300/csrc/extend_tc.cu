@@ -171,6 +171,11 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// s0 += low bf16 of x, s1 += high bf16 of x (each widened exactly, one rounding in the add)
+__device__ __forceinline__ void add_bf16x2(float& s0, float& s1, uint32_t x) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}" : "+f"(s0), "+f"(s1) : "r"(x));
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -945,15 +950,14 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       named_bar_arrive(kHandoffBar0 + X, kHandoffThreads);
       // The rounded sum is not needed for the hand-off: it runs while the tensor core does P.V.
       // O is normalised by the sum of the rounded weights P.V uses; the log-sum-exp output
-      // uses the exact sum.
-      uint64_t rs2[2] = {0, 0};
+      // uses the exact sum. Each rounded weight enters the sum through one f32 + bf16 add (four
+      // chains), without unpacking it first.
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < kN / 2; ++u)
-        rs2[u & 1] = add2(rs2[u & 1], f2pack(bf16lo(pk[u]), bf16hi(pk[u])));
-      float a0, a1, b0, b1;
-      f2unpack(add2(rs2[0], rs2[1]), a0, a1);
+      for (int u = 0; u < kN / 2; ++u) add_bf16x2(rs[2 * (u & 1)], rs[2 * (u & 1) + 1], pk[u]);
+      float b0, b1;
       f2unpack(add2(re2[0], re2[1]), b0, b1);
-      l_run = l_run * alpha + (a0 + a1);
+      l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
       l_exact = l_exact * alpha + (b0 + b1);
       m_run = m_use;
     }
