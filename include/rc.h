@@ -288,7 +288,8 @@ int rc_kv_copy(const rc_kv_copy_args* args, void* stream);
  *   q [T, Hq, d], k_new / v_new [T, Hkv, d], o [T, Hq, d] in dtype; lse [T, Hq] fp32 natural log
  *   of the softmax denominator of the scaled scores (optional, NULL to skip); out_loc [T],
  *   qo_indptr [B+1], prefix_len [B], req_idx [B] device int32. bf16 requires head_dim 128
- *   (tensor-core path); f32 takes head_dim 64 or 128. Requests may have S = 0. */
+ *   (tensor-core path); f32 takes head_dim 64 or 128. Requests may have S = 0. q, k_new,
+ *   v_new, o and the pool planes are 16-byte aligned (RC_ERR_INVALID otherwise). */
 typedef struct rc_extend_args {
   int32_t dtype;
   int32_t num_reqs;

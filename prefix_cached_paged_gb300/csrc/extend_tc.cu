@@ -37,6 +37,9 @@
 //                grows by more than 8 in log2 units); weights rounded to bf16, normalised by
 //                the sum of the rounded weights; epilogue O / l.
 // Every mbarrier wait is bounded; on expiry the kernel records a status code and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "device_common.cuh"
 #include "extend_common.h"
 #include "host_common.h"
@@ -93,6 +96,7 @@ struct SmemLayout {
 static_assert(SmemLayout::ALLOC <= 232448, "shared memory budget");
 
 struct TcParams {
+  CUtensorMap tmap_q;   // q as (head_dim, heads, tokens), boxes of 64 x G x 128 / G, 128-byte swizzle
   rc_extend_args a;
   int* status;
   int ppt;           // query positions per tile
@@ -145,13 +149,16 @@ __device__ __forceinline__ int fold_tiles(const rc_extend_args& a, int r, int qo
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// 16-byte copy that reads `bytes` (0 or 16) from global memory and zero-fills the rest
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// one box of a 3-D tensor map into shared memory, completing bytes on `bar`
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ uint64_t f2pack(float a, float b) {
   uint64_t r;
@@ -497,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // TMEM lane of a query tile's first row: a tile of at most 96 rows starts at lane 32, so that
   // lane quadrant 0 holds no rows. Its softmax warps share a sub-partition with the MMA warp,
   // and a busy warp there slows the MMA warp's issue (measured: one tcgen05.mma per ~89 cycles
-  // with idle neighbours, ~123 with one arithmetic-bound warp beside it, ~159 with two).
-  const int shA = nposA * G <= 96 ? 32 : 0;
-  const int shB = nposB * G <= 96 ? 32 : 0;
+  // with idle neighbours, ~123 with one arithmetic-bound warp beside it, ~159 with two). The
+  // Q box then starts 32 / G positions early, so G must divide 32.
+  const bool can_shift = 32 % G == 0;
+  const int shA = can_shift && nposA * G <= 96 ? 32 : 0;
+  const int shB = can_shift && nposB * G <= 96 ? 32 : 0;
   const int n_pre = (P - kstart + kN - 1) / kN;     // prefix key tiles: keys [kstart, P)
   // key tiles of each query tile: the prefix, then (per-request pass) new-token keys up to its
   // last position
@@ -549,10 +558,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       mbar_init(&o_done[s], 1);
     }
     mbar_init(e_done, 2 * kGroupThreads);
-    mbar_init(q_full, kThreads);
+    mbar_init(q_full, 1);
     mbar_init(drain, 1);
     *mma_done = 0;
     fence_mbar_init();
+    // Q tiles: smem row (= TMEM lane) m of tile X holds position iX + (m - shX) / G, head
+    // hk * G + m % G -- one TMA box of 128 / G positions x G heads per 64-column block, starting
+    // shX / G positions early. Rows outside the tile hold other tokens' queries, or zeros past
+    // either end of the batch; their results are never stored. The MMA warp waits on q_full.
+    const int nq = nposB > 0 ? 2 : 1;
+    mbar_arrive_expect_tx(q_full, nq * (kM / G) * G * kD * 2);
+    for (int X = 0; X < nq; ++X) {
+      const int z = qo + (X ? iB : iA) - (X ? shB : shA) / G;
+      for (int blk = 0; blk < 2; ++blk)
+        tma_load_3d(sQ + X * kTileBytes + blk * kBlockBytes, &p.tmap_q, blk * 64, hk * G, z,
+                    smem_u32(q_full));
+    }
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
@@ -657,30 +678,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   // stage 0 is free at the start: the first key tile's copies go out before the setup barrier
   if (producer && ntiles > 0) copy_tile(0, rowptr(0, 0, raw(0, 0)), rowptr(0, 1, raw(0, 1)));
 
-  // Q tiles: smem row (= TMEM lane) m of tile X holds tile row m - shX = (position
-  // iX + row / G, head hk * G + row % G); rows outside the tile are zero-filled. Copied
-  // asynchronously (every thread, 16 bytes at a time); the MMA warp waits on q_full, so the
-  // copies overlap TMEM allocation and the first K/V loads.
-  {
-    const __nv_bfloat16* q = (const __nv_bfloat16*)a.q;
-    const uint32_t sQ0 = smem_u32(smem) + SmemLayout::Q;
-    static_assert(2 * kM * 16 % kThreads == 0, "every Q chunk is copied");
-#pragma unroll
-    for (int k = 0; k < 2 * kM * 16 / kThreads; ++k) {
-      const int e = threadIdx.x + k * kThreads;
-      const int X = e >> 11, m = (e >> 4) & 127, c = e & 15;
-      const int i0 = X ? iB : iA, np = X ? nposB : nposA;
-      const int mr = m - (X ? shB : shA);           // tile row held by smem row m
-      const __nv_bfloat16* src = q;
-      uint32_t bytes = 0;
-      if (mr >= 0 && mr < np * G) {
-        const int i = i0 + mr / G, hh = mr % G;
-        src = q + ((int64_t)(qo + i) * Hq + hk * G + hh) * kD + c * 8;
-        bytes = 16;
-      }
-      cp_async16_zfill(sQ0 + X * kTileBytes + sw128_off(m, c), src, bytes);
-    }
-  }
   // the folded pass's remainder-tile map: one thread walks the CTA's members (its loads overlap
   // the other threads' first copies)
   if (fold && threadIdx.x == kThreads - 1) {
@@ -696,7 +693,6 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();   // barrier initialisation and the TMEM address are visible from here
   tc_fence_after();
-  cp_async_arrive_noinc(smem_u32(q_full));
   const uint32_t tmem = *tmem_slot;
   // register split (each role branch starts with its setmaxnreg, so that its code is compiled
   // for its own budget): launched with kRegsLaunch per thread; the control warpgroup (warps 0-3)
@@ -751,8 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
         if (last) mma_commit_by(smem_u32(&v_empty[st]), leader);
         return true;
       };
-      bool ok = wait_lim(q_full, 0, p.status, lim);
-      fence_async_smem();   // Q arrived through the generic proxy (cp.async)
+      bool ok = wait_lim(q_full, 0, p.status, lim);   // Q by TMA: the async proxy already
       if (ok) ok = qk(0, 0);
       if (ok && nt1 > 0) ok = qk(1, 0);
       for (int t = 0; t < max(nt0, nt1) && ok; ++t) {
@@ -771,13 +766,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
       // (this wait keeps the full bound whatever the launch's: it guards the deallocation)
       mma_commit_by(smem_u32(drain), leader);
       mbar_wait(drain, 0, p.status);
+      // the Q boxes have landed before the CTA exits, also when the wait above for them gave up
+      mbar_wait(q_full, 0, p.status);
     }
     __syncwarp();
   } else if (warp < kScatterWarp0) {
     // ------------------------------------------------------------ producers (K: warps 1-2, V: 3-4)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-    // tile 0 was issued before the barrier; its arrival (which also covers this thread's Q
-    // chunks) can only follow the barrier initialisation
+    // tile 0 was issued before the barrier; its arrival can only follow the barrier
+    // initialisation
     bool ok = true;
     if (ntiles > 0) cp_async_arrive_noinc(smem_u32(&full[0]));
     int n0 = ntiles > 1 ? raw(1, 0) : 0, n1 = ntiles > 1 ? raw(1, 1) : 0;
@@ -1097,10 +1094,26 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(const __grid_con
 
 }  // namespace
 
+// The driver's tensor-map encoder, looked up once per process through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return (PFN_cuTensorMapEncodeTiled_v12000)f;
+  }();
+  return fn;
+}
+
 int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
   if (a->head_dim != kD) return fail(RC_ERR_INVALID, "extend (tensor cores): head_dim must be 128");
   const int G = a->num_q_heads / a->num_kv_heads;
   if (G > kM) return fail(RC_ERR_INVALID, "extend (tensor cores): group size %d > 128", G);
+  if (((uintptr_t)a->q & 15) != 0)
+    return fail(RC_ERR_INVALID, "extend (tensor cores): q must be 16-byte aligned");
   // per instantiation and device: opt in to the shared memory, and check that the launch
   // allocation covers the register split (the softmax warpgroups' setmaxnreg.inc would never
   // return)
@@ -1131,6 +1144,23 @@ int launch_extend_tc(const rc_extend_args* a, int* status, cudaStream_t s) {
       return fail(RC_ERR_CUDA, "extend (tensor cores): kernel built with %d registers per "
                   "thread, the register split needs %d", regs, kRegsLaunch);
   TcParams p;
+  // q [T, Hq, 128] bf16 as a 3-D tensor (columns, heads, tokens); one box is the 64-column block
+  // of 128 / G positions x the G heads of a query tile
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(RC_ERR_CUDA, "extend (tensor cores): no tensor-map encoder in the driver");
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)a->num_q_heads,
+                                (cuuint64_t)(a->num_tokens > 0 ? a->num_tokens : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)a->num_q_heads * kD * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kM / G)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = encode(&p.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a->q),
+                              dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(RC_ERR_CUDA, "extend (tensor cores): tensor map for q (error %d)", (int)r);
+  }
   p.a = *a;
   p.status = status;
   p.ppt = kM / G;
