@@ -144,6 +144,26 @@ def test_extend_bf16_ragged_all_units(Hq, Hkv):
     _status_clear()
 
 
+PAIRS_WIDE = [(0, 1), (37, 64), (130, 129), (2, 257), (255, 1)]
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 2), (32, 2), (64, 2), (128, 2)])
+def test_extend_bf16_group_sizes(Hq, Hkv):
+    """Query tiles of 128 / G positions x G heads for G = 3 (42 positions, 126 rows; no lane
+    shift, as 3 does not divide 32), 16 and 32 (ragged tiles start 2 and 1 positions early, at
+    TMEM lane 32) and 64 (two positions per tile; no lane shift): every unit within tolerance."""
+    w = _custom_extend(Hq, Hkv, PAIRS_WIDE, seed=13)
+    eng = H.make_engine(w)
+    H.run_cache_phase(eng, w.model, w.phases[0].seqs)
+    seqs = w.phases[1].seqs
+    b, outs = H.run_extend_phase(eng, w.model, seqs, lse=True)
+    assert b.plan.prefix_len.tolist() == [min(p, p + s - 1) for p, s in PAIRS_WIDE]
+    units = [(i, 0, h) for i in range(len(seqs)) for h in range(Hkv)]
+    _check_extend(w, b, outs, seqs, units)
+    _check_scatter(eng, w, seqs, b)
+    _status_clear()
+
+
 def _sample_units(rng, n_req, layers, n_kv, k):
     """k distinct (request, layer, KV head) units (all of them if there are fewer)."""
     k = min(k, n_req * layers * n_kv)
