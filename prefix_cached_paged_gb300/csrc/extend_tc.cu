@@ -20,6 +20,9 @@
 // outputs (fp32). The bf16 weights P overwrite the first 64 columns of the scores they came from
 // (two weights per 32-bit column) and feed P.V straight from TMEM as the A operand.
 //
+// The two Q tiles arrive by TMA (one tensor box of 64 columns x G heads x 128 / G positions per
+// 64-column block, 128-byte swizzled), issued by thread 0 right after the barrier set-up.
+//
 // Warp roles (512 threads):
 //   warp 0       allocates TMEM and issues every tcgen05.mma from one lane;
 //   warps 1-4    producers, two for K and two for V, each filling half of a key tile's rows
